@@ -1,0 +1,179 @@
+"""Seeded synthetic inputs for the quantization workloads.
+
+This module is the one piece shared by the CUDA path's tests/benchmark and the
+CPU oracle: it only draws random numbers and rounds them to bf16 bit patterns.
+It holds none of the quantization arithmetic (no scales, no FP8 codes, no
+SwiGLU).  Every array it returns is host memory (numpy).
+
+Rows are generated in fixed chunks of ``CHUNK_ROWS`` rows, each chunk from its
+own PCG64 stream keyed by (seed, workload, chunk index).  The result does not
+depend on how many threads generate it, and a workload cut to fewer rows is a
+prefix of the full-size workload.
+
+Workloads (all seeded, no dataset involved):
+
+* ``plain_small``   bf16 [1024, 4096], N(0, 1).
+* ``plain_outlier`` bf16 [8192, 7168], N(0, 1); 0.1% of the entries, chosen by
+  the generator, multiplied by 100; rows 0, 1024, 2048, ... all zero.
+* ``swiglu``        bf16 [16384, 4096] = gate | up with gate ~ N(0, 2) (standard
+  deviation 2) and up ~ N(0, 1); H = 2048.
+* ``swiglu_moe``    bf16 [65536, 4096] N(0, 1) (8192 tokens x top-8 rows) and
+  a fp32 routing weight per row: Uniform(0.01, 1) normalised over the 8 rows of
+  each token.
+* ``swiglu_t``      bf16 [131072, 4096] N(0, 1), for the cast + transposed cast.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+CHUNK_ROWS = 1024
+
+WORKLOADS = {
+    # name: (rows, cols, description)
+    "plain_small": (1024, 4096, "per_token_cast E4M3, x bf16 [1024, 4096] ~ N(0,1)"),
+    "plain_outlier": (8192, 7168, "per_token_cast E4M3/E5M2, x bf16 [8192, 7168] ~ N(0,1), "
+                                  "0.1% outliers x100, one all-zero row per 1024"),
+    "swiglu": (16384, 4096, "swiglu + per-token E4M3 cast, bf16 [16384, 4096] "
+                            "gate~N(0,2) | up~N(0,1), H=2048"),
+    "swiglu_moe": (65536, 4096, "swiglu x routing weight + per-token E4M3 cast, "
+                                "bf16 [65536, 4096] ~ N(0,1), 8192 tokens x top-8, H=2048"),
+    "swiglu_t": (131072, 4096, "swiglu + per-token E4M3 cast + transposed cast, "
+                               "bf16 [131072, 4096] ~ N(0,1), H=2048"),
+}
+
+_WORKLOAD_IDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
+
+
+def rng_for(*key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(k) for k in key])))
+
+
+def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """Round binary32 values to bf16 (nearest, ties to even); return uint16 bits.
+    Inputs must be finite.  Works on a copy."""
+    u = np.array(v, dtype=np.float32, order="C", copy=True).view(np.uint32)
+    _round_inplace(u)
+    return np.ascontiguousarray(u.view(np.uint16)[..., 1::2]) if u.ndim else \
+        np.uint16(int(u) >> 16)
+
+
+def _round_inplace(u: np.ndarray) -> None:
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+
+
+def _to_bf16_into(v: np.ndarray, dst: np.ndarray) -> None:
+    """Round float32 ``v`` (modified in place) to bf16 bits written into ``dst``."""
+    u = v.view(np.uint32)
+    _round_inplace(u)
+    dst[...] = u.view(np.uint16)[..., 1::2]
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def _chunked(T: int, fill) -> None:
+    """Run fill(chunk_index, row_begin, row_end) over fixed row chunks.  Each fill
+    draws a whole chunk's worth of numbers and keeps the rows it needs, so a
+    short last chunk holds the same values as the full workload's chunk."""
+    n = -(-T // CHUNK_ROWS)
+    if n <= 1:
+        for i in range(n):
+            fill(i, 0, T)
+        return
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(lambda i: fill(i, i * CHUNK_ROWS, min(T, (i + 1) * CHUNK_ROWS)), range(n)))
+
+
+def normal_bf16(seed: int, stream: int, T: int, C: int, std: float = 1.0) -> np.ndarray:
+    """bf16 bits of a [T, C] matrix of N(0, std^2) samples."""
+    out = np.empty((int(T), int(C)), np.uint16)
+
+    def fill(i, a, b):
+        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
+        if std != 1.0:
+            v *= np.float32(std)
+        _to_bf16_into(v, out[a:b])
+
+    _chunked(int(T), fill)
+    return out
+
+
+def outlier_bf16(seed: int, stream: int, T: int, C: int, frac: float = 1e-3,
+                 factor: float = 100.0, zero_row_every: int = 1024) -> np.ndarray:
+    """N(0,1) with a fraction ``frac`` of entries, chosen by the generator,
+    multiplied by ``factor`` and every ``zero_row_every``-th row (from row 0) zero."""
+    out = np.empty((int(T), int(C)), np.uint16)
+
+    def fill(i, a, b):
+        rng = rng_for(seed, stream, i)
+        v = rng.standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
+        mask = rng.random((CHUNK_ROWS, C), dtype=np.float32)[:b - a] < np.float32(frac)
+        v[mask] *= np.float32(factor)
+        _to_bf16_into(v, out[a:b])
+
+    _chunked(int(T), fill)
+    if zero_row_every:
+        out[::zero_row_every] = 0
+    return out
+
+
+def swiglu_bf16(seed: int, stream: int, T: int, H: int, gate_std: float = 1.0,
+                up_std: float = 1.0) -> np.ndarray:
+    """bf16 bits of a [T, 2H] gate | up matrix."""
+    out = np.empty((int(T), 2 * int(H)), np.uint16)
+
+    def fill(i, a, b):
+        rng = rng_for(seed, stream, i)
+        g = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[:b - a]
+        if gate_std != 1.0:
+            g *= np.float32(gate_std)
+        u = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[:b - a]
+        if up_std != 1.0:
+            u *= np.float32(up_std)
+        _to_bf16_into(g, out[a:b, :H])
+        _to_bf16_into(u, out[a:b, H:])
+
+    _chunked(int(T), fill)
+    return out
+
+
+def routing_weights(seed: int, stream: int, tokens: int, topk: int = 8) -> np.ndarray:
+    """fp32 [tokens * topk]: Uniform(0.01, 1) normalised over each token's rows."""
+    raw = rng_for(seed, stream, 1 << 20).uniform(0.01, 1.0, size=(int(tokens), int(topk)))
+    w = raw / raw.sum(axis=1, keepdims=True)
+    return np.ascontiguousarray(w.astype(np.float32).reshape(-1))
+
+
+def workload(name: str, seed: int = 0, rows: int | None = None) -> dict:
+    """Inputs of a named workload: dict with ``x`` (uint16 bf16 bits, row-major)
+    and, for the weighted SwiGLU, ``w`` (fp32, one per row).  ``rows`` cuts the
+    workload to its first rows (same distribution), which quick tests use."""
+    if name not in WORKLOADS:
+        raise KeyError(name)
+    T, C, _ = WORKLOADS[name]
+    if rows is not None:
+        T = int(rows)
+    sid = _WORKLOAD_IDS[name]
+    if name == "plain_small":
+        return {"x": normal_bf16(seed, sid, T, C)}
+    if name == "plain_outlier":
+        return {"x": outlier_bf16(seed, sid, T, C)}
+    if name == "swiglu":
+        return {"x": swiglu_bf16(seed, sid, T, C // 2, gate_std=2.0, up_std=1.0)}
+    if name == "swiglu_moe":
+        topk = 8
+        w = routing_weights(seed, sid, -(-T // topk), topk)[:T]
+        return {"x": swiglu_bf16(seed, sid, T, C // 2), "w": np.ascontiguousarray(w)}
+    if name == "swiglu_t":
+        return {"x": swiglu_bf16(seed, sid, T, C // 2)}
+    raise KeyError(name)

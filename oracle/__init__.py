@@ -1,0 +1,315 @@
+"""CPU oracle for per-token-group FP8 activation quantization.
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm are the only code allowed to import
+this package.  The product path (the CUDA library and its Python binding)
+never imports, links or calls it, and this package never imports the product.
+
+The arithmetic lives in ``tkq_oracle.c`` (plain single-threaded C, binary32
+steps in round-to-nearest-even, compiled without FMA contraction); this module
+only builds it with gcc and marshals numpy arrays through ctypes.  bf16 inputs
+are passed as ``uint16`` bit patterns; codes come back as ``uint8``.
+
+Sources: the TileKernels walkthrough "DeepSeek开源TileKernels：用Python写的GPU
+算子逼近硬件性能上限" (itsolotime.com) §3.1-§3.3, the operator table of
+"TileKernels 与 DeepGEMM 的分界线" (chatdocs.ruinique.com) §2, and the quant/
+section of "刚刚！DeepSeek开源高性能GPU算子库TileKernels" (info.datadowell.com).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+E4M3 = 0
+E5M2 = 1
+FMT = {"e4m3": E4M3, "e5m2": E5M2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tkq_oracle.c")
+_LIB = os.path.join(_HERE, "libtkq_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``tkq_oracle.c`` into ``libtkq_oracle.so`` next to it."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= max(
+            os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "tkq_oracle.h"))):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    if verbose:
+        print(" ".join(cmd))
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def build_variant(src_text: str, out_dir: str) -> str:
+    """Compile a modified copy of the oracle source (used by the mutation tests
+    that show the pins reject a planted mistake) and return the library path."""
+    src = os.path.join(out_dir, "tkq_oracle.c")
+    with open(src, "w") as f:
+        f.write(src_text)
+    hdr = os.path.join(out_dir, "tkq_oracle.h")
+    with open(os.path.join(_HERE, "tkq_oracle.h")) as f, open(hdr, "w") as g:
+        g.write(f.read())
+    lib = os.path.join(out_dir, "libtkq_oracle_variant.so")
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                    "-fPIC", "-shared", "-o", lib, src, "-lm"], check=True)
+    return lib
+
+
+class use_library:
+    """Context manager: route every call of this module to another build of the
+    oracle (a planted-mistake variant) and restore the real one afterwards."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        _load()
+        with _lock:
+            self.saved = _lib
+            _lib = _configure(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
+        return False
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _configure(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _configure(lib):
+    """Declare the C signatures on a freshly loaded oracle library."""
+    p = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    i = ctypes.c_int
+    lib.ora_fp8_max.argtypes = [i]
+    lib.ora_fp8_max.restype = ctypes.c_double
+    lib.ora_fp8_decode.argtypes = [ctypes.c_uint8, i]
+    lib.ora_fp8_decode.restype = ctypes.c_double
+    lib.ora_fp8_encode.argtypes = [ctypes.c_float, i]
+    lib.ora_fp8_encode.restype = ctypes.c_uint8
+    lib.ora_fp8_encode_array.argtypes = [p, i64, i, p]
+    lib.ora_fp8_encode_array.restype = ctypes.c_int
+    lib.ora_group_scale.argtypes = [ctypes.c_float, i]
+    lib.ora_group_scale.restype = ctypes.c_float
+    lib.ora_per_token_cast.argtypes = [p, i64, i64, i64, i, p, p]
+    lib.ora_cast_rows_f32.argtypes = [p, i64, i64, i64, i, p, p]
+    lib.ora_cast_cols_f32.argtypes = [p, i64, i64, i64, i, p, p]
+    lib.ora_swiglu_values.argtypes = [p, p, i64, i64, p]
+    lib.ora_swiglu_cast.argtypes = [p, p, i64, i64, i64, i, p, p]
+    lib.ora_swiglu_cast_t.argtypes = [p, p, i64, i64, i64, i, p, p, p, p]
+    for f in ("ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
+              "ora_swiglu_values", "ora_swiglu_cast", "ora_swiglu_cast_t"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def _fmt(fmt) -> int:
+    return FMT[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what}: invalid arguments")
+
+
+# --------------------------------------------------------------------------
+# scalar codec
+# --------------------------------------------------------------------------
+
+def fp8_max(fmt) -> float:
+    return _load().ora_fp8_max(_fmt(fmt))
+
+
+def fp8_decode(code: int, fmt) -> float:
+    return _load().ora_fp8_decode(int(code) & 0xFF, _fmt(fmt))
+
+
+def fp8_encode(v: float, fmt) -> int:
+    return int(_load().ora_fp8_encode(float(np.float32(v)), _fmt(fmt)))
+
+
+def fp8_encode_array(v: np.ndarray, fmt) -> np.ndarray:
+    """Encode every binary32 value of ``v``."""
+    lib = _load()
+    flat = np.ascontiguousarray(v, dtype=np.float32).ravel()
+    out = np.empty(flat.shape, np.uint8)
+    _check(lib.ora_fp8_encode_array(_ptr(flat), flat.size, _fmt(fmt), _ptr(out)), "encode_array")
+    return out.reshape(np.shape(v))
+
+
+def group_scale(amax: float, fmt) -> np.float32:
+    return np.float32(_load().ora_group_scale(float(np.float32(amax)), _fmt(fmt)))
+
+
+# --------------------------------------------------------------------------
+# casts (rows are independent; ``threads`` splits row ranges across threads,
+# ctypes releases the GIL during each call)
+# --------------------------------------------------------------------------
+
+def _row_parallel(T: int, threads: int, body, align: int = 1):
+    threads = max(1, min(int(threads), max(1, T // max(align, 1))))
+    if threads == 1:
+        body(0, T)
+        return
+    per = -(-T // threads)
+    per = -(-per // align) * align
+    errs = []
+
+    def run(a, b):
+        try:
+            body(a, b)
+        except Exception as e:  # pragma: no cover - surfaced below
+            errs.append(e)
+
+    ts = [threading.Thread(target=run, args=(a, min(T, a + per)))
+          for a in range(0, T, per)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    if errs:
+        raise errs[0]
+
+
+def per_token_cast(x_bits: np.ndarray, fmt="e4m3", group: int = 128, threads: int = 1):
+    """x_bits: uint16 [T, C] (bf16 bits) -> (codes uint8 [T, C], sf float32 [T, C/group])."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, C = x_bits.shape
+    if group <= 0 or C % group:
+        raise ValueError("group must divide C")
+    out = np.empty((T, C), np.uint8)
+    sf = np.empty((T, C // group), np.float32)
+    f = _fmt(fmt)
+
+    def body(a, b):
+        _check(lib.ora_per_token_cast(_ptr(x_bits[a:b]), b - a, C, group, f,
+                                      _ptr(out[a:b]), _ptr(sf[a:b])), "per_token_cast")
+
+    _row_parallel(T, threads, body)
+    return out, sf
+
+
+def cast_rows_f32(y: np.ndarray, fmt="e4m3", group: int = 128):
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, C = y.shape
+    out = np.empty((T, C), np.uint8)
+    sf = np.empty((T, C // group), np.float32)
+    _check(lib.ora_cast_rows_f32(_ptr(y), T, C, group, _fmt(fmt), _ptr(out), _ptr(sf)),
+           "cast_rows_f32")
+    return out, sf
+
+
+def cast_cols_f32(y: np.ndarray, fmt="e4m3", group: int = 128):
+    """fp32 [T, C] -> (codes [C, T], sf_t [C, T/group]) with groups along tokens."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, C = y.shape
+    out_t = np.empty((C, T), np.uint8)
+    sf_t = np.empty((C, T // group), np.float32)
+    _check(lib.ora_cast_cols_f32(_ptr(y), T, C, group, _fmt(fmt), _ptr(out_t), _ptr(sf_t)),
+           "cast_cols_f32")
+    return out_t, sf_t
+
+
+def swiglu_values(x_bits: np.ndarray, w: np.ndarray | None = None, threads: int = 1):
+    """x_bits: uint16 [T, 2H] (gate | up) -> fp32 y [T, H]."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    y = np.empty((T, H), np.float32)
+
+    def body(a, b):
+        _check(lib.ora_swiglu_values(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                     b - a, H, _ptr(y[a:b])), "swiglu_values")
+
+    _row_parallel(T, threads, body)
+    return y
+
+
+def swiglu_cast(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
+                group: int = 128, threads: int = 1):
+    """-> (codes [T, H], sf [T, H/group])."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty((T, H), np.uint8)
+    sf = np.empty((T, H // group), np.float32)
+    f = _fmt(fmt)
+
+    def body(a, b):
+        _check(lib.ora_swiglu_cast(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                   b - a, H, group, f, _ptr(out[a:b]), _ptr(sf[a:b])),
+               "swiglu_cast")
+
+    _row_parallel(T, threads, body)
+    return out, sf
+
+
+def swiglu_cast_t(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
+                  group: int = 128, threads: int = 1):
+    """-> (codes [T, H], sf [T, H/group], codes_t [H, T], sf_t [H, T/group])."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    if T % group:
+        raise ValueError("T must be a multiple of group")
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty((T, H), np.uint8)
+    sf = np.empty((T, H // group), np.float32)
+    out_t = np.empty((H, T), np.uint8)
+    sf_t = np.empty((H, T // group), np.float32)
+    f = _fmt(fmt)
+    if threads <= 1:
+        _check(lib.ora_swiglu_cast_t(_ptr(x_bits), _ptr(w), T, H, group, f, _ptr(out),
+                                     _ptr(sf), _ptr(out_t), _ptr(sf_t)), "swiglu_cast_t")
+        return out, sf, out_t, sf_t
+
+    # Row blocks of `group` tokens are independent: run each block as its own
+    # oracle problem and scatter its column outputs into the [H, T] arrays.
+    def body(a, b):
+        n = b - a
+        o_t = np.empty((H, n), np.uint8)
+        s_t = np.empty((H, n // group), np.float32)
+        _check(lib.ora_swiglu_cast_t(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                     n, H, group, f, _ptr(out[a:b]), _ptr(sf[a:b]),
+                                     _ptr(o_t), _ptr(s_t)), "swiglu_cast_t")
+        out_t[:, a:b] = o_t
+        sf_t[:, a // group:b // group] = s_t
+
+    _row_parallel(T, threads, body, align=group)
+    return out, sf, out_t, sf_t

@@ -1,0 +1,413 @@
+"""Pins for the CPU oracle (no GPU).
+
+The oracle is checked against things other than itself:
+* the FP8 decode of all 256 codes against torch's float8 dtypes (a library
+  routine) and against hand-worked code values;
+* the encoder against a brute-force nearest-value search over the 256 decoded
+  values (a different algorithm from the oracle's bit rounding), against torch's
+  round-to-nearest conversion in range, and against hand-worked points;
+* the group cast against hand-worked 1x128 groups (tests/golden);
+* invariants that hold for any input: sign symmetry, exact 2^k scale
+  equivariance, permutation equivariance, the half-spacing error bound, the
+  clamp floor, the amax element mapping to the largest code;
+* SwiGLU against a binary64 evaluation and torch's silu, the gate/up
+  orientation, w = 1 and zero-gate special cases;
+* the token-axis cast against the channel-axis cast of the explicit transpose.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_activation_quantization_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TORCH_FP8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+MAXCODE = {"e4m3": 0x7E, "e5m2": 0x7B}
+FMAX = {"e4m3": 448.0, "e5m2": 57344.0}
+MBITS = {"e4m3": 3, "e5m2": 2}
+EMIN = {"e4m3": -6, "e5m2": -14}
+FMTS = ["e4m3", "e5m2"]
+
+
+def torch_decode_all(fmt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(TORCH_FP8[fmt]).to(torch.float64).numpy()
+
+
+def _val(spec):
+    if isinstance(spec, dict):
+        (k, v), = spec.items()
+        f = np.float32(v)
+        return np.nextafter(f, np.float32(np.inf if k == "nextup" else -np.inf), dtype=np.float32)
+    if isinstance(spec, str):
+        return np.float32(float(spec))
+    return np.float32(spec)
+
+
+# ---------------------------------------------------------------------------
+# decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_decode_all_codes_match_torch(fmt):
+    ref = torch_decode_all(fmt)
+    got = np.array([oracle.fp8_decode(c, fmt) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_decode_hand_points():
+    pts = json.load(open(os.path.join(GOLDEN, "codec_points.json")))["decode"]
+    for fmt, code, val in pts:
+        got = oracle.fp8_decode(int(code, 16), fmt)
+        if val == "nan":
+            assert math.isnan(got), (fmt, code)
+        else:
+            exp = float(val)
+            assert got == exp and math.copysign(1, got) == math.copysign(1, exp), (fmt, code, got)
+
+
+def test_fp8_max():
+    assert oracle.fp8_max("e4m3") == 448.0 and oracle.fp8_max("e5m2") == 57344.0
+
+
+# ---------------------------------------------------------------------------
+# encode
+# ---------------------------------------------------------------------------
+
+def brute_force_encode(v: np.ndarray, fmt: str) -> np.ndarray:
+    """Nearest finite FP8 value by exhaustive search over the torch-decoded
+    table; ties go to the code with an even mantissa (even code); magnitudes at
+    or above the largest finite value saturate; NaN -> 0x7F; sign kept."""
+    table = torch_decode_all(fmt)
+    maxcode = MAXCODE[fmt]
+    pos_codes = np.arange(0, maxcode + 1)
+    pos_vals = table[pos_codes]
+    assert np.all(np.diff(pos_vals) > 0)
+    v = np.asarray(v, dtype=np.float32)
+    a = np.abs(v.astype(np.float64))
+    out = np.zeros(v.shape, np.uint8)
+    nan = np.isnan(v)
+    a_f = np.where(nan, 0.0, a)
+    # distance to every finite code (small tables: brute force is cheap)
+    res = np.empty(v.shape, np.int64)
+    B = 1 << 16
+    flat_a = a_f.ravel()
+    flat_res = res.ravel()
+    for s in range(0, flat_a.size, B):
+        d = np.abs(flat_a[s:s + B, None] - pos_vals[None, :])
+        best = d.min(axis=1, keepdims=True)
+        cand = d == best
+        # among the nearest, prefer an even code
+        even = cand & ((pos_codes[None, :] & 1) == 0)
+        pick = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+        flat_res[s:s + B] = pos_codes[pick]
+    res = flat_res.reshape(v.shape)
+    res = np.where(a_f >= FMAX[fmt], maxcode, res)
+    sign = np.signbit(v).astype(np.uint8) << 7
+    out[...] = (res | sign).astype(np.uint8)
+    out[nan] = 0x7F
+    return out
+
+
+def encode_test_points(fmt: str, n_random: int = 400_000, seed: int = 7) -> np.ndarray:
+    table = torch_decode_all(fmt)
+    pos = table[: MAXCODE[fmt] + 1].astype(np.float32)
+    mids = ((table[: MAXCODE[fmt]] + table[1: MAXCODE[fmt] + 1]) / 2).astype(np.float32)
+    extra = np.array([FMAX[fmt] * 1.03125, FMAX[fmt] * 1.0625, FMAX[fmt] * 1.07, FMAX[fmt] * 2,
+                      1e30, np.inf, 1e-45, 1e-40, 1.17549435e-38, 0.0], np.float32)
+    base = np.concatenate([pos, mids, extra])
+    pts = [base]
+    for k in (1, 2, 3):
+        up = base.copy()
+        dn = base.copy()
+        for _ in range(k):
+            up = np.nextafter(up, np.float32(np.inf), dtype=np.float32)
+            dn = np.nextafter(dn, np.float32(-np.inf), dtype=np.float32)
+        pts += [up, dn]
+    rng = np.random.default_rng(seed)
+    e = rng.integers(EMIN[fmt] - 14, int(math.log2(FMAX[fmt])) + 3, n_random)
+    m = rng.random(n_random) + 1.0
+    pts.append((m * np.exp2(e)).astype(np.float32))
+    bits = rng.integers(0, 2 ** 31 - 1, 50_000, dtype=np.int64).astype(np.uint32)
+    rnd = bits.view(np.float32)
+    pts.append(rnd[np.isfinite(rnd)])
+    allp = np.concatenate(pts)
+    allp = allp[~np.isnan(allp)]
+    return np.concatenate([allp, -allp])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_encode_matches_brute_force(fmt):
+    v = encode_test_points(fmt)
+    got = oracle.fp8_encode_array(v, fmt)
+    ref = brute_force_encode(v, fmt)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(v[i]), hex(got[i]), hex(ref[i])) for i in bad[:10]]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_encode_matches_torch_in_range(fmt):
+    v = encode_test_points(fmt, n_random=200_000, seed=11)
+    v = v[np.abs(v) <= FMAX[fmt]]
+    ref = torch.from_numpy(v).to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+    got = oracle.fp8_encode_array(v, fmt)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(float(v[i]), hex(got[i]), hex(ref[i])) for i in bad[:10]]
+
+
+def test_encode_hand_points():
+    pts = json.load(open(os.path.join(GOLDEN, "codec_points.json")))["encode"]
+    for fmt, val, code in pts:
+        v = _val(val)
+        assert oracle.fp8_encode(v, fmt) == int(code, 16), (fmt, val, float(v))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_encode_decode_roundtrip_all_codes(fmt):
+    table = torch_decode_all(fmt)
+    for c in range(256):
+        if not np.isfinite(table[c]):
+            continue
+        assert oracle.fp8_encode(np.float32(table[c]), fmt) == c, hex(c)
+
+
+# ---------------------------------------------------------------------------
+# group cast: hand-worked groups
+# ---------------------------------------------------------------------------
+
+def _bf16_exact(vals: np.ndarray) -> np.ndarray:
+    bits = synth.f32_to_bf16_bits(vals)
+    assert np.array_equal(synth.bf16_bits_to_f32(bits).view(np.uint32),
+                          vals.astype(np.float32).view(np.uint32)), "not bf16-exact"
+    return bits
+
+
+def test_hand_groups():
+    spec = json.load(open(os.path.join(GOLDEN, "hand_groups.json")))
+    G = spec["group"]
+    for case in spec["cases"]:
+        vals = np.full(G, case["fill"], np.float32)
+        for k, v in case["set"].items():
+            vals[int(k)] = np.float32(v)
+        bits = _bf16_exact(vals).reshape(1, G)
+        codes, sf = oracle.per_token_cast(bits, case["fmt"], G)
+        assert sf.shape == (1, 1)
+        assert hex(int(sf.view(np.uint32)[0, 0])) == case["scale_hex"], case["name"]
+        exp = np.full(G, int(case["code_fill"], 16), np.uint8)
+        for k, c in case["codes"].items():
+            exp[int(k)] = int(c, 16)
+        bad = np.nonzero(codes[0] != exp)[0]
+        assert bad.size == 0, (case["name"], [(int(i), hex(codes[0, i]), hex(exp[i])) for i in bad])
+
+
+# ---------------------------------------------------------------------------
+# group cast: invariants on seeded random data
+# ---------------------------------------------------------------------------
+
+def _random_bits(T=96, C=1024, seed=3, outliers=True):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((T, C)).astype(np.float32)
+    if outliers:
+        m = rng.random((T, C)) < 0.002
+        v[m] *= 300.0
+    v[5] = 0.0
+    v[6, :128] = np.float32(3e-5) * np.sign(v[6, :128])  # clamped group
+    return synth.f32_to_bf16_bits(v)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_negation_flips_only_sign(fmt):
+    x = _random_bits()
+    c1, s1 = oracle.per_token_cast(x, fmt)
+    c2, s2 = oracle.per_token_cast(x ^ np.uint16(0x8000), fmt)
+    assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+    assert np.array_equal(c2, c1 ^ np.uint8(0x80))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("k", [-7, 3])
+def test_power_of_two_scaling(fmt, k):
+    x = _random_bits(outliers=False, seed=5)
+    xf = synth.bf16_bits_to_f32(x)
+    xf = np.where(np.abs(xf) < 2.0 ** -60, np.float32(0), xf)  # keep far from bf16 underflow
+    x = synth.f32_to_bf16_bits(xf)
+    keep = np.ones(x.shape[0], bool)
+    keep[[5, 6]] = False  # zero / clamped rows change scale non-proportionally
+    x = x[keep]
+    xs = synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x) * np.float32(2.0 ** k))
+    assert np.array_equal(synth.bf16_bits_to_f32(xs), synth.bf16_bits_to_f32(x) * np.float32(2.0 ** k))
+    c1, s1 = oracle.per_token_cast(x, fmt)
+    c2, s2 = oracle.per_token_cast(xs, fmt)
+    assert np.array_equal(c1, c2)
+    assert np.array_equal(s2, s1 * np.float32(2.0 ** k))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_permutation_within_group(fmt):
+    x = _random_bits(seed=9)
+    T, C = x.shape
+    perm = np.random.default_rng(1).permutation(128)
+    xp = x.reshape(T, C // 128, 128)[:, :, perm].reshape(T, C)
+    c1, s1 = oracle.per_token_cast(x, fmt)
+    c2, s2 = oracle.per_token_cast(xp, fmt)
+    assert np.array_equal(s1, s2)
+    assert np.array_equal(c2, c1.reshape(T, C // 128, 128)[:, :, perm].reshape(T, C))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_scale_floor_amax_code_and_error_bound(fmt):
+    x = _random_bits(seed=13)
+    codes, sf = oracle.per_token_cast(x, fmt)
+    T, C = x.shape
+    G = C // 128
+    v = synth.bf16_bits_to_f32(x).astype(np.float64).reshape(T, G, 128)
+    s = sf.astype(np.float64).reshape(T, G, 1)
+    floor = np.float32(1e-4) / np.float32(FMAX[fmt])
+    assert np.all(sf >= floor)
+    amax = np.abs(v).max(axis=2)
+    # scale is amax / fmt_max to within half a binary32 ulp where not clamped
+    big = amax > 1e-4
+    rel = np.abs(sf.astype(np.float64)[big] * FMAX[fmt] - amax[big]) / amax[big]
+    assert rel.max() <= 2.0 ** -24 * 1.0001
+    # the element attaining amax gets the largest code
+    arg = np.abs(v).argmax(axis=2)
+    c = codes.reshape(T, G, 128)
+    top = np.take_along_axis(c, arg[..., None], axis=2)[..., 0]
+    assert np.all((top & 0x7F)[big] == MAXCODE[fmt])
+    # |dec(q) - v/s| <= half the FP8 spacing at v/s (+ the binary32 quotient rounding)
+    table = torch_decode_all(fmt)
+    dec = table[c]
+    q = v / s
+    e = np.floor(np.log2(np.maximum(np.abs(q), 1e-300)))
+    e = np.maximum(e, EMIN[fmt])
+    half = 0.5 * np.exp2(e - MBITS[fmt])
+    err = np.abs(dec - q)
+    assert np.all(err <= half * (1 + 2.0 ** -20) + np.abs(q) * 2.0 ** -23)
+
+
+def test_zero_row_and_signed_zero():
+    x = np.zeros((2, 256), np.uint16)
+    x[1, 3] = 0x8000  # -0.0
+    c, s = oracle.per_token_cast(x, "e4m3")
+    assert np.all(s == np.float32(1e-4) / np.float32(448))
+    assert c[1, 3] == 0x80 and np.count_nonzero(c) == 1
+
+
+# ---------------------------------------------------------------------------
+# token-axis cast
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_cols_equal_rows_of_transpose(fmt):
+    rng = np.random.default_rng(21)
+    y = rng.standard_normal((256, 384)).astype(np.float32) * np.float32(3)
+    y[:128, 7] = 0.0
+    y[128:, 9] *= np.float32(1e3)
+    ct, st = oracle.cast_cols_f32(y, fmt)
+    cr, sr = oracle.cast_rows_f32(np.ascontiguousarray(y.T), fmt)
+    assert ct.shape == (384, 256) and st.shape == (384, 2)
+    assert np.array_equal(ct, cr) and np.array_equal(st.view(np.uint32), sr.view(np.uint32))
+
+
+def test_cols_index_orientation():
+    # distinct column magnitudes: column c of the input is scaled by (c + 1),
+    # so sf_t[c, b] must grow with c; rows b*128.. share a scale per column
+    y = np.ones((256, 256), np.float32) * (np.arange(256, dtype=np.float32) + 1)[None, :]
+    y[128:] *= 2
+    _, st = oracle.cast_cols_f32(y, "e4m3")
+    exp0 = (np.arange(256, dtype=np.float32) + 1) / np.float32(448)
+    assert np.array_equal(st[:, 0], exp0)
+    assert np.array_equal(st[:, 1], ((np.arange(256, dtype=np.float32) + 1) * 2) / np.float32(448))
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU values
+# ---------------------------------------------------------------------------
+
+def _swiglu_input(T=64, H=256, seed=17, gate_std=2.0):
+    rng = np.random.default_rng(seed)
+    g = rng.standard_normal((T, H)).astype(np.float32) * np.float32(gate_std)
+    u = rng.standard_normal((T, H)).astype(np.float32)
+    x = np.concatenate([synth.f32_to_bf16_bits(g), synth.f32_to_bf16_bits(u)], axis=1)
+    return x
+
+
+def test_swiglu_vs_binary64():
+    x = _swiglu_input()
+    H = x.shape[1] // 2
+    w = np.random.default_rng(2).uniform(0.01, 1.0, x.shape[0]).astype(np.float32)
+    for ww in (None, w):
+        y = oracle.swiglu_values(x, ww).astype(np.float64)
+        f = synth.bf16_bits_to_f32(x).astype(np.float64)
+        g, u = f[:, :H], f[:, H:]
+        ref = g / (1.0 + np.exp(-g)) * u
+        if ww is not None:
+            ref = ref * ww.astype(np.float64)[:, None]
+        tol = 4 * 2.0 ** -24 * np.abs(ref) + 1e-38
+        assert np.all(np.abs(y - ref) <= tol)
+
+
+def test_swiglu_vs_torch_silu():
+    x = _swiglu_input(seed=23)
+    H = x.shape[1] // 2
+    y = oracle.swiglu_values(x)
+    f = torch.from_numpy(synth.bf16_bits_to_f32(x))
+    ref = (torch.nn.functional.silu(f[:, :H]) * f[:, H:]).numpy().astype(np.float64)
+    tol = 8 * 2.0 ** -24 * np.abs(ref) + 1e-38
+    assert np.all(np.abs(y.astype(np.float64) - ref) <= tol)
+
+
+def test_swiglu_orientation_and_special_cases():
+    H = 128
+    x = np.zeros((3, 2 * H), np.uint16)
+    g10 = synth.f32_to_bf16_bits(np.array([10.0], np.float32))[0]
+    one = synth.f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    mone = synth.f32_to_bf16_bits(np.array([-1.0], np.float32))[0]
+    x[0, 0], x[0, H] = g10, one          # gate 10, up 1 -> silu(10) ~ 9.9995
+    x[1, :H], x[1, H:] = 0, mone         # gate 0 -> 0 whatever up is
+    x[2, 0], x[2, H] = one, g10          # gate 1, up 10 -> 7.3106
+    y = oracle.swiglu_values(x)
+    assert abs(y[0, 0] - 10.0 / (1 + math.exp(-10.0))) < 1e-5
+    assert abs(y[2, 0] - 10.0 / (1 + math.exp(-1.0))) < 1e-5
+    assert np.all(y[1] == 0.0)
+    assert np.all(y[0, 1:] == 0.0)
+
+
+def test_swiglu_weight_one_and_weight_product():
+    x = _swiglu_input(seed=31)
+    T = x.shape[0]
+    y0 = oracle.swiglu_values(x)
+    y1 = oracle.swiglu_values(x, np.ones(T, np.float32))
+    assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32))
+    w = np.random.default_rng(4).uniform(0.01, 1.0, T).astype(np.float32)
+    yw = oracle.swiglu_values(x, w)
+    assert np.array_equal(yw.view(np.uint32), (y0 * w[:, None]).view(np.uint32))
+
+
+def test_swiglu_cast_t_consistency():
+    x = _swiglu_input(T=256, H=256, seed=41)
+    out, sf, out_t, sf_t = oracle.swiglu_cast_t(x)
+    o2, s2 = oracle.swiglu_cast(x)
+    assert np.array_equal(out, o2) and np.array_equal(sf, s2)
+    y = oracle.swiglu_values(x)
+    ct, st = oracle.cast_rows_f32(np.ascontiguousarray(y.T))
+    assert np.array_equal(out_t, ct) and np.array_equal(sf_t, st)
+    # threaded block split gives the same arrays
+    t4 = oracle.swiglu_cast_t(x, threads=2)
+    for a, b in zip((out, sf, out_t, sf_t), t4):
+        assert np.array_equal(a, b)
+
+
+def test_invalid_arguments_raise():
+    with pytest.raises(ValueError):
+        oracle.per_token_cast(np.zeros((2, 100), np.uint16))
+    with pytest.raises(ValueError):
+        oracle.swiglu_cast_t(np.zeros((100, 256), np.uint16))
