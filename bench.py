@@ -1,0 +1,554 @@
+"""Benchmark of the GB300 per-token FP8 activation quantization path.
+
+One step = one launch of the fused SwiGLU + per-token E4M3 cast + transposed
+cast (every step of the path: row-tile load, SwiGLU epilogue, group absmax,
+scale, FP8 pack, transposed copy) on the bf16 [131072, 4096] gate|up workload
+(H = 2048).  Inputs are resident in HBM when the timed region starts and are
+larger than L2 (1.07 GB per step), so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  Metric: HBM GB/s of algorithmic bytes (bytes
+read + bytes written), with the fraction of the measured HBM peak and rows/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--fmt e4m3|e5m2] [--no-extras]
+
+--impl reference times the CPU oracle (test infrastructure, plain C) on the
+host cores instead: the reference arm of this benchmark.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "fused SwiGLU+FP8 per-token cast HBM GB/s and % of GB300 peak; rows/sec"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "swiglu_t"
+
+# workload -> (kernel, rows, C or 2H, fmt list)
+KERNEL_OF = {
+    "plain_small": "per_token_cast",
+    "plain_outlier": "per_token_cast",
+    "swiglu": "swiglu_cast",
+    "swiglu_moe": "swiglu_cast",
+    "swiglu_t": "swiglu_cast_t",
+}
+KERNEL_SOURCES = {
+    "per_token_cast": ["per_token_cast.cu", "tkq_device.cuh"],
+    "swiglu_cast": ["swiglu_cast.cu", "tkq_device.cuh"],
+    "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh"],
+}
+
+
+def algorithmic_bytes(workload: str, T: int, C: int, weighted: bool) -> int:
+    """Bytes the operation must read and write once (per launch)."""
+    kern = KERNEL_OF[workload]
+    if kern == "per_token_cast":
+        return T * C * 2 + T * C + T * (C // 128) * 4
+    H = C // 2
+    b = T * 2 * H * 2 + T * H + T * (H // 128) * 4
+    if weighted:
+        b += T * 4
+    if kern == "swiglu_cast_t":
+        b += T * H + H * (T // 128) * 4
+    return b
+
+
+def kernel_source_hash(kern: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kern]:
+        with open(os.path.join(ROOT, "fp8_activation_quantization_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kern: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel and
+    workload, if the summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kern}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    s = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash(kern):
+        return None
+    return int(m.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        base = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                "-lms", "100"]
+        for cmd in ([base + ["-i", self.gpu_id]] if self.gpu_id else []) + [base]:
+            try:
+                self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
+                continue
+            time.sleep(0.3)
+            if self.proc.poll() is None:  # still sampling: the device filter was accepted
+                self.reader = threading.Thread(target=self._read, daemon=True)
+                self.reader.start()
+                break
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Problem:
+    """Device buffers + one launch closure for a named workload."""
+
+    def __init__(self, workload: str, fmt: str, dev, seed: int = 0):
+        import torch
+        import fp8_activation_quantization_gb300 as tkq
+        from fp8_activation_quantization_gb300 import synth
+        self.workload = workload
+        self.kern = KERNEL_OF[workload]
+        self.fmt = fmt
+        d = synth.workload(workload, seed=seed)
+        self.x_host = d["x"]
+        self.w_host = d.get("w")
+        self.T, self.C = self.x_host.shape
+        self.weighted = self.w_host is not None
+        self.bytes = algorithmic_bytes(workload, self.T, self.C, self.weighted)
+        self.dev = dev
+        self.x = torch.from_numpy(self.x_host.view(np.int16)).to(dev).view(torch.bfloat16)
+        self.w = None if self.w_host is None else torch.from_numpy(self.w_host).to(dev)
+        T, C = self.T, self.C
+        fcode = 0 if fmt == "e4m3" else 1
+        P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+        if self.kern == "per_token_cast":
+            self.out = torch.empty((T, C), dtype=torch.uint8, device=dev)
+            self.sf = torch.empty((T, C // 128), dtype=torch.float32, device=dev)
+            args = (P(self.x), P(self.out), P(self.sf), T, C, 128, fcode)
+            fn = tkq.tkq_per_token_cast
+            self.outputs = [self.out, self.sf]
+        else:
+            H = C // 2
+            self.out = torch.empty((T, H), dtype=torch.uint8, device=dev)
+            self.sf = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+            self.outputs = [self.out, self.sf]
+            if self.kern == "swiglu_cast":
+                args = (P(self.x), P(self.w), P(self.out), P(self.sf), T, H, 128, fcode)
+                fn = tkq.tkq_swiglu_cast
+            else:
+                self.out_t = torch.empty((H, T), dtype=torch.uint8, device=dev)
+                self.sf_t = torch.empty((H, T // 128), dtype=torch.float32, device=dev)
+                self.outputs += [self.out_t, self.sf_t]
+                args = (P(self.x), P(self.w), P(self.out), P(self.sf), P(self.out_t),
+                        P(self.sf_t), T, H, 128, fcode)
+                fn = tkq.tkq_swiglu_cast_t
+        self._fn, self._args = fn, args
+
+    def launch(self, stream):
+        st = self._fn(*self._args, ctypes.c_void_p(stream.cuda_stream))
+        if st:
+            raise RuntimeError(f"{self.kern} failed with status {st}")
+
+
+def time_steps(prob: Problem, steps: int, warmup: int, stream, barrier):
+    import torch
+    for _ in range(warmup):
+        prob.launch(stream)
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        prob.launch(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / 1000.0  # seconds
+
+
+def time_flushed(prob: Problem, reps: int, stream, flush):
+    """Median per-launch time with L2 flushed before each launch."""
+    import torch
+    ts = []
+    for i in range(reps + 3):
+        flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        prob.launch(stream)
+        e.record(stream)
+        e.synchronize()
+        if i >= 3:
+            ts.append(s.elapsed_time(e) / 1000.0)
+    return float(np.median(ts))
+
+
+def e2e_steps(prob: Problem, steps: int, stream):
+    """Metric through the public tensor API with host buffers: per step copy
+    the input from pinned host memory, run the op, copy every output back."""
+    import torch
+    import fp8_activation_quantization_gb300 as tkq
+    x_pin = torch.from_numpy(prob.x_host.view(np.int16)).pin_memory()
+    w_pin = None if prob.w_host is None else torch.from_numpy(prob.w_host).pin_memory()
+    outs_pin = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in prob.outputs]
+    x_dev = torch.empty_like(prob.x.view(torch.int16))
+    w_dev = None if w_pin is None else torch.empty_like(prob.w)
+    h2d = x_pin.numel() * 2 + (0 if w_pin is None else w_pin.numel() * 4)
+    d2h = sum(o.numel() * o.element_size() for o in prob.outputs)
+
+    def one():
+        x_dev.copy_(x_pin, non_blocking=True)
+        if w_dev is not None:
+            w_dev.copy_(w_pin, non_blocking=True)
+        xb = x_dev.view(torch.bfloat16)
+        fmt = prob.fmt
+        if prob.kern == "per_token_cast":
+            res = tkq.per_token_cast(xb, fmt, out=prob.outputs[0].view(_fp8(fmt)),
+                                     out_sf=prob.outputs[1])
+        else:
+            res = tkq.swiglu_forward_and_per_token_cast(
+                xb, fmt, topk_weights=w_dev, with_transpose=prob.kern == "swiglu_cast_t",
+                out=prob.outputs[0].view(_fp8(fmt)), out_sf=prob.outputs[1],
+                out_t=None if len(prob.outputs) < 3 else prob.outputs[2].view(_fp8(fmt)),
+                out_sf_t=None if len(prob.outputs) < 4 else prob.outputs[3])
+        for hp, dv in zip(outs_pin, res):
+            hp.copy_(dv.view(hp.dtype) if dv.dtype != hp.dtype else dv, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            one()
+        e.record(stream)
+        torch.cuda.synchronize()
+    dt = s.elapsed_time(e) / 1000.0
+    return dt, h2d, d2h
+
+
+def _fp8(fmt):
+    import torch
+    return torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+
+
+def cpu_baseline_single_thread(workload: str, fmt: str, rows: int = 32768):
+    """The oracle, as it stands, on one host core over the first `rows` rows."""
+    import oracle
+    from fp8_activation_quantization_gb300 import synth
+    d = synth.workload(workload, rows=rows)
+    x, w = d["x"], d.get("w")
+    T, C = x.shape
+    kern = KERNEL_OF[workload]
+    t0 = time.perf_counter()
+    if kern == "per_token_cast":
+        oracle.per_token_cast(x, fmt)
+    elif kern == "swiglu_cast":
+        oracle.swiglu_cast(x, w, fmt)
+    else:
+        oracle.swiglu_cast_t(x, w, fmt)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(workload, T, C, w is not None)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {T} rows of the {workload} workload ({b / 1e6:.0f} MB of "
+                      f"algorithmic bytes), single-threaded C oracle, {dt:.1f} s",
+            "rows_per_s": round(T / dt, 1)}
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = lambda: dist.barrier()
+    else:
+        barrier = lambda: None
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        barrier()
+    import fp8_activation_quantization_gb300 as tkq
+    tkq.load_library()
+    stream = torch.cuda.Stream(dev)
+    peak, peak_src = measured_peaks()
+
+    prob = Problem(args.workload, args.fmt, dev)
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    with torch.cuda.stream(stream):
+        with ClockSampler(uuid) as clk:
+            dt = time_steps(prob, args.steps, args.warmup, stream, barrier)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([dt], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    total_bytes = prob.bytes * args.steps * ws
+    gbs = total_bytes / dt / 1e9
+    per_launch = dt / args.steps
+    achieved = prob.bytes / per_launch / 1e9
+    rows_per_s = prob.T * args.steps * ws / dt
+
+    if rank != 0:
+        if ws > 1:
+            barrier()
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    res = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded bf16 N(0,1) gate|up, generated on the host)",
+        "config": {
+            "workload": _workload_desc(args.workload),
+            "T": prob.T, "cols": prob.C, "fmt": args.fmt, "group": 128,
+            "weighted": prob.weighted,
+            "algorithmic_bytes_per_step": prob.bytes,
+            "l2": "inputs larger than L2 (no flush between steps)"
+            if prob.bytes > 256e6 else "L2 flushed between launches",
+            "parallelism": f"replicas x{ws} (rows independent, no collective)",
+        },
+        "pct_of_peak": round(100.0 * gbs / ws / peak, 2),
+        "rows_per_s": round(rows_per_s, 1),
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "roofline": {
+            "bound": "hbm", "kernel": prob.kern,
+            "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(prob.kern, args.workload),
+            "algorithmic_bytes_per_launch": prob.bytes,
+            "peak_source": peak_src,
+        },
+    }
+    if prob.bytes < 256e6:
+        # small working sets: time launches individually with L2 flushed
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
+            t1 = time_flushed(prob, max(10, min(args.steps, 50)), stream, flush)
+        res["roofline"]["achieved"] = round(prob.bytes / t1 / 1e9, 2)
+        res["roofline"]["frac"] = round(prob.bytes / t1 / 1e9 / peak, 4)
+        res["roofline"]["timing"] = "median of L2-flushed single launches"
+    if not args.no_extras and ws == 1:
+        e_steps = max(3, min(args.steps, 20))
+        edt, h2d, d2h = e2e_steps(prob, e_steps, stream)
+        res["e2e"] = {"value": round(prob.bytes * e_steps / edt / 1e9, 2), "unit": "GB/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": round(edt / e_steps * 1e3, 3)}
+        res["cpu_baseline"] = cpu_baseline_single_thread(args.workload, args.fmt)
+        res["per_workload"] = other_workloads(dev, stream, peak, args)
+    print(json.dumps(res), flush=True)
+    if ws > 1:
+        barrier()
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def other_workloads(dev, stream, peak, args):
+    """Each kernel on every workload shape: median L2-flushed launch time."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, fmt in [("plain_small", "e4m3"), ("plain_outlier", "e4m3"), ("plain_outlier", "e5m2"),
+                      ("swiglu", "e4m3"), ("swiglu_moe", "e4m3"), ("swiglu_t", "e4m3")]:
+        prob = Problem(name, fmt, dev)
+        with torch.cuda.stream(stream):
+            t = time_flushed(prob, 20, stream, flush)
+        gbs = prob.bytes / t / 1e9
+        out[f"{name}/{fmt}"] = {"kernel": prob.kern, "us": round(t * 1e6, 2),
+                                "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                                "rows_per_s": round(prob.T / t, 1), "bytes": prob.bytes}
+        del prob
+        torch.cuda.empty_cache()
+    return out
+
+
+def _workload_desc(name):
+    from fp8_activation_quantization_gb300 import synth
+    return synth.WORKLOADS[name][2]
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from fp8_activation_quantization_gb300 import synth
+    oracle.build()
+    cores = max(1, os.cpu_count() or 1)
+    T_full, C, _ = synth.WORKLOADS[args.workload]
+    kern = KERNEL_OF[args.workload]
+    # calibrate: one 128-row block per core
+    rows = 128 * cores
+    d = synth.workload(args.workload, rows=min(T_full, 8192))
+    x_all, w_all = d["x"], d.get("w")
+
+    def step(r):
+        x = x_all[:r]
+        w = None if w_all is None else w_all[:r]
+        if kern == "per_token_cast":
+            oracle.per_token_cast(x, args.fmt, threads=cores)
+        elif kern == "swiglu_cast":
+            oracle.swiglu_cast(x, w, args.fmt, threads=cores)
+        else:
+            oracle.swiglu_cast_t(x, w, args.fmt, threads=cores)
+
+    t0 = time.perf_counter()
+    step(min(rows, x_all.shape[0]))
+    t_cal = time.perf_counter() - t0
+    per_row = t_cal / min(rows, x_all.shape[0])
+    budget = 150.0  # seconds for warmup + steps
+    r = int(budget / max(args.steps + args.warmup, 1) / per_row)
+    r = max(128, min(x_all.shape[0], (r // 128) * 128))
+    for _ in range(args.warmup):
+        step(r)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(r)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(args.workload, r, C, w_all is not None)
+    gbs = b * args.steps / dt / 1e9
+    res = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded bf16 N(0,1) gate|up, generated on the host)",
+        "config": {"workload": _workload_desc(args.workload), "T": T_full, "cols": C,
+                   "fmt": args.fmt, "group": 128},
+        "rows_per_s": round(r * args.steps / dt, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {r} rows of the workload per step, row blocks split "
+                                   f"over {cores} threads"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(KERNEL_OF))
+    ap.add_argument("--fmt", default="e4m3", choices=["e4m3", "e5m2"])
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip e2e, CPU baseline and the per-workload table")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+"""GB300-native per-token-group FP8 activation quantization.
+
+A thin ctypes binding over ``libtkq.so`` (C ABI in ``include/tkq.h``).  Every
+step of the computation runs in the library's CUDA kernels; this module only
+marshals pointers, sizes and the current CUDA stream, and allocates output
+tensors with PyTorch.  There is no CPU fallback: if the library is missing or a
+call fails, an exception is raised.
+
+Low-level names mirror the C ABI (``tkq_per_token_cast``, ``tkq_swiglu_cast``,
+``tkq_swiglu_cast_t``: raw device pointers, return the status code).  The
+tensor-level helpers follow the call shape of the TileKernels quant API
+(``per_token_cast(x, fmt='e4m3', num_per_channels=128) -> (out, out_sf)``,
+"DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件性能上限", quick start).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "TkqError", "library_path", "load_library", "tkq_per_token_cast", "tkq_swiglu_cast",
+    "tkq_swiglu_cast_t", "tkq_status_string", "per_token_cast",
+    "swiglu_forward_and_per_token_cast", "FMT_E4M3", "FMT_E5M2", "GROUP",
+]
+
+FMT_E4M3 = 0
+FMT_E5M2 = 1
+GROUP = 128
+_FMTS = {"e4m3": FMT_E4M3, "e5m2": FMT_E5M2}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libtkq.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class TkqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {tkq_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libtkq.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        p, i64, i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.tkq_per_token_cast.argtypes = [p, p, p, i64, i64, i, i, p]
+        lib.tkq_per_token_cast.restype = i
+        lib.tkq_swiglu_cast.argtypes = [p, p, p, p, i64, i64, i, i, p]
+        lib.tkq_swiglu_cast.restype = i
+        lib.tkq_swiglu_cast_t.argtypes = [p, p, p, p, p, p, i64, i64, i, i, p]
+        lib.tkq_swiglu_cast_t.restype = i
+        lib.tkq_status_string.argtypes = [i]
+        lib.tkq_status_string.restype = ctypes.c_char_p
+        lib.tkq_version.argtypes = []
+        lib.tkq_version.restype = i
+        _lib = lib
+        return lib
+
+
+def tkq_status_string(status: int) -> str:
+    return load_library().tkq_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------------------
+# C-ABI mirrors: raw device pointers (ints or None), sizes, stream handle.
+# ---------------------------------------------------------------------------
+
+def tkq_per_token_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, stream=None) -> int:
+    return load_library().tkq_per_token_cast(x, out, sf, T, C, group, fmt, stream)
+
+
+def tkq_swiglu_cast(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, stream=None) -> int:
+    return load_library().tkq_swiglu_cast(x, w, out, sf, T, H, group, fmt, stream)
+
+
+def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
+                      stream=None) -> int:
+    return load_library().tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group, fmt, stream)
+
+
+# ---------------------------------------------------------------------------
+# Tensor-level helpers (PyTorch supplies device memory and the stream).
+# ---------------------------------------------------------------------------
+
+def _fmt_code(fmt) -> int:
+    if isinstance(fmt, str):
+        if fmt not in _FMTS:
+            raise ValueError(f"unknown fmt {fmt!r}: expected 'e4m3' or 'e5m2'")
+        return _FMTS[fmt]
+    return int(fmt)
+
+
+def _fp8_dtype(fmt_code: int):
+    import torch
+    return torch.float8_e4m3fn if fmt_code == FMT_E4M3 else torch.float8_e5m2
+
+
+def _check_input(x, name="x"):
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous 2-D bfloat16 tensor")
+
+
+def _stream_handle(dev):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_sf=None):
+    """bf16 [T, C] -> (FP8 codes [T, C], fp32 scales [T, C/128])."""
+    import torch
+    _check_input(x)
+    f = _fmt_code(fmt)
+    T, C = x.shape
+    if out is None:
+        out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty((T, max(C // max(num_per_channels, 1), 0)), dtype=torch.float32,
+                             device=x.device)
+    with torch.cuda.device(x.device):
+        st = tkq_per_token_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
+                                _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_per_token_cast")
+    return out, out_sf
+
+
+def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP,
+                                      topk_weights=None, with_transpose: bool = False,
+                                      out=None, out_sf=None, out_t=None, out_sf_t=None):
+    """bf16 [T, 2H] (gate | up) -> (codes [T, H], scales [T, H/128]) and, with
+    ``with_transpose``, also (codes_t [H, T], scales_t [H, T/128]).
+    ``topk_weights``: optional fp32 [T] routing weight per row."""
+    import torch
+    _check_input(x)
+    f = _fmt_code(fmt)
+    T, H2 = x.shape
+    if H2 % 2:
+        raise ValueError("x must have an even number of columns (gate | up)")
+    H = H2 // 2
+    g = max(num_per_channels, 1)
+    if topk_weights is not None:
+        if (topk_weights.dtype != torch.float32 or topk_weights.numel() != T
+                or not topk_weights.is_contiguous() or topk_weights.device != x.device):
+            raise TypeError("topk_weights must be a contiguous fp32 tensor of T elements on x's device")
+    if out is None:
+        out = torch.empty((T, H), dtype=_fp8_dtype(f), device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty((T, H // g), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        stream = _stream_handle(x.device)
+        if not with_transpose:
+            st = tkq_swiglu_cast(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), T, H,
+                                 num_per_channels, f, stream)
+            if st:
+                raise TkqError(st, "tkq_swiglu_cast")
+            return out, out_sf
+        if out_t is None:
+            out_t = torch.empty((H, T), dtype=_fp8_dtype(f), device=x.device)
+        if out_sf_t is None:
+            out_sf_t = torch.empty((H, T // g), dtype=torch.float32, device=x.device)
+        st = tkq_swiglu_cast_t(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), _ptr(out_t),
+                               _ptr(out_sf_t), T, H, num_per_channels, f, stream)
+        if st:
+            raise TkqError(st, "tkq_swiglu_cast_t")
+        return out, out_sf, out_t, out_sf_t

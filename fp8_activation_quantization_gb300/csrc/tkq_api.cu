@@ -1,0 +1,161 @@
+// tkq_api.cu -- the C ABI of libtkq.so (declared in include/tkq.h): argument
+// validation, status codes and dispatch to the kernel launchers.  Nothing here
+// allocates device memory.
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+
+#include <cuda_runtime.h>
+
+#include "../../include/tkq.h"
+#include "tkq_internal.h"
+
+namespace tkq {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+Range span(const void* p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+}  // namespace
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (const char* env = std::getenv("TKQ_NUM_SMS")) {
+        const int v = std::atoi(env);
+        if (v > 0) return v;
+    }
+    if (dev < kMaxDevices) {
+        int v = g_sms[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        v = 1;
+    if (dev < kMaxDevices) g_sms[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+            cudaSuccess ||
+        per_sm <= 0)
+        per_sm = 1;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * per_sm;
+    const int64_t g = blocks_needed < cap ? blocks_needed : cap;
+    return static_cast<int>(g > 0 ? g : 1);
+}
+
+}  // namespace tkq
+
+namespace {
+
+tkq_status check_common(int64_t T, int64_t C, int group, int fmt) {
+    if (T < 0 || C <= 0) return TKQ_ERR_SHAPE;
+    if (group != 128) return TKQ_ERR_GROUP;
+    if (C % group) return TKQ_ERR_SHAPE;
+    if (fmt != TKQ_FMT_E4M3 && fmt != TKQ_FMT_E5M2) return TKQ_ERR_FMT;
+    // group indices are 32-bit in the SwiGLU kernel; 2^32 groups of 128 would
+    // be a 2 TiB input, far beyond one GPU
+    if (T > 0 && (T > (int64_t{1} << 40) || T * (C / group) >= (int64_t{1} << 32)))
+        return TKQ_ERR_SHAPE;
+    return TKQ_OK;
+}
+
+tkq_status launch_status(cudaError_t e) { return e == cudaSuccess ? TKQ_OK : TKQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+tkq_status tkq_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                              int group, int fmt, tkq_stream_t stream) {
+    tkq_status st = check_common(T, C, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
+               rs = tkq::span(sf, T * (C / group) * 4);
+    if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    return launch_status(tkq::launch_per_token_cast(x, out, sf, T, C, fmt,
+                                                    static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
+                           int64_t H, int group, int fmt, tkq_stream_t stream) {
+    tkq_status st = check_common(T, H, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4) ||
+        (w && !tkq::aligned(w, 4)))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * H * 4), ro = tkq::span(out, T * H),
+               rs = tkq::span(sf, T * (H / group) * 4);
+    if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    if (w) {
+        const auto rw = tkq::span(w, T * 4);
+        if (tkq::overlap(rw, ro) || tkq::overlap(rw, rs)) return TKQ_ERR_ALIAS;
+    }
+    return launch_status(tkq::launch_swiglu_cast(x, w, out, sf, T, H, fmt,
+                                                 static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
+                             float* sf_t, int64_t T, int64_t H, int group, int fmt,
+                             tkq_stream_t stream) {
+    tkq_status st = check_common(T, H, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (T % group) return TKQ_ERR_SHAPE;
+    if (T == 0) return TKQ_OK;
+    if (H > (int64_t{1} << 30)) return TKQ_ERR_SHAPE;
+    if (!x || !out || !sf || !out_t || !sf_t) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(out_t, 16) ||
+        !tkq::aligned(sf, 4) || !tkq::aligned(sf_t, 4) || (w && !tkq::aligned(w, 4)))
+        return TKQ_ERR_ALIGN;
+    const tkq::Range r[5] = {tkq::span(x, T * H * 4), tkq::span(out, T * H),
+                             tkq::span(sf, T * (H / group) * 4), tkq::span(out_t, T * H),
+                             tkq::span(sf_t, H * (T / group) * 4)};
+    for (int i = 0; i < 5; ++i)
+        for (int k = i + 1; k < 5; ++k)
+            if (tkq::overlap(r[i], r[k])) return TKQ_ERR_ALIAS;
+    if (w) {
+        const auto rw = tkq::span(w, T * 4);
+        for (int i = 1; i < 5; ++i)
+            if (tkq::overlap(rw, r[i])) return TKQ_ERR_ALIAS;
+    }
+    return launch_status(tkq::launch_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, fmt,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+const char* tkq_status_string(int status) {
+    switch (status) {
+        case TKQ_OK: return "TKQ_OK";
+        case TKQ_ERR_NULL: return "TKQ_ERR_NULL: a required pointer is NULL";
+        case TKQ_ERR_SHAPE: return "TKQ_ERR_SHAPE: invalid or unsupported extents";
+        case TKQ_ERR_GROUP: return "TKQ_ERR_GROUP: group must be 128";
+        case TKQ_ERR_FMT: return "TKQ_ERR_FMT: unknown FP8 format";
+        case TKQ_ERR_ALIGN: return "TKQ_ERR_ALIGN: misaligned pointer";
+        case TKQ_ERR_CUDA: return "TKQ_ERR_CUDA: kernel launch failed";
+        case TKQ_ERR_ALIAS: return "TKQ_ERR_ALIAS: buffers overlap";
+        default: return "TKQ_ERR_UNKNOWN";
+    }
+}
+
+int tkq_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,178 @@
+// tkq_device.cuh -- device building blocks shared by the quantization kernels.
+//
+// Everything here is per-element or per-group arithmetic of the per-token-group
+// FP8 cast described in "DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件
+// 性能上限" (itsolotime.com) §3.1-§3.3:
+//   scale  s = fl32(max(amax, 1e-4) / fmt_max)
+//   code   = saturating RNE FP8 code of fl32(y / s)
+//   SwiGLU y = (g / (1 + exp(-g))) * u [* w], binary32 steps.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace tkq {
+
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtE5M2 = 1;
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<kFmtE4M3> {
+    static constexpr float kMax = 448.0f;
+};
+template <>
+struct FmtTraits<kFmtE5M2> {
+    static constexpr float kMax = 57344.0f;
+};
+
+// ---------------------------------------------------------------------------
+// memory access
+// ---------------------------------------------------------------------------
+
+// 16-byte streaming load of read-only input: not kept in L1 (each byte is read
+// once by this kernel).
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float ld_stream_f32(const float* p) {
+    float r;
+    asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(r) : "l"(p));
+    return r;
+}
+
+// Streaming stores (.cs: the output is not read again by this kernel).
+__device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream(float* p, float v) {
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// bf16 -> fp32 (exact): a bf16 is the upper half of a binary32
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Eight bf16 packed in a uint4 -> eight floats, element order preserved.
+__device__ __forceinline__ void unpack8(const uint4& q, float* v) {
+    v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);
+    v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+    v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z);
+    v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+
+// ---------------------------------------------------------------------------
+// scale and quotient
+// ---------------------------------------------------------------------------
+
+// s = fl32(max(amax, 1e-4) / fmt_max) with an IEEE division, and the correctly
+// rounded reciprocal inv = fl32(1 / s).
+template <int FMT>
+__device__ __forceinline__ void group_scale(float amax, float& s, float& inv) {
+    s = __fdiv_rn(fmaxf(amax, 1e-4f), FmtTraits<FMT>::kMax);
+    inv = __frcp_rn(s);
+}
+
+// fl32(y / s) from inv = fl32(1/s): the product y*inv is within one ulp of the
+// quotient, and one Newton-Raphson residual step (Markstein's correction:
+// r = y - q0*s is exact with an FMA, q0 + r*inv rounds to the correctly
+// rounded quotient) recovers the IEEE result.  It holds whenever the residual
+// is a normal binary32, i.e. for every quotient large enough to give a
+// non-zero FP8 code; smaller quotients encode to a signed zero either way, and
+// copysign keeps that sign (s > 0, so sign(y / s) = sign(y)).
+__device__ __forceinline__ float quotient(float y, float s, float inv) {
+    const float q0 = __fmul_rn(y, inv);
+    const float r = __fmaf_rn(-q0, s, y);
+    const float q1 = __fmaf_rn(r, inv, q0);
+    return copysignf(q1, y);
+}
+
+// ---------------------------------------------------------------------------
+// FP8 packing: cvt.rn.satfinite converts two binary32 values to two FP8 codes
+// with round-to-nearest-even and saturation to the largest finite value.  The
+// first source operand lands in the upper byte, so operands are swapped to
+// keep element order in memory (byte 0 = first element).
+// ---------------------------------------------------------------------------
+
+template <int FMT>
+__device__ __forceinline__ uint32_t pack4(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    if constexpr (FMT == kFmtE4M3) {
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r)
+            : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    } else {
+        asm("{\n\t.reg .b16 lo, hi;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n\t"
+            "mov.b32 %0, {lo, hi};\n\t}"
+            : "=r"(r)
+            : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    }
+    return r;
+}
+
+// Codes of eight values sharing one group scale, packed little-endian.
+template <int FMT>
+__device__ __forceinline__ uint2 quantize8(const float* v, float s, float inv) {
+    uint2 r;
+    r.x = pack4<FMT>(quotient(v[0], s, inv), quotient(v[1], s, inv), quotient(v[2], s, inv),
+                     quotient(v[3], s, inv));
+    r.y = pack4<FMT>(quotient(v[4], s, inv), quotient(v[5], s, inv), quotient(v[6], s, inv),
+                     quotient(v[7], s, inv));
+    return r;
+}
+
+__device__ __forceinline__ float absmax8(const float* v) {
+    float m = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU ("DeepSeek开源TileKernels..." §3.3: val_l / (1 + exp(-val_l)) * val_r),
+// each step a single binary32 operation; exp is the CUDA math library's expf.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float swiglu(float g, float u) {
+    const float e = expf(-g);
+    const float den = __fadd_rn(1.0f, e);
+    const float silu = __fdiv_rn(g, den);
+    return __fmul_rn(silu, u);
+}
+
+// ---------------------------------------------------------------------------
+// Unsigned 32-bit division by a run-time invariant divisor with a multiply and
+// shifts (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994, the round-up method).  The host computes
+// (m, sh1, sh2) once per launch.
+// ---------------------------------------------------------------------------
+
+struct FastDiv {
+    uint32_t d, m, sh1, sh2;
+};
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+    const uint32_t t1 = __umulhi(f.m, n);
+    return (t1 + ((n - t1) >> f.sh1)) >> f.sh2;
+}
+
+}  // namespace tkq

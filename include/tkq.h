@@ -1,0 +1,127 @@
+/*
+ * tkq.h -- C ABI of libtkq.so: per-token-group FP8 activation quantization on
+ * GB300 (sm_103a).
+ *
+ * The operations follow the TileKernels quantization operators described in
+ *   [P2] "DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件性能上限"
+ *        (itsolotime.com), §3.1 (cast config, clamp_min_value), §3.2 (the
+ *        per-token cast kernel), §3.3 (SwiGLU fused with the cast);
+ *   [P1] "TileKernels 与 DeepGEMM 的分界线：DeepSeek 开源内核栈的分工"
+ *        (chatdocs.ruinique.com), §2 operator table;
+ *   [P4] "刚刚！DeepSeek开源高性能GPU算子库TileKernels" (info.datadowell.com),
+ *        quant/ section (SwiGLU + FP8 + transpose in one pass).
+ *
+ * Common definitions
+ * ------------------
+ * group      Only 128 is accepted (1x128 groups along the quantized axis).
+ * fmt        TKQ_FMT_E4M3 (float8_e4m3fn, largest finite 448) or
+ *            TKQ_FMT_E5M2 (float8_e5m2, largest finite 57344).
+ * scale      For each group, s = fl32(max(amax, 1e-4) / fmt_max) where amax is
+ *            the largest |value| of the group ([P2] §3.1 and §3.2).
+ * code       The saturating round-to-nearest-even FP8 code of the binary32
+ *            quotient fl32(value / s); results beyond the largest finite value
+ *            saturate to it.  The sign of zero is kept.
+ * bf16       Inputs are bf16, row-major and contiguous.
+ * outputs    Codes are one byte per element, row-major; scales are fp32.
+ *
+ * Memory, streams, errors
+ * -----------------------
+ * - Every pointer is a DEVICE pointer owned and allocated by the caller; the
+ *   library allocates nothing and keeps no per-call state.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream).  TKQ_OK means "arguments valid and kernel launched";
+ *   results are ready when the stream reaches that point.
+ * - Argument errors are detected on the host before anything is launched and
+ *   leave every buffer untouched: TKQ_ERR_NULL (a required pointer is NULL),
+ *   TKQ_ERR_SHAPE (negative sizes, or an extent that is not a multiple of the
+ *   group), TKQ_ERR_GROUP (group != 128), TKQ_ERR_FMT (unknown format),
+ *   TKQ_ERR_ALIGN (x, out, out_t not 16-byte aligned, or sf, sf_t, w not
+ *   4-byte aligned), TKQ_ERR_ALIAS (an output overlaps an input or another
+ *   output).  T == 0 is an empty batch: TKQ_OK, nothing is launched and the
+ *   pointers may be NULL.
+ * - A failed launch returns TKQ_ERR_CUDA (cudaGetLastError after the launch).
+ * - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ * - Calls on the same buffers from different streams must be ordered by the
+ *   caller.
+ */
+#ifndef TKQ_H
+#define TKQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TKQ_FMT_E4M3 = 0,
+    TKQ_FMT_E5M2 = 1
+} tkq_fmt;
+
+typedef enum {
+    TKQ_OK = 0,
+    TKQ_ERR_NULL = 1,
+    TKQ_ERR_SHAPE = 2,
+    TKQ_ERR_GROUP = 3,
+    TKQ_ERR_FMT = 4,
+    TKQ_ERR_ALIGN = 5,
+    TKQ_ERR_CUDA = 6,
+    TKQ_ERR_ALIAS = 7
+} tkq_status;
+
+/* A cudaStream_t passed as an opaque pointer. */
+typedef void* tkq_stream_t;
+
+/*
+ * Plain per-token cast ([P2] §3.2, per_token_cast; [P1] §6 steps 3 and 10).
+ *   x   : bf16 [T, C], row-major
+ *   out : FP8 codes [T, C], row-major
+ *   sf  : fp32 [T, C/128], row-major; sf[t, j] scales x[t, 128j : 128j+128]
+ * T >= 0 (any value, no tile alignment needed); C > 0, C % 128 == 0.
+ */
+tkq_status tkq_per_token_cast(const void* x, void* out, float* sf,
+                              int64_t T, int64_t C, int group, int fmt,
+                              tkq_stream_t stream);
+
+/*
+ * SwiGLU fused with the per-token cast ([P2] §3.3,
+ * swiglu_forward_and_per_token_cast), optionally with a per-row routing
+ * weight.  For every row t and channel c < H:
+ *   g = x[t, c], u = x[t, H + c] (both widened to fp32),
+ *   y = ((g / (1 + exp(-g))) * u) [* w[t]]       (binary32 arithmetic)
+ * and y is cast as in tkq_per_token_cast.
+ *   x   : bf16 [T, 2H], gate = columns [0, H), up = columns [H, 2H)
+ *   w   : fp32 [T] or NULL (no weight)
+ *   out : FP8 codes [T, H];  sf : fp32 [T, H/128]
+ * T >= 0; H > 0, H % 128 == 0.
+ * exp() is the CUDA math library's; y may differ from an exactly rounded
+ * evaluation by a few ulp, so codes are not bit-pinned to a CPU evaluation.
+ */
+tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf,
+                           int64_t T, int64_t H, int group, int fmt,
+                           tkq_stream_t stream);
+
+/*
+ * SwiGLU + per-token cast + transposed cast in one pass ([P4] quant/ triple
+ * fusion; [P1] §2 "per_channel_cast (+transpose / fused)").  Writes the same
+ * out / sf as tkq_swiglu_cast (bit for bit) and, from the same fp32 y, a
+ * column-major copy quantized with 1x128 groups along the token axis:
+ *   out_t : FP8 codes [H, T]; out_t[c, t] is the code of y[t, c]
+ *   sf_t  : fp32 [H, T/128]; sf_t[c, b] scales y[128b : 128b+128, c]
+ * T >= 0 with T % 128 == 0; H > 0, H % 128 == 0.
+ */
+tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
+                             void* out_t, float* sf_t,
+                             int64_t T, int64_t H, int group, int fmt,
+                             tkq_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* tkq_status_string(int status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int tkq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TKQ_H */

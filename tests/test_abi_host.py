@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds for sm_103a, loads, exports every function declared in
+include/tkq.h, and rejects invalid arguments with the documented status codes
+before touching CUDA (no kernel is launched on these paths).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tkq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_activation_quantization_gb300 import _build
+    import fp8_activation_quantization_gb300 as tkq
+    _build.build()
+    return tkq.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_]\w*[\s\*]+(tkq_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tkq_per_token_cast", "tkq_swiglu_cast", "tkq_swiglu_cast_t", "tkq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libtkq.so does not export {name}"
+
+
+def test_library_is_built_for_sm_103a():
+    from fp8_activation_quantization_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+    assert os.path.exists(_build.LIB)
+
+
+def test_status_strings(lib):
+    import fp8_activation_quantization_gb300 as tkq
+    for code, word in [(0, "TKQ_OK"), (1, "NULL"), (2, "SHAPE"), (3, "GROUP"), (4, "FMT"),
+                       (5, "ALIGN"), (6, "CUDA"), (7, "ALIAS"), (99, "UNKNOWN")]:
+        assert word in tkq.tkq_status_string(code)
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every case below fails validation first
+
+
+def p(off=0):
+    return ctypes.c_void_p(FAKE + off)
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((None, p(1 << 20), p(2 << 20), 4, 256, 128, 0), 1),          # NULL input
+    ((p(), p(1 << 20), p(2 << 20), 4, 200, 128, 0), 2),           # C % 128
+    ((p(), p(1 << 20), p(2 << 20), -1, 256, 128, 0), 2),          # T < 0
+    ((p(), p(1 << 20), p(2 << 20), 4, 0, 128, 0), 2),             # C == 0
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 64, 0), 3),            # group
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 2), 4),           # fmt
+    ((p(8), p(1 << 20), p(2 << 20), 4, 256, 128, 0), 5),          # x misaligned
+    ((p(), p((1 << 20) + 4), p(2 << 20), 4, 256, 128, 0), 5),     # out misaligned
+    ((p(), p(1 << 20), p((2 << 20) + 2), 4, 256, 128, 0), 5),     # sf misaligned
+    ((p(), p(512), p(2 << 20), 4, 256, 128, 0), 7),               # out overlaps x
+    ((p(), p(1 << 20), p((1 << 20) + 512), 4, 256, 128, 0), 7),   # sf overlaps out
+    ((None, None, None, 0, 256, 128, 0), 0),                      # empty batch
+])
+def test_per_token_cast_validation(lib, args, expected):
+    assert lib.tkq_per_token_cast(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((p(), None, p(1 << 24), None, 4, 256, 128, 0), 1),
+    ((p(), p((1 << 24) + 4), p(1 << 24), p(2 << 24), 4, 256, 128, 0), 7),  # w overlaps out
+    ((p(), p(4), p(1 << 24), p(2 << 24), 0, 256, 128, 0), 0),     # empty batch
+    ((p(), p(1 << 26), p(1 << 24), p(2 << 24), 4, 100, 128, 0), 2),
+    ((p(), p((1 << 26) + 2), p(1 << 24), p(2 << 24), 4, 256, 128, 0), 5),
+    ((p(), None, p(1 << 24), p(2 << 24), 4, 256, 128, 3), 4),
+])
+def test_swiglu_cast_validation(lib, args, expected):
+    assert lib.tkq_swiglu_cast(*args, None) == expected
+
+
+@pytest.mark.parametrize("T,expected", [(100, 2), (0, 0), (-128, 2)])
+def test_swiglu_cast_t_validation(lib, T, expected):
+    if T == 0:
+        args = (None, None, None, None, None, None, 0, 256, 128, 0, None)
+    else:
+        args = (p(), None, p(1 << 24), p(2 << 24), p(3 << 24), p(4 << 24), T, 256, 128, 0, None)
+    assert lib.tkq_swiglu_cast_t(*args) == expected
+
+
+def test_swiglu_cast_t_output_alias(lib):
+    # out_t overlapping out
+    assert lib.tkq_swiglu_cast_t(p(), None, p(1 << 24), p(2 << 24), p((1 << 24) + 256),
+                                 p(4 << 24), 128, 256, 128, 0, None) == 7
