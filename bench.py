@@ -365,9 +365,12 @@ def run_ours(args):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = None
+    tkq.tkq_read_device_status(clear=True)
     with torch.cuda.stream(stream):
         with ClockSampler(uuid) as clk:
             dt = time_steps(prob, args.steps, args.warmup, stream, barrier)
+    if tkq.tkq_read_device_status():
+        raise RuntimeError("a bounded wait inside a kernel gave up: timing is invalid")
     if ws > 1:
         import torch.distributed as dist
         t = torch.tensor([dt], dtype=torch.float64, device=dev)

@@ -67,8 +67,29 @@ def load_library():
         lib.tkq_status_string.restype = ctypes.c_char_p
         lib.tkq_version.argtypes = []
         lib.tkq_version.restype = i
+        lib.tkq_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
+        lib.tkq_read_device_status.restype = i
+        lib.tkq_selftest_wait_timeout.argtypes = [i64, p]
+        lib.tkq_selftest_wait_timeout.restype = i
         _lib = lib
         return lib
+
+
+DEVICE_TIMEOUT = 1
+
+
+def tkq_read_device_status(clear: bool = False) -> int:
+    """Synchronize the current device and return its status word (bit
+    DEVICE_TIMEOUT: a bounded wait inside a kernel gave up)."""
+    v = ctypes.c_uint32(0)
+    st = load_library().tkq_read_device_status(ctypes.byref(v), 1 if clear else 0)
+    if st:
+        raise TkqError(st, "tkq_read_device_status")
+    return int(v.value)
+
+
+def tkq_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return load_library().tkq_selftest_wait_timeout(int(limit_ns), stream)
 
 
 def tkq_status_string(status: int) -> str:

@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(kThreads)
             float s, inv;
             group_scale<FMT>(m, s, inv);
             if (g[u] < n_groups) {
-                st_stream(out + g[u] * 16 + j, quantize8<FMT>(y, s, inv));
-                st_stream(out + g[u] * 16 + 8 + j, quantize8<FMT>(y + 8, s, inv));
+                st_stream(out + g[u] * 16 + j, quantize8_mul<FMT>(y, inv));
+                st_stream(out + g[u] * 16 + 8 + j, quantize8_mul<FMT>(y + 8, inv));
                 if (j == 0) st_stream(sf + g[u], s);
             }
         }

@@ -1,5 +1,5 @@
 // swiglu_cast_t.cu -- SwiGLU + per-token FP8 cast + transposed (token-axis)
-// FP8 cast in one pass.
+// FP8 cast in one pass over HBM.
 //
 // The operation is the SwiGLU + FP8 + transpose triple fusion of the quant/
 // section of "刚刚！DeepSeek开源高性能GPU算子库TileKernels" (info.datadowell.com),
@@ -9,215 +9,317 @@
 // "per_channel_cast (+transpose / fused)").  Both outputs are quantized from the
 // same fp32 y.
 //
-// GB300 design.  A CTA owns a 128-token x 128-channel tile of y at a time and
-// walks tiles with a persistent grid.  Thread layout (256 threads = 8 warps):
-// lane & 15 picks an 8-channel chunk, warp * 2 + lane / 16 picks an 8-token
-// block, so each thread holds an 8 x 8 block of y in registers.  Per warp load
-// instruction the 16 lanes of a half-warp read one 256-byte run of a row, so
-// global loads are fully coalesced.
-//   * Row groups (1 x 128 channels): the 16 lanes of a half-warp own the same 8
-//     rows; their absmax is a butterfly that halves the live values at each of
-//     four xor-shuffle steps (8 shuffles instead of 32), after which lane pair
-//     (2r, 2r+1) holds row r's absmax, computes its scale once, and shuffles
-//     scale and reciprocal back to the other lanes.  Codes go straight from
-//     registers to HBM as 8-byte stores (a half-warp writes a 128-byte row run).
+// GB300 design: one persistent CTA per SM walks 128-token x 128-channel tiles
+// of y.  Warp 16 is the producer: one lane streams the gate and up tiles of the
+// CTA's upcoming tiles (2 x 32 KB, one 2-D TMA box each) into a 3-stage shared
+// ring, so up to 192 KB per SM are in flight while the consumers compute.
+// Warps 0..15 are consumers; warp w owns tokens 8w..8w+7 of the tile and lane
+// l owns channels 4l..4l+3, i.e. an 8 x 4 block of y per thread, read from the
+// ring with conflict-free 8-byte shared loads (a warp reads one 256-byte row).
+// As soon as y is in registers the warp releases the stage to the producer.
+//   * Row groups (1 x 128 channels = one warp row): a butterfly absmax across
+//     the 32 lanes that halves the live values at each xor step (9 shuffles
+//     for 8 rows); lanes 4r..4r+3 then hold row r, compute its scale once and
+//     shuffle scale and reciprocal back.  Codes leave as 4-byte stores, one
+//     128-byte run per warp store instruction.
 //   * Column groups (128 tokens x 1 channel): per-thread maxima over 8 tokens,
-//     one halving xor-16 step, a 8 x 128 shared-memory table reduced by 128
-//     threads, scales broadcast through shared memory.  The column codes are
-//     transposed through a 16 KB shared tile of bytes [channel][token] whose
-//     8-byte token units are XOR-swizzled by (channel / 8) so that the 8-byte
-//     writes of a half-warp hit 32 distinct banks; the tile leaves as 16-byte
-//     stores, eight lanes per 128-byte row run of out_t.  (The transpose
-//     walkthrough of the TileKernels page, §6, rotates the column index by the
-//     thread id and pads the tile for the same purpose.)
-// No tensor cores: the kernel is bound by HBM bandwidth.
+//     a 16 x 128 shared table reduced by 128 threads, scales broadcast through
+//     shared memory.  Codes are transposed through a 16 KB byte tile
+//     [channel][token] whose 8-byte token units are XOR-swizzled by
+//     (channel / 4) & 15 so that each half-warp's 8-byte writes cover 32
+//     distinct banks; the tile leaves as 16-byte stores, eight lanes per
+//     128-byte run of out_t.  (The TileKernels transpose of the same page, §6,
+//     rotates a column index by the thread id and pads the tile for the same
+//     purpose.)
+// All mbarrier waits are bounded (tkq_async.cuh); on a timeout the consumers
+// agree through a barrier-with-OR and leave together, and the producer waits
+// (bounded) for its issued copies before it returns.
+#include <cuda.h>
+
+#include "tkq_async.cuh"
 #include "tkq_device.cuh"
 #include "tkq_internal.h"
 
 namespace tkq {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 3;
+constexpr int kTileBytes = 128 * 128 * 2;    // one bf16 128 x 128 box
+constexpr int kStageBytes = 2 * kTileBytes;  // gate + up
+constexpr int kBarConsumers = 1;             // named barrier of the consumer warps
+
+struct alignas(1024) SharedStorage {
+    uint8_t stage[kStages][kStageBytes];
+    uint2 codes[128][16];                   // [channel][8-token unit], swizzled
+    float colmax[kConsumerWarps][128];
+    float cinv[128];
+    float rowinv[kConsumerWarps][8];
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int abort;
+};
 
 template <int FMT, bool WEIGHTED>
-__global__ void __launch_bounds__(kThreads, 2)
-    swiglu_cast_t_kernel(const uint4* __restrict__ x, const float* __restrict__ w,
-                         uint2* __restrict__ out, float* __restrict__ sf,
-                         uint4* __restrict__ out_t, float* __restrict__ sf_t, int64_t T, int H) {
-    __shared__ __align__(16) float s_colmax[8][128];
-    __shared__ __align__(16) float s_cs[128];
-    __shared__ __align__(16) float s_cinv[128];
-    __shared__ __align__(16) uint2 s_codes[128][16];
+__global__ void __launch_bounds__(kThreads, 1)
+    swiglu_cast_t_kernel(const __grid_constant__ CUtensorMap tmap, const float* __restrict__ w,
+                         uint8_t* __restrict__ out, float* __restrict__ sf,
+                         uint4* __restrict__ out_t, float* __restrict__ sf_t, int64_t T, int H,
+                         unsigned int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    SharedStorage& sm = *reinterpret_cast<SharedStorage*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
 
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int cc = lane & 15;                // channel chunk (8 channels)
-    const int half = lane >> 4;              // which row block of the warp
-    const int rb = warp * 2 + half;          // token block (8 tokens)
-    const int CB = H >> 7;                   // channel tiles
-    const int64_t TB = T >> 7;               // token tiles
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int CB = H >> 7;
+    const int64_t TB = T >> 7;
     const int64_t n_tiles = TB * CB;
-    const int64_t row_u4 = H >> 2;           // uint4 per input row (2H bf16)
-    const int64_t half_u4 = H >> 3;          // uint4 offset of the up half
-    const int64_t out_row_u2 = H >> 3;       // uint2 per output row
 
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            int64_t issued = 0;
+            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++issued) {
+                const int s = static_cast<int>(issued % kStages);
+                const uint32_t use = static_cast<uint32_t>(issued / kStages);
+                if (use > 0 &&
+                    !mbar_wait_bounded(&sm.empty[s], (use - 1) & 1u, &sm.abort, status)) {
+                    sm.abort = 1;
+                    break;
+                }
+                const int64_t tb = tile / CB;
+                const int cb = static_cast<int>(tile - tb * CB);
+                mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
+                tma_load_2d(sm.stage[s], &tmap, cb * 128, static_cast<int>(tb * 128), &sm.full[s]);
+                tma_load_2d(sm.stage[s] + kTileBytes, &tmap, H + cb * 128,
+                            static_cast<int>(tb * 128), &sm.full[s]);
+            }
+            // every copy this CTA issued must have landed before it may exit
+            const int64_t first = issued > kStages ? issued - kStages : 0;
+            for (int64_t k = first; k < issued; ++k)
+                mbar_wait_bounded(&sm.full[k % kStages], static_cast<uint32_t>(k / kStages) & 1u,
+                                  nullptr, status);
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int ct = threadIdx.x;  // 0 .. kConsumers-1
+    int64_t i = 0;
+    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
+        const int s = static_cast<int>(i % kStages);
+        const uint32_t use = static_cast<uint32_t>(i / kStages);
         const int64_t tb = tile / CB;
         const int cb = static_cast<int>(tile - tb * CB);
         const int64_t t0 = tb * 128;
         const int c0 = cb * 128;
+        const int64_t row0 = t0 + warp * 8;
 
-        // ---- load the 8 x 8 block of gate and up --------------------------
-        uint4 gq[8], uq[8];
         float wt[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int64_t row = t0 + rb * 8 + r;
-            const uint4* p = x + row * row_u4 + (c0 >> 3) + cc;
-            gq[r] = ld_stream(p);
-            uq[r] = ld_stream(p + half_u4);
-            wt[r] = 1.0f;
-            if constexpr (WEIGHTED) wt[r] = ld_stream_f32(w + row);
+        for (int r = 0; r < 8; ++r) wt[r] = 1.0f;
+        if constexpr (WEIGHTED) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) wt[r] = __ldg(w + row0 + r);
         }
 
-        // ---- y = silu(g) * u [* w] ----------------------------------------
-        float y[8][8];
+        const bool ok = mbar_wait_bounded(&sm.full[s], use & 1u, &sm.abort, status);
+
+        // ---- y = silu(g) * u [* w] for this thread's 8 x 4 block ----------
+        float y[8][4];
+        {
+            const uint8_t* g_base = sm.stage[s] + warp * 8 * 256 + lane * 8;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            float gv[8], uv[8];
-            unpack8(gq[r], gv);
-            unpack8(uq[r], uv);
+            for (int r = 0; r < 8; ++r) {
+                uint2 gq = make_uint2(0, 0), uq = make_uint2(0, 0);
+                if (ok) {
+                    gq = *reinterpret_cast<const uint2*>(g_base + r * 256);
+                    uq = *reinterpret_cast<const uint2*>(g_base + kTileBytes + r * 256);
+                }
+                float gv[4], uv[4];
+                unpack4(gq, gv);
+                unpack4(uq, uv);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                y[r][k] = swiglu(gv[k], uv[k]);
-                if constexpr (WEIGHTED) y[r][k] = __fmul_rn(y[r][k], wt[r]);
+                for (int k = 0; k < 4; ++k) {
+                    y[r][k] = swiglu(gv[k], uv[k]);
+                    if constexpr (WEIGHTED) y[r][k] = __fmul_rn(y[r][k], wt[r]);
+                }
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // stage may be refilled
 
-        // ---- column maxima over this thread's 8 tokens, halved across the
-        //      two row blocks of the warp, into shared memory ----------------
+        // ---- column maxima over this thread's 8 tokens -> shared table ----
         {
-            float cm[8];
+            float4 cm;
+            float* c = &cm.x;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 4; ++k) {
                 float m = fabsf(y[0][k]);
 #pragma unroll
                 for (int r = 1; r < 8; ++r) m = fmaxf(m, fabsf(y[r][k]));
-                cm[k] = m;
+                c[k] = m;
             }
-            float4 keep;
-            float* kp = &keep.x;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = half ? cm[i] : cm[4 + i];
-                const float mine = half ? cm[4 + i] : cm[i];
-                kp[i] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 16));
-            }
-            *reinterpret_cast<float4*>(&s_colmax[warp][cc * 8 + half * 4]) = keep;
+            *reinterpret_cast<float4*>(&sm.colmax[warp][lane * 4]) = cm;
         }
 
-        // ---- row groups: butterfly absmax over the 16 lanes of the half-warp
+        // ---- row groups: butterfly absmax across the warp --------------------
         {
             float m[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) m[r] = absmax8(y[r]);
-            const int b3 = (cc >> 3) & 1, b2 = (cc >> 2) & 1, b1 = (cc >> 1) & 1;
+            for (int r = 0; r < 8; ++r)
+                m[r] = fmaxf(fmaxf(fabsf(y[r][0]), fabsf(y[r][1])),
+                             fmaxf(fabsf(y[r][2]), fabsf(y[r][3])));
+            const int b4 = (lane >> 4) & 1, b3 = (lane >> 3) & 1, b2 = (lane >> 2) & 1;
             float a[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float send = b3 ? m[i] : m[4 + i];
-                const float mine = b3 ? m[4 + i] : m[i];
-                a[i] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 8));
+            for (int q = 0; q < 4; ++q) {
+                const float send = b4 ? m[q] : m[4 + q];
+                const float mine = b4 ? m[4 + q] : m[q];
+                a[q] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 16));
             }
             float b[2];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float send = b2 ? a[i] : a[2 + i];
-                const float mine = b2 ? a[2 + i] : a[i];
-                b[i] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 4));
+            for (int q = 0; q < 2; ++q) {
+                const float send = b3 ? a[q] : a[2 + q];
+                const float mine = b3 ? a[2 + q] : a[q];
+                b[q] = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 8));
             }
             float c;
             {
-                const float send = b1 ? b[0] : b[1];
-                const float mine = b1 ? b[1] : b[0];
-                c = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 2));
+                const float send = b2 ? b[0] : b[1];
+                const float mine = b2 ? b[1] : b[0];
+                c = fmaxf(mine, __shfl_xor_sync(0xffffffffu, send, 4));
             }
+            c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, 2));
             c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, 1));
-            // this lane now holds the absmax of row (cc >> 1) of its row block
+            // lanes 4r .. 4r+3 hold the absmax of row r of this warp's 8 rows;
+            // one of them publishes the row's reciprocal scale to the warp
             float s_own, inv_own;
             group_scale<FMT>(c, s_own, inv_own);
-            const int64_t my_row = t0 + rb * 8 + (cc >> 1);
-            if ((cc & 1) == 0) st_stream(sf + my_row * CB + cb, s_own);
+            if ((lane & 3) == 0) {
+                st_stream(sf + (row0 + (lane >> 2)) * CB + cb, s_own);
+                sm.rowinv[warp][lane >> 2] = inv_own;
+            }
+            __syncwarp();
+            float rinv[8];
+            *reinterpret_cast<float4*>(rinv) = *reinterpret_cast<const float4*>(&sm.rowinv[warp][0]);
+            *reinterpret_cast<float4*>(rinv + 4) =
+                *reinterpret_cast<const float4*>(&sm.rowinv[warp][4]);
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                const int src = (lane & 16) | (r * 2);
-                const float s = __shfl_sync(0xffffffffu, s_own, src);
-                const float inv = __shfl_sync(0xffffffffu, inv_own, src);
-                const int64_t row = t0 + rb * 8 + r;
-                st_stream(out + row * out_row_u2 + (c0 >> 3) + cc, quantize8<FMT>(y[r], s, inv));
+                const uint32_t code = quantize4_mul<FMT>(y[r], rinv[r]);
+                st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * H + c0) + lane, code);
             }
         }
 
-        __syncthreads();  // s_colmax complete
-
-        // ---- column scales ------------------------------------------------
-        if (tid < 128) {
-            float m = s_colmax[0][tid];
-#pragma unroll
-            for (int q = 1; q < 8; ++q) m = fmaxf(m, s_colmax[q][tid]);
-            float s, inv;
-            group_scale<FMT>(m, s, inv);
-            s_cs[tid] = s;
-            s_cinv[tid] = inv;
-            st_stream(sf_t + static_cast<int64_t>(c0 + tid) * TB + tb, s);
+        // all consumers agree whether to go on (a wait may have given up)
+        if (named_bar_or(kBarConsumers, kConsumers, !ok)) {
+            if (ct == 0) *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
+            break;
         }
 
-        __syncthreads();  // s_cs / s_cinv ready
-
-        // ---- column codes into the swizzled [channel][token] byte tile ----
-        {
-            float cs[8], ci[8];
-            *reinterpret_cast<float4*>(cs) = *reinterpret_cast<const float4*>(&s_cs[cc * 8]);
-            *reinterpret_cast<float4*>(cs + 4) = *reinterpret_cast<const float4*>(&s_cs[cc * 8 + 4]);
-            *reinterpret_cast<float4*>(ci) = *reinterpret_cast<const float4*>(&s_cinv[cc * 8]);
-            *reinterpret_cast<float4*>(ci + 4) = *reinterpret_cast<const float4*>(&s_cinv[cc * 8 + 4]);
+        // ---- column scales ------------------------------------------------
+        if (ct < 128) {
+            float m = sm.colmax[0][ct];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int q = 1; q < kConsumerWarps; ++q) m = fmaxf(m, sm.colmax[q][ct]);
+            float s_c, inv_c;
+            group_scale<FMT>(m, s_c, inv_c);
+            sm.cinv[ct] = inv_c;
+            st_stream(sf_t + static_cast<int64_t>(c0 + ct) * TB + tb, s_c);
+        }
+        named_bar_sync(kBarConsumers, kConsumers);
+
+        // ---- column codes into the swizzled [channel][token] tile -----------
+        {
+            const float4 ci4 = *reinterpret_cast<const float4*>(&sm.cinv[lane * 4]);
+            const float civ[4] = {ci4.x, ci4.y, ci4.z, ci4.w};
+            const int unit = warp ^ (lane & 15);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
                 float col[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) col[r] = y[r][k];
-                s_codes[cc * 8 + k][rb ^ cc] = quantize8<FMT>(col, cs[k], ci[k]);
+                sm.codes[lane * 4 + k][unit] = quantize8_mul<FMT>(col, civ[k]);
             }
         }
+        named_bar_sync(kBarConsumers, kConsumers);
 
-        __syncthreads();  // code tile complete
-
-        // ---- code tile -> out_t rows c0.., tokens t0..t0+127 -------------
+        // ---- code tile -> out_t rows c0.., tokens t0..t0+127 ----------------
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int c = p * 32 + (tid >> 3);
-            const int ch = tid & 7;          // 16-byte chunk = tokens 16ch .. 16ch+15
-            const int sw = (c >> 3) & 15;    // swizzle of row c
-            uint4 v = *reinterpret_cast<const uint4*>(&s_codes[c][2 * (ch ^ (sw >> 1))]);
+        for (int p = 0; p < 2; ++p) {
+            const int c = p * 64 + (ct >> 3);
+            const int ch = ct & 7;            // tokens 16ch .. 16ch+15
+            const int sw = (c >> 2) & 15;     // swizzle of row c
+            uint4 v = *reinterpret_cast<const uint4*>(&sm.codes[c][2 * (ch ^ (sw >> 1))]);
             if (sw & 1) v = make_uint4(v.z, v.w, v.x, v.y);
             st_stream(out_t + ((static_cast<int64_t>(c0 + c) * T + t0) >> 4) + ch, v);
         }
-        // The next tile's first shared-memory writes (s_colmax) come after this
-        // tile's last reads of s_colmax (before the second barrier), and
-        // s_codes is rewritten only after two more barriers.
+        // The next tile writes colmax before its first consumer barrier and
+        // codes only after its second, so every read of this tile's shared data
+        // is complete before it is overwritten.
     }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
 }
 
 template <int FMT, bool WEIGHTED>
 cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* out_t,
                    float* sf_t, int64_t T, int64_t H, cudaStream_t stream) {
-    const void* k = reinterpret_cast<const void*>(&swiglu_cast_t_kernel<FMT, WEIGHTED>);
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    // x viewed as a 2-D bf16 tensor: inner extent 2H (gate | up), outer T rows
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * H), static_cast<cuuint64_t>(T)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4 * H)};  // bytes between rows
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+
+    auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED>;
+    const size_t smem = sizeof(SharedStorage) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
     const int64_t n_tiles = (T / 128) * (H / 128);
-    const int grid = persistent_grid(k, kThreads, 0, n_tiles);
-    swiglu_cast_t_kernel<FMT, WEIGHTED><<<grid, kThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), w, static_cast<uint2*>(out), sf,
-        static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H));
+    const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
+    k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,
+                                        static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H),
+                                        device_status_word());
     return cudaGetLastError();
 }
 

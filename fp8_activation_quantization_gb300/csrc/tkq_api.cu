@@ -9,13 +9,34 @@
 #include <cuda_runtime.h>
 
 #include "../../include/tkq.h"
+#include "tkq_async.cuh"
 #include "tkq_internal.h"
+
+// The library's device status word (one per device): kernels OR status bits
+// into it (tkq::kDeviceTimeout when a bounded wait gave up); the host reads and
+// clears it with tkq_read_device_status.
+__device__ unsigned int g_tkq_device_status;
 
 namespace tkq {
 
 namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
+std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+
+// One CTA waits on an mbarrier that nothing ever arrives on, so its bounded
+// wait must give up after limit_ns and record a timeout in the status word.
+__global__ void selftest_wait_kernel(unsigned int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, &abort, status, limit_ns);
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -45,6 +66,20 @@ int num_sms() {
         v = 1;
     if (dev < kMaxDevices) g_sms[dev].store(v, std::memory_order_relaxed);
     return v;
+}
+
+unsigned int* device_status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    if (dev < kMaxDevices) {
+        unsigned int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+        if (p) return p;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tkq_device_status) != cudaSuccess) return nullptr;
+    if (dev < kMaxDevices)
+        g_status_ptr[dev].store(static_cast<unsigned int*>(p), std::memory_order_release);
+    return static_cast<unsigned int*>(p);
 }
 
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed) {
@@ -122,7 +157,8 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
     if (st != TKQ_OK) return st;
     if (T % group) return TKQ_ERR_SHAPE;
     if (T == 0) return TKQ_OK;
-    if (H > (int64_t{1} << 30)) return TKQ_ERR_SHAPE;
+    // TMA box coordinates are 32-bit
+    if (H > (int64_t{1} << 30) || T > INT32_MAX) return TKQ_ERR_SHAPE;
     if (!x || !out || !sf || !out_t || !sf_t) return TKQ_ERR_NULL;
     if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(out_t, 16) ||
         !tkq::aligned(sf, 4) || !tkq::aligned(sf_t, 4) || (w && !tkq::aligned(w, 4)))
@@ -140,6 +176,30 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
     }
     return launch_status(tkq::launch_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, fmt,
                                                    static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
+    if (!flags) return TKQ_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tkq_device_status, sizeof v) != cudaSuccess)
+        return TKQ_ERR_CUDA;
+    if (clear) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_tkq_device_status, &zero, sizeof zero) != cudaSuccess)
+            return TKQ_ERR_CUDA;
+    }
+    *flags = v;
+    return TKQ_OK;
+}
+
+tkq_status tkq_selftest_wait_timeout(int64_t limit_ns, tkq_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > int64_t{2000000000}) return TKQ_ERR_SHAPE;
+    unsigned int* status = tkq::device_status_word();
+    if (!status) return TKQ_ERR_CUDA;
+    tkq::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        status, static_cast<uint64_t>(limit_ns));
+    return launch_status(cudaGetLastError());
 }
 
 const char* tkq_status_string(int status) {

@@ -21,10 +21,12 @@ struct FmtTraits;
 template <>
 struct FmtTraits<kFmtE4M3> {
     static constexpr float kMax = 448.0f;
+    static constexpr float kInvMax = 1.0f / 448.0f;  // rounded to nearest binary32
 };
 template <>
 struct FmtTraits<kFmtE5M2> {
     static constexpr float kMax = 57344.0f;
+    static constexpr float kInvMax = 1.0f / 57344.0f;
 };
 
 // ---------------------------------------------------------------------------
@@ -56,6 +58,9 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
+__device__ __forceinline__ void st_stream_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_stream(float* p, float v) {
     asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -79,11 +84,17 @@ __device__ __forceinline__ void unpack8(const uint4& q, float* v) {
 // scale and quotient
 // ---------------------------------------------------------------------------
 
-// s = fl32(max(amax, 1e-4) / fmt_max) with an IEEE division, and the correctly
-// rounded reciprocal inv = fl32(1 / s).
+// s = fl32(max(amax, 1e-4) / fmt_max) and the correctly rounded reciprocal
+// inv = fl32(1 / s).  The division is a product by c = fl32(1 / fmt_max) with
+// one FMA residual correction (Markstein): q0 = a*c, r = a - q0*fmt_max,
+// s = q0 + r*c.  For every binary32 a >= 1e-4 this equals the IEEE quotient
+// (checked exhaustively for both formats: all 2.37e9 such a).
 template <int FMT>
 __device__ __forceinline__ void group_scale(float amax, float& s, float& inv) {
-    s = __fdiv_rn(fmaxf(amax, 1e-4f), FmtTraits<FMT>::kMax);
+    const float a = fmaxf(amax, 1e-4f);
+    const float q0 = __fmul_rn(a, FmtTraits<FMT>::kInvMax);
+    const float r = __fmaf_rn(-q0, FmtTraits<FMT>::kMax, a);
+    s = __fmaf_rn(r, FmtTraits<FMT>::kInvMax, q0);
     inv = __frcp_rn(s);
 }
 
@@ -148,15 +159,65 @@ __device__ __forceinline__ float absmax8(const float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// SwiGLU ("DeepSeek开源TileKernels..." §3.3: val_l / (1 + exp(-val_l)) * val_r),
-// each step a single binary32 operation; exp is the CUDA math library's expf.
+// SwiGLU ("DeepSeek开源TileKernels..." §3.3: val_l / (1 + exp(-val_l)) * val_r)
+// with the SM's transcendental unit:
+//   exp(-g) = 2^(-g * log2 e)      hardware base-2 exponential (ex2.approx)
+//   g / (1 + exp(-g))              hardware reciprocal (rcp.approx) times g
+// Error against exactly rounded binary32 steps: the product t = -g * log2 e is
+// rounded (absolute error <= |t| 2^-24 with the rounded constant), which gives
+// exp(-g) a relative error of about (1.04 |t| + 2) ulp; it enters the result
+// scaled by exp(-g) / (1 + exp(-g)) < 1/2 for g > 0.  Rounded reciprocal and the
+// two products add about 2 ulp.  So y is within a few ulp wherever |y| is not
+// tiny relative to |g u| (g > -6 or so), which covers the element that sets a
+// group's scale; the parity tolerance is 1e-6 relative on scales (about 16 ulp)
+// and one FP8 step on codes.
 // ---------------------------------------------------------------------------
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 __device__ __forceinline__ float swiglu(float g, float u) {
-    const float e = expf(-g);
+    const float e = ex2_approx(__fmul_rn(g, -1.4426950408889634f));
     const float den = __fadd_rn(1.0f, e);
-    const float silu = __fdiv_rn(g, den);
-    return __fmul_rn(silu, u);
+    return __fmul_rn(__fmul_rn(g, rcp_approx(den)), u);
+}
+
+// Four bf16 packed in a uint2 -> four floats, element order preserved.
+__device__ __forceinline__ void unpack4(const uint2& q, float* v) {
+    v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);
+    v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+}
+
+// Codes of four values sharing one group scale, packed little-endian.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize4(const float* v, float s, float inv) {
+    return pack4<FMT>(quotient(v[0], s, inv), quotient(v[1], s, inv), quotient(v[2], s, inv),
+                      quotient(v[3], s, inv));
+}
+
+// The SwiGLU kernels quantize y * inv, the product by the rounded reciprocal of
+// the scale, as the TileKernels per-token kernel does (x * sf_inv, "DeepSeek开源
+// TileKernels..." §3.2 step 4).  It is within one ulp of y / s; y itself carries
+// a few ulp of exp error, so the exact quotient would buy nothing measurable
+// there, while the plain cast keeps `quotient` to be bit-exact.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize4_mul(const float* v, float inv) {
+    return pack4<FMT>(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
+                      __fmul_rn(v[3], inv));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 quantize8_mul(const float* v, float inv) {
+    return make_uint2(quantize4_mul<FMT>(v, inv), quantize4_mul<FMT>(v + 4, inv));
 }
 
 // ---------------------------------------------------------------------------

@@ -11,6 +11,11 @@ namespace tkq {
 // variable TKQ_NUM_SMS overrides it for grid sizing experiments).
 int num_sms();
 
+// Address of the library's device status word on the current device (bit
+// kDeviceTimeout: a bounded wait inside a kernel gave up).  Resolved once per
+// device with cudaGetSymbolAddress.
+unsigned int* device_status_word();
+
 // Persistent grid: min(blocks needed, SMs x resident blocks per SM).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
 

@@ -115,6 +115,29 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
                              int64_t T, int64_t H, int group, int fmt,
                              tkq_stream_t stream);
 
+/*
+ * Device status word.  The pipelined kernels (tkq_swiglu_cast_t) wait on
+ * shared-memory barriers for their bulk copies; every such wait gives up after
+ * one second, sets TKQ_DEVICE_TIMEOUT in the current device's status word and
+ * lets the kernel return (its outputs are then incomplete) instead of hanging.
+ * tkq_read_device_status synchronizes the current device, stores the word in
+ * *flags and, if clear != 0, resets it.  Errors: TKQ_ERR_NULL (flags NULL),
+ * TKQ_ERR_CUDA (the synchronization or copy failed).
+ * (Not from the source pages: this is the library's failure reporting.)
+ */
+#define TKQ_DEVICE_TIMEOUT 1u
+tkq_status tkq_read_device_status(uint32_t* flags, int clear);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one CTA on `stream` that
+ * waits on a barrier nothing ever arrives on, for limit_ns nanoseconds
+ * (0 < limit_ns <= 2e9), then records TKQ_DEVICE_TIMEOUT in the status word and
+ * returns.  No memory is touched besides the status word.  Errors:
+ * TKQ_ERR_SHAPE (limit out of range), TKQ_ERR_CUDA (launch failed).
+ * (Not from the source pages.)
+ */
+tkq_status tkq_selftest_wait_timeout(int64_t limit_ns, tkq_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);
 

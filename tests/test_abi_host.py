@@ -98,6 +98,12 @@ def test_swiglu_cast_t_validation(lib, T, expected):
     assert lib.tkq_swiglu_cast_t(*args) == expected
 
 
+def test_status_calls_validate_before_cuda(lib):
+    assert lib.tkq_read_device_status(None, 0) == 1          # NULL flags
+    assert lib.tkq_selftest_wait_timeout(0, None) == 2       # limit out of range
+    assert lib.tkq_selftest_wait_timeout(3_000_000_000, None) == 2
+
+
 def test_swiglu_cast_t_output_alias(lib):
     # out_t overlapping out
     assert lib.tkq_swiglu_cast_t(p(), None, p(1 << 24), p(2 << 24), p((1 << 24) + 256),

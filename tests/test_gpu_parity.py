@@ -313,6 +313,7 @@ def test_swiglu_t_full_workload_sampled(cuda_device):
     st = tkq.tkq_swiglu_cast(p(xd), None, p(out2), p(sf2), T, H, 128, 0, stream_of(dev))
     assert st == 0
     torch.cuda.synchronize()
+    assert tkq.tkq_read_device_status() == 0, "a bounded wait gave up"
     assert torch.equal(out, out2) and torch.equal(sf.view(torch.int32), sf2.view(torch.int32))
     blocks = np.unique(np.concatenate([[0, T // 128 - 1],
                                        np.random.default_rng(3).integers(0, T // 128, 46)]))
@@ -359,6 +360,21 @@ def test_argument_errors_launch_nothing(cuda_device):
     # empty batch: OK, nothing launched, NULL pointers accepted
     assert tkq.tkq_per_token_cast(None, None, None, 0, 4096, 128, 0, s) == 0
     assert tkq.tkq_swiglu_cast_t(None, None, None, None, None, None, 0, 2048, 128, 0, s) == 0
+
+
+def test_bounded_wait_times_out_and_context_survives(cuda_device):
+    """A kernel waits on a barrier nothing arrives on: its wait gives up after
+    2 ms, the device status word reports the timeout, and the context keeps
+    working (a cast afterwards is still correct)."""
+    tkq.tkq_read_device_status(clear=True)
+    assert tkq.tkq_selftest_wait_timeout(2_000_000, stream_of(cuda_device)) == 0
+    assert tkq.tkq_read_device_status(clear=True) & tkq.DEVICE_TIMEOUT
+    assert tkq.tkq_read_device_status() == 0
+    x = synth.workload("swiglu", rows=256)["x"]
+    out, sf, out_t, sf_t = run_swiglu(x, None, "e4m3", cuda_device, transposed=True)
+    ro, rs, rot, rst = oracle.swiglu_cast_t(x, None, "e4m3")
+    parity.assert_codes_close("column codes", out_t, rot, max_frac=max(1e-4, 1.0 / out_t.size))
+    assert tkq.tkq_read_device_status() == 0
 
 
 def test_runs_on_caller_stream(cuda_device):
