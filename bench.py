@@ -47,9 +47,9 @@ KERNEL_OF = {
     "swiglu_t": "swiglu_cast_t",
 }
 KERNEL_SOURCES = {
-    "per_token_cast": ["per_token_cast.cu", "tkq_device.cuh"],
-    "swiglu_cast": ["swiglu_cast.cu", "tkq_device.cuh"],
-    "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh"],
+    "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
 }
 
 
@@ -248,11 +248,14 @@ def time_steps(prob: Problem, steps: int, warmup: int, stream, barrier):
 
 
 def time_flushed(prob: Problem, reps: int, stream, flush):
-    """Median per-launch time with L2 flushed before each launch."""
+    """Median per-launch time with L2 flushed before each launch.  The flush
+    READS a buffer four times the size of L2, which leaves L2 full of clean
+    lines (a write-based flush would leave dirty lines whose write-back lands
+    inside the timed launch)."""
     import torch
     ts = []
     for i in range(reps + 3):
-        flush.zero_()
+        flush.max()
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(stream)

@@ -16,7 +16,8 @@
 // Warps 0..15 are consumers; warp w owns tokens 8w..8w+7 of the tile and lane
 // l owns channels 4l..4l+3, i.e. an 8 x 4 block of y per thread, read from the
 // ring with conflict-free 8-byte shared loads (a warp reads one 256-byte row).
-// As soon as y is in registers the warp releases the stage to the producer.
+// Once its row codes are stored (they consume every value the warp read) the
+// warp releases the stage to the producer; the column work runs from registers.
 //   * Row groups (1 x 128 channels = one warp row): a butterfly absmax across
 //     the 32 lanes that halves the live values at each xor step (9 shuffles
 //     for 8 rows); lanes 4r..4r+3 then hold row r, compute its scale once and
@@ -74,9 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int CB = H >> 7;
-    const int64_t TB = T >> 7;
-    const int64_t n_tiles = TB * CB;
+    const uint32_t CB = static_cast<uint32_t>(H) >> 7;
+    const uint32_t TB = static_cast<uint32_t>(T >> 7);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -91,40 +91,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            int64_t issued = 0;
-            for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++issued) {
-                const int s = static_cast<int>(issued % kStages);
-                const uint32_t use = static_cast<uint32_t>(issued / kStages);
-                if (use > 0 &&
-                    !mbar_wait_bounded(&sm.empty[s], (use - 1) & 1u, &sm.abort, status)) {
-                    sm.abort = 1;
+            uint32_t issued = 0;
+            RingPos<kStages> pos;
+            for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), ++issued) {
+                if (!mbar_wait_bounded(&sm.empty[pos.stage], pos.phase ^ 1u, &sm.abort, status)) {
+                    *static_cast<volatile int*>(&sm.abort) = 1;
                     break;
                 }
-                const int64_t tb = tile / CB;
-                const int cb = static_cast<int>(tile - tb * CB);
-                mbar_arrive_expect_tx(&sm.full[s], kStageBytes);
-                tma_load_2d(sm.stage[s], &tmap, cb * 128, static_cast<int>(tb * 128), &sm.full[s]);
-                tma_load_2d(sm.stage[s] + kTileBytes, &tmap, H + cb * 128,
-                            static_cast<int>(tb * 128), &sm.full[s]);
+                const int y0 = static_cast<int>(tw.row * 128);
+                const int x0 = static_cast<int>(tw.col * 128);
+                uint64_t* full = &sm.full[pos.stage];
+                mbar_arrive_expect_tx(full, kStageBytes);
+                tma_load_2d(sm.stage[pos.stage], &tmap, x0, y0, full);
+                tma_load_2d(sm.stage[pos.stage] + kTileBytes, &tmap, H + x0, y0, full);
+                pos.advance();
             }
             // every copy this CTA issued must have landed before it may exit
-            const int64_t first = issued > kStages ? issued - kStages : 0;
-            for (int64_t k = first; k < issued; ++k)
-                mbar_wait_bounded(&sm.full[k % kStages], static_cast<uint32_t>(k / kStages) & 1u,
-                                  nullptr, status);
+            const uint32_t first = issued > kStages ? issued - kStages : 0;
+            for (uint32_t k = first; k < issued; ++k)
+                mbar_wait_bounded(&sm.full[k % kStages], (k / kStages) & 1u, nullptr, status);
         }
         return;
     }
 
     // ----------------------------------------------------------- consumers
     const int ct = threadIdx.x;  // 0 .. kConsumers-1
-    int64_t i = 0;
-    for (int64_t tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++i) {
-        const int s = static_cast<int>(i % kStages);
-        const uint32_t use = static_cast<uint32_t>(i / kStages);
-        const int64_t tb = tile / CB;
-        const int cb = static_cast<int>(tile - tb * CB);
-        const int64_t t0 = tb * 128;
+    RingPos<kStages> pos;
+    for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), pos.advance()) {
+        const int s = static_cast<int>(pos.stage);
+        const uint32_t tb = tw.row;
+        const int cb = static_cast<int>(tw.col);
+        const int64_t t0 = static_cast<int64_t>(tb) * 128;
         const int c0 = cb * 128;
         const int64_t row0 = t0 + warp * 8;
 
@@ -136,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = 0; r < 8; ++r) wt[r] = __ldg(w + row0 + r);
         }
 
-        const bool ok = mbar_wait_bounded(&sm.full[s], use & 1u, &sm.abort, status);
+        const bool ok = mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status);
 
         // ---- y = silu(g) * u [* w] for this thread's 8 x 4 block ----------
         float y[8][4];
@@ -159,8 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);  // stage may be refilled
 
         // ---- column maxima over this thread's 8 tokens -> shared table ----
         {
@@ -225,6 +220,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * H + c0) + lane, code);
             }
         }
+        // Release the stage only now: the row-code stores above consume all 32
+        // values this thread read from it, so its shared loads have completed
+        // before the arrive is issued (an arrive placed right after the loads
+        // can retire while they are pending, and the refill then overwrites
+        // their data).  The proxy fence orders these generic-proxy reads before
+        // the refill, which the TMA unit performs in the async proxy.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
 
         // all consumers agree whether to go on (a wait may have given up)
         if (named_bar_or(kBarConsumers, kConsumers, !ok)) {
@@ -275,40 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_tiled() {
-    static EncodeTiledFn fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
 template <int FMT, bool WEIGHTED>
 cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* out_t,
                    float* sf_t, int64_t T, int64_t H, cudaStream_t stream) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return cudaErrorNotSupported;
-    // x viewed as a 2-D bf16 tensor: inner extent 2H (gate | up), outer T rows
+    // x as a bf16 [T, 2H] matrix (gate | up), read in 128 x 128 boxes
     CUtensorMap map;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(2 * H), static_cast<cuuint64_t>(T)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(4 * H)};  // bytes between rows
-    const cuuint32_t box[2] = {128, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    if (!encode_bf16_2d(&map, x, 2 * H, T, 128, 128)) return cudaErrorInvalidValue;
 
     auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED>;
     const size_t smem = sizeof(SharedStorage) + 1024;

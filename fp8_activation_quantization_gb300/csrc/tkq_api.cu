@@ -68,6 +68,40 @@ int num_sms() {
     return v;
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+}  // namespace
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                    uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 unsigned int* device_status_word() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
@@ -102,10 +136,8 @@ tkq_status check_common(int64_t T, int64_t C, int group, int fmt) {
     if (group != 128) return TKQ_ERR_GROUP;
     if (C % group) return TKQ_ERR_SHAPE;
     if (fmt != TKQ_FMT_E4M3 && fmt != TKQ_FMT_E5M2) return TKQ_ERR_FMT;
-    // group indices are 32-bit in the SwiGLU kernel; 2^32 groups of 128 would
-    // be a 2 TiB input, far beyond one GPU
-    if (T > 0 && (T > (int64_t{1} << 40) || T * (C / group) >= (int64_t{1} << 32)))
-        return TKQ_ERR_SHAPE;
+    // TMA row coordinates are 32-bit; C beyond 2^30 is far beyond one GPU
+    if (T > INT32_MAX || C > (int64_t{1} << 30)) return TKQ_ERR_SHAPE;
     return TKQ_OK;
 }
 

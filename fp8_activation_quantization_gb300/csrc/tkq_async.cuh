@@ -91,6 +91,44 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Walk of a persistent CTA over a [rows x cols] grid of tiles (cols fastest):
+// tiles start, start + step, start + 2 step, ...  The row/column of each tile
+// is updated incrementally, so the loop needs no integer division.
+struct TileWalk {
+    uint32_t row, col, step_row, step_col, cols;
+    __device__ __forceinline__ TileWalk(uint32_t start, uint32_t step, uint32_t n_cols)
+        : cols(n_cols) {
+        row = start / n_cols;
+        col = start - row * n_cols;
+        step_row = step / n_cols;
+        step_col = step - step_row * n_cols;
+    }
+    __device__ __forceinline__ void next() {
+        row += step_row;
+        col += step_col;
+        if (col >= cols) {
+            col -= cols;
+            ++row;
+        }
+    }
+};
+
+// Position in a ring of S stages: the stage index and the parity of the
+// current use of that stage.  A consumer waits for `full[stage]` with parity
+// `phase`; the producer waits for `empty[stage]` with parity `phase ^ 1`, which
+// completes at once on the first use (the barrier's preceding phase counts as
+// complete), so neither side needs a first-round special case.
+template <int S>
+struct RingPos {
+    uint32_t stage = 0, phase = 0;
+    __device__ __forceinline__ void advance() {
+        if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
 // Barrier over `n` threads (a multiple of 32) on hardware barrier `id`.
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");

@@ -3,9 +3,18 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace tkq {
+
+// Tensor map of a row-major bf16 matrix [rows, cols] (row stride cols * 2
+// bytes) for 2-D TMA boxes of box_rows x box_cols elements, no swizzle,
+// out-of-range elements read as zero.  The driver entry point is looked up
+// through the runtime once.  Returns false if the driver call is unavailable
+// or rejects the arguments.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                    uint32_t box_cols, uint32_t box_rows);
 
 // Number of SMs of the current device (cached per device; the environment
 // variable TKQ_NUM_SMS overrides it for grid sizing experiments).
