@@ -8,7 +8,7 @@
 // GB300 design: a persistent CTA per (SM x 3) streams "chunks" of 32 rows x
 // one 128-channel block.  Warp 8 is the producer: one lane loads each chunk
 // with one 2-D TMA box per operand (gate, and up for SwiGLU: 8 KB each) into a
-// ring of stages, so a CTA keeps up to 56-64 KB of loads in flight.  Rows past
+// 64 KB ring of stages (8 plain or 4 SwiGLU chunks in flight per CTA).  Rows past
 // T are zero-filled by the TMA unit and never stored, so ragged T needs no
 // special path.  Warps 0..7 are consumers: warp w owns rows 4w..4w+3 of the
 // chunk, eight lanes per row (lane j holds elements [8j, 8j+8) and
@@ -29,17 +29,19 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRows = 32;                 // rows per chunk (4 per consumer warp)
-constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
+constexpr int kGroupsPerLane = 1;               // row groups per lane per chunk
+constexpr int kRows = 32 * kGroupsPerLane;      // rows per chunk
+constexpr int kBoxBytes = kRows * 256;          // one kRows x 128 bf16 box
 constexpr int kMinBlocksPerSm = 3;
+constexpr int kRingBytes = 65536;               // shared ring per CTA
 
 enum Mode { kPlain = 0, kSwiglu = 1, kSwigluWeighted = 2 };
 
 template <int MODE>
 struct ModeTraits {
     static constexpr int kOperands = MODE == kPlain ? 1 : 2;  // boxes per chunk
-    static constexpr int kStages = MODE == kPlain ? 7 : 4;
     static constexpr int kStageBytes = kOperands * kBoxBytes;
+    static constexpr int kStages = kRingBytes / kStageBytes;
 };
 
 template <int MODE>
@@ -104,61 +106,69 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     }
 
     // ----------------------------------------------------------- consumers
-    const int sub = lane >> 3;          // row within the warp's four
+    const int sub = lane >> 3;          // row within a block of four
     const int j = lane & 7;             // position within the group
-    const int r = warp * 4 + sub;       // row within the chunk
     RingPos<MT::kStages> pos;
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < RB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
         const int cb = static_cast<int>(tw.col);
-        const int64_t row = static_cast<int64_t>(tw.row) * kRows + r;
-        const bool live = row < T;
+        const int64_t row_base = static_cast<int64_t>(tw.row) * kRows;
 
-        float wt = 1.0f;
-        if constexpr (MODE == kSwigluWeighted) {
-            if (live) wt = __ldg(w + row);
+        float wt[kGroupsPerLane];
+#pragma unroll
+        for (int q = 0; q < kGroupsPerLane; ++q) {
+            wt[q] = 1.0f;
+            if constexpr (MODE == kSwigluWeighted) {
+                const int64_t row = row_base + q * 32 + warp * 4 + sub;
+                if (row < T) wt[q] = __ldg(w + row);
+            }
         }
 
         if (!mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status)) {
             *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
             break;
         }
-        const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
-        float v[16];
-        if constexpr (MODE == kPlain) {
-            unpack8(*reinterpret_cast<const uint4*>(p), v);
-            unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
-        } else {
-            float g[16], u[16];
-            unpack8(*reinterpret_cast<const uint4*>(p), g);
-            unpack8(*reinterpret_cast<const uint4*>(p + 128), g + 8);
-            unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes), u);
-            unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes + 128), u + 8);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                v[k] = swiglu(g[k], u[k]);
-                if constexpr (MODE == kSwigluWeighted) v[k] = __fmul_rn(v[k], wt);
-            }
-        }
-        float m = fmaxf(absmax8(v), absmax8(v + 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        float sc, inv;
-        group_scale<FMT>(m, sc, inv);
-        if (live) {
-            uint2* o = out + (row * C_out + cb * 128) / 8;
-            uint2 lo, hi;
+        for (int q = 0; q < kGroupsPerLane; ++q) {
+            const int r = q * 32 + warp * 4 + sub;  // row within the chunk
+            const int64_t row = row_base + r;
+            const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
+            float v[16];
             if constexpr (MODE == kPlain) {
-                lo = quantize8<FMT>(v, sc, inv);
-                hi = quantize8<FMT>(v + 8, sc, inv);
+                unpack8(*reinterpret_cast<const uint4*>(p), v);
+                unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
             } else {
-                lo = quantize8_mul<FMT>(v, inv);
-                hi = quantize8_mul<FMT>(v + 8, inv);
+                float g[16], u[16];
+                unpack8(*reinterpret_cast<const uint4*>(p), g);
+                unpack8(*reinterpret_cast<const uint4*>(p + 128), g + 8);
+                unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes), u);
+                unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes + 128), u + 8);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    v[k] = swiglu(g[k], u[k]);
+                    if constexpr (MODE == kSwigluWeighted) v[k] = __fmul_rn(v[k], wt[q]);
+                }
             }
-            st_stream(o + j, lo);
-            st_stream(o + 8 + j, hi);
-            if (j == 0) st_stream(sf + row * CB + cb, sc);
+            float m = fmaxf(absmax8(v), absmax8(v + 8));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            float sc, inv;
+            group_scale<FMT>(m, sc, inv);
+            if (row < T) {
+                uint2* o = out + (row * C_out + cb * 128) / 8;
+                uint2 lo, hi;
+                if constexpr (MODE == kPlain) {
+                    lo = quantize8<FMT>(v, sc, inv);
+                    hi = quantize8<FMT>(v + 8, sc, inv);
+                } else {
+                    lo = quantize8_mul<FMT>(v, inv);
+                    hi = quantize8_mul<FMT>(v + 8, inv);
+                }
+                st_stream(o + j, lo);
+                st_stream(o + 8 + j, hi);
+                if (j == 0) st_stream(sf + row * CB + cb, sc);
+            }
         }
         // Release the stage only now: the stores above consume every value
         // read from it, so the shared loads have completed before the arrive
@@ -182,9 +192,6 @@ cudaError_t launch(const void* x, const float* w, void* out, float* sf, int64_t 
 
     auto* k = &row_cast_kernel<FMT, MODE>;
     const size_t smem = sizeof(RowSmem<MODE>) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint2*>(out), sf, T,

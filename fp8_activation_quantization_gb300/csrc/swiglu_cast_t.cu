@@ -288,9 +288,6 @@ cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* ou
 
     auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED>;
     const size_t smem = sizeof(SharedStorage) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
     const int64_t n_tiles = (T / 128) * (H / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,

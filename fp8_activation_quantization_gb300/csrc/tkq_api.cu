@@ -5,6 +5,9 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <functional>
+#include <mutex>
+#include <unordered_map>
 
 #include <cuda_runtime.h>
 
@@ -116,12 +119,50 @@ unsigned int* device_status_word() {
     return static_cast<unsigned int*>(p);
 }
 
+namespace {
+// Per (kernel, device, threads, smem): resident blocks per SM.  The first
+// launch on a device raises the kernel's dynamic shared-memory limit and asks
+// the occupancy calculator; later launches reuse the answer, which keeps both
+// calls off the per-launch host path.
+struct OccKey {
+    const void* kernel;
+    int dev, threads;
+    size_t smem;
+    bool operator==(const OccKey& o) const {
+        return kernel == o.kernel && dev == o.dev && threads == o.threads && smem == o.smem;
+    }
+};
+struct OccKeyHash {
+    size_t operator()(const OccKey& k) const {
+        return std::hash<const void*>()(k.kernel) ^ (static_cast<size_t>(k.dev) << 1) ^
+               (static_cast<size_t>(k.threads) << 8) ^ (k.smem << 20);
+    }
+};
+std::mutex g_occ_mutex;
+std::unordered_map<OccKey, int, OccKeyHash> g_occ;
+}  // namespace
+
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const OccKey key{kernel, dev, threads, smem};
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
-            cudaSuccess ||
-        per_sm <= 0)
-        per_sm = 1;
+    {
+        std::lock_guard<std::mutex> lock(g_occ_mutex);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) per_sm = it->second;
+    }
+    if (per_sm == 0) {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) !=
+                cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+        std::lock_guard<std::mutex> lock(g_occ_mutex);
+        g_occ[key] = per_sm;
+    }
     const int64_t cap = static_cast<int64_t>(num_sms()) * per_sm;
     const int64_t g = blocks_needed < cap ? blocks_needed : cap;
     return static_cast<int>(g > 0 ? g : 1);
