@@ -118,8 +118,11 @@ def _configure(lib):
     lib.ora_swiglu_values.argtypes = [p, p, i64, i64, p]
     lib.ora_swiglu_cast.argtypes = [p, p, i64, i64, i64, i, p, p]
     lib.ora_swiglu_cast_t.argtypes = [p, p, i64, i64, i64, i, p, p, p, p]
+    lib.ora_swiglu_backward_values.argtypes = [p, p, p, i64, i64, p]
+    lib.ora_swiglu_backward_cast.argtypes = [p, p, p, i64, i64, i64, i, p, p]
     for f in ("ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
-              "ora_swiglu_values", "ora_swiglu_cast", "ora_swiglu_cast_t"):
+              "ora_swiglu_values", "ora_swiglu_cast", "ora_swiglu_cast_t",
+              "ora_swiglu_backward_values", "ora_swiglu_backward_cast"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -313,3 +316,48 @@ def swiglu_cast_t(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
 
     _row_parallel(T, threads, body, align=group)
     return out, sf, out_t, sf_t
+
+
+def swiglu_backward_values(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray | None = None,
+                           threads: int = 1):
+    """x_bits: uint16 [T, 2H] (gate | up), dy_bits: uint16 [T, H] -> fp32 [T, 2H] = [dg | du]."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    dy_bits = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    assert dy_bits.shape == (T, H)
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    grad = np.empty((T, 2 * H), np.float32)
+
+    def body(a, b):
+        _check(lib.ora_swiglu_backward_values(_ptr(x_bits[a:b]), _ptr(dy_bits[a:b]),
+                                              None if w is None else _ptr(w[a:b]), b - a, H,
+                                              _ptr(grad[a:b])), "swiglu_backward_values")
+
+    _row_parallel(T, threads, body)
+    return grad
+
+
+def swiglu_backward_cast(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray | None = None,
+                         fmt="e4m3", group: int = 128, threads: int = 1):
+    """-> (codes [T, 2H] of [dg | du], sf [T, 2H/group])."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    dy_bits = np.ascontiguousarray(dy_bits, dtype=np.uint16)
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    assert dy_bits.shape == (T, H)
+    w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
+    out = np.empty((T, 2 * H), np.uint8)
+    sf = np.empty((T, 2 * H // group), np.float32)
+    f = _fmt(fmt)
+
+    def body(a, b):
+        _check(lib.ora_swiglu_backward_cast(_ptr(x_bits[a:b]), _ptr(dy_bits[a:b]),
+                                            None if w is None else _ptr(w[a:b]), b - a, H, group,
+                                            f, _ptr(out[a:b]), _ptr(sf[a:b])),
+               "swiglu_backward_cast")
+
+    _row_parallel(T, threads, body)
+    return out, sf

@@ -246,3 +246,40 @@ int ora_swiglu_cast_t(const uint16_t* x, const float* w, int64_t T, int64_t H,
     free(y);
     return rc;
 }
+
+/* SwiGLU backward: the derivative of y = silu(g) * u [* w] ("TileKernels 与
+ * DeepGEMM 的分界线" (chatdocs.ruinique.com) §2 and §6 step 13 name the
+ * operator; no formula is given, so this is the textbook one), evaluated in
+ * binary64 and rounded once to binary32. */
+int ora_swiglu_backward_values(const uint16_t* x, const uint16_t* dy, const float* w,
+                               int64_t T, int64_t H, float* grad) {
+    if (T < 0 || H < 0) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t* row = x + t * 2 * H;
+        const double wt = w ? (double)w[t] : 1.0;
+        for (int64_t c = 0; c < H; ++c) {
+            const double g = (double)ora_bf16_to_f32(row[c]);
+            const double u = (double)ora_bf16_to_f32(row[H + c]);
+            const double d = (double)ora_bf16_to_f32(dy[t * H + c]);
+            const double sig = 1.0 / (1.0 + exp(-g));
+            const double silu = g * sig;
+            const double dsilu = sig * (1.0 + g * (1.0 - sig));
+            grad[t * 2 * H + c] = (float)(d * u * dsilu * wt);
+            grad[t * 2 * H + H + c] = (float)(d * silu * wt);
+        }
+    }
+    return 0;
+}
+
+int ora_swiglu_backward_cast(const uint16_t* x, const uint16_t* dy, const float* w,
+                             int64_t T, int64_t H, int64_t group, int fmt,
+                             uint8_t* out, float* sf) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || H < 0 || group <= 0 || H % group) return -1;
+    float* g = (float*)malloc((size_t)(T * 2 * H > 0 ? T * 2 * H : 1) * sizeof(float));
+    if (!g) return -1;
+    int rc = ora_swiglu_backward_values(x, dy, w, T, H, g);
+    if (!rc) rc = ora_cast_rows_f32(g, T, 2 * H, group, fmt, out, sf);
+    free(g);
+    return rc;
+}

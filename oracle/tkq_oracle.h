@@ -104,6 +104,23 @@ int ora_swiglu_cast_t(const uint16_t* x, const float* w, int64_t T, int64_t H,
                       int64_t group, int fmt, uint8_t* out, float* sf,
                       uint8_t* out_t, float* sf_t);
 
+/* Gradient of y = silu(g) * u [* w] for a bf16 [T, 2H] gate|up input and a
+ * bf16 [T, H] upstream gradient dy, written as the fp32 [T, 2H] matrix
+ * [dg | du]:
+ *   dg = dy * u * sigma(g) * (1 + g * (1 - sigma(g))) [* w]
+ *   du = dy * silu(g) [* w],   sigma(g) = 1 / (1 + exp(-g)), silu = g sigma(g).
+ * The pages name swiglu_backward_and_per_token_cast but give no formula and
+ * no precision, so this is the textbook derivative evaluated in binary64 and
+ * rounded once to binary32. */
+int ora_swiglu_backward_values(const uint16_t* x, const uint16_t* dy, const float* w,
+                               int64_t T, int64_t H, float* grad);
+
+/* The gradient above followed by the per-token cast of [dg | du]:
+ * out [T, 2H] codes, sf [T, 2H/group]. */
+int ora_swiglu_backward_cast(const uint16_t* x, const uint16_t* dy, const float* w,
+                             int64_t T, int64_t H, int64_t group, int fmt,
+                             uint8_t* out, float* sf);
+
 #ifdef __cplusplus
 }
 #endif

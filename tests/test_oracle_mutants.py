@@ -42,6 +42,12 @@ MUTANTS = [
      "d->maxval = 61440.0; d->maxcode = 0x7B;"),
     ("scale from the first element", "const float s = ora_group_scale(amax, fmt);",
      "const float s = ora_group_scale(fabsf(v[0]), fmt);"),
+    ("backward: 1 + sigma in dsilu", "const double dsilu = sig * (1.0 + g * (1.0 - sig));",
+     "const double dsilu = sig * (1.0 + g * (1.0 + sig));"),
+    ("backward: dg and du swapped", "grad[t * 2 * H + c] = (float)(d * u * dsilu * wt);",
+     "grad[t * 2 * H + H + c] = (float)(d * u * dsilu * wt); continue;"),
+    ("backward: weight dropped from du", "grad[t * 2 * H + H + c] = (float)(d * silu * wt);",
+     "grad[t * 2 * H + H + c] = (float)(d * silu);"),
 ]
 
 # cheapest first: most mistakes are caught by the hand-worked fixtures
@@ -53,6 +59,8 @@ CHECKS = [
     (pins.test_swiglu_orientation_and_special_cases, {}),
     (pins.test_swiglu_weight_one_and_weight_product, {}),
     (pins.test_swiglu_vs_binary64, {}),
+    (pins.test_swiglu_backward_special_cases, {}),
+    (pins.test_swiglu_backward_vs_finite_differences, {}),
     (pins.test_cols_equal_rows_of_transpose, {"fmt": "e4m3"}),
     (pins.test_cols_index_orientation, {}),
     (pins.test_scale_floor_amax_code_and_error_bound, {"fmt": "e4m3"}),

@@ -411,3 +411,75 @@ def test_invalid_arguments_raise():
         oracle.per_token_cast(np.zeros((2, 100), np.uint16))
     with pytest.raises(ValueError):
         oracle.swiglu_cast_t(np.zeros((100, 256), np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU backward
+# ---------------------------------------------------------------------------
+
+def _bwd_inputs(T=32, H=128, seed=51):
+    rng = np.random.default_rng(seed)
+    x = _swiglu_input(T, H, seed=seed)
+    dy = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    w = rng.uniform(0.01, 1.0, T).astype(np.float32)
+    return x, dy, w
+
+
+def test_swiglu_backward_vs_finite_differences():
+    """Central differences of the forward formula g / (1 + exp(-g)) * u * w in
+    binary64: independent of the closed-form derivative the oracle uses."""
+    x, dy, w = _bwd_inputs()
+    H = x.shape[1] // 2
+    grad = oracle.swiglu_backward_values(x, dy, w).astype(np.float64)
+    f = synth.bf16_bits_to_f32(x).astype(np.float64)
+    g, u = f[:, :H], f[:, H:]
+    d = synth.bf16_bits_to_f32(dy).astype(np.float64)
+    wt = w.astype(np.float64)[:, None]
+    y = lambda gg, uu: gg / (1.0 + np.exp(-gg)) * uu * wt
+    h = 1e-5
+    fd_g = d * (y(g + h, u) - y(g - h, u)) / (2 * h)
+    fd_u = d * (y(g, u + h) - y(g, u - h)) / (2 * h)
+    scale = np.abs(d * wt) * (np.abs(u) + np.abs(g) + 1.0)
+    assert np.all(np.abs(grad[:, :H] - fd_g) <= 1e-6 * scale + 1e-9)
+    assert np.all(np.abs(grad[:, H:] - fd_u) <= 1e-6 * scale + 1e-9)
+
+
+def test_swiglu_backward_vs_torch_autograd():
+    x, dy, w = _bwd_inputs(seed=53)
+    H = x.shape[1] // 2
+    grad = oracle.swiglu_backward_values(x, dy, w).astype(np.float64)
+    f = torch.from_numpy(synth.bf16_bits_to_f32(x).astype(np.float64))
+    g = f[:, :H].clone().requires_grad_(True)
+    u = f[:, H:].clone().requires_grad_(True)
+    d = torch.from_numpy(synth.bf16_bits_to_f32(dy).astype(np.float64))
+    y = torch.nn.functional.silu(g) * u * torch.from_numpy(w.astype(np.float64))[:, None]
+    y.backward(d)
+    ref = np.concatenate([g.grad.numpy(), u.grad.numpy()], axis=1)
+    tol = 2.0 ** -23 * np.abs(ref) + 1e-30
+    assert np.all(np.abs(grad - ref) <= tol)
+
+
+def test_swiglu_backward_special_cases():
+    H = 128
+    x = np.zeros((3, 2 * H), np.uint16)
+    dy = np.zeros((3, H), np.uint16)
+    one = synth.f32_to_bf16_bits(np.array([1.0], np.float32))[0]
+    three = synth.f32_to_bf16_bits(np.array([3.0], np.float32))[0]
+    x[0, H:] = three            # g = 0, u = 3, dy = 1: dg = 0.5 * 3, du = 0
+    dy[0] = one
+    x[1, :H] = three            # dy = 0 everywhere in row 1: all zero
+    x[2, :H] = three            # g = 3, u = 0, dy = 1: dg = 0, du = silu(3)
+    dy[2] = one
+    grad = oracle.swiglu_backward_values(x, dy)
+    assert np.all(grad[0, :H] == 1.5) and np.all(grad[0, H:] == 0)
+    assert np.all(grad[1] == 0)
+    assert np.all(grad[2, :H] == 0)
+    assert np.allclose(grad[2, H:], 3.0 / (1 + math.exp(-3.0)), rtol=1e-7)
+
+
+def test_swiglu_backward_cast_is_cast_of_values():
+    x, dy, w = _bwd_inputs(T=64, H=256, seed=57)
+    grad = oracle.swiglu_backward_values(x, dy, w)
+    c1, s1 = oracle.cast_rows_f32(grad)
+    c2, s2 = oracle.swiglu_backward_cast(x, dy, w)
+    assert np.array_equal(c1, c2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
