@@ -45,11 +45,13 @@ KERNEL_OF = {
     "swiglu": "swiglu_cast",
     "swiglu_moe": "swiglu_cast",
     "swiglu_t": "swiglu_cast_t",
+    "swiglu_bwd": "swiglu_backward_cast",
 }
 KERNEL_SOURCES = {
     "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_backward_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
 }
 
 
@@ -59,6 +61,9 @@ def algorithmic_bytes(workload: str, T: int, C: int, weighted: bool) -> int:
     if kern == "per_token_cast":
         return T * C * 2 + T * C + T * (C // 128) * 4
     H = C // 2
+    if kern == "swiglu_backward_cast":
+        # read gate|up and dy, write codes and scales of [dg | du]
+        return T * 4 * H + T * 2 * H + T * 2 * H + T * (2 * H // 128) * 4 + (T * 4 if weighted else 0)
     b = T * 2 * H * 2 + T * H + T * (H // 128) * 4
     if weighted:
         b += T * 4
@@ -197,10 +202,20 @@ class Problem:
         self.dev = dev
         self.x = torch.from_numpy(self.x_host.view(np.int16)).to(dev).view(torch.bfloat16)
         self.w = None if self.w_host is None else torch.from_numpy(self.w_host).to(dev)
+        self.dy_host = d.get("dy")
+        self.dy = None if self.dy_host is None else \
+            torch.from_numpy(self.dy_host.view(np.int16)).to(dev).view(torch.bfloat16)
         T, C = self.T, self.C
         fcode = 0 if fmt == "e4m3" else 1
         P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
-        if self.kern == "per_token_cast":
+        if self.kern == "swiglu_backward_cast":
+            H = C // 2
+            self.out = torch.empty((T, 2 * H), dtype=torch.uint8, device=dev)
+            self.sf = torch.empty((T, 2 * H // 128), dtype=torch.float32, device=dev)
+            self.outputs = [self.out, self.sf]
+            args = (P(self.x), P(self.dy), P(self.w), P(self.out), P(self.sf), T, H, 128, fcode)
+            fn = tkq.tkq_swiglu_backward_cast
+        elif self.kern == "per_token_cast":
             self.out = torch.empty((T, C), dtype=torch.uint8, device=dev)
             self.sf = torch.empty((T, C // 128), dtype=torch.float32, device=dev)
             args = (P(self.x), P(self.out), P(self.sf), T, C, 128, fcode)
@@ -309,7 +324,10 @@ def e2e_steps(prob: Problem, steps: int, stream):
     x_dev = [torch.empty_like(prob.x.view(torch.int16)) for _ in range(2)]
     w_dev = [None if w_pin is None else torch.empty_like(prob.w) for _ in range(2)]
     outs_dev = [[torch.empty_like(o) for o in prob.outputs] for _ in range(2)]
-    h2d = x_pin.numel() * 2 + (0 if w_pin is None else w_pin.numel() * 4)
+    dy_pin = None if prob.dy_host is None else torch.from_numpy(prob.dy_host.view(np.int16)).pin_memory()
+    dy_dev = [None if dy_pin is None else torch.empty_like(dy_pin, device=dev) for _ in range(2)]
+    h2d = x_pin.numel() * 2 + (0 if w_pin is None else w_pin.numel() * 4) + \
+        (0 if dy_pin is None else dy_pin.numel() * 2)
     d2h = sum(o.numel() * o.element_size() for o in prob.outputs)
     s_in, s_out, s_cmp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
     in_done = [torch.cuda.Event() for _ in range(2)]
@@ -325,6 +343,8 @@ def e2e_steps(prob: Problem, steps: int, stream):
             x_dev[b].copy_(x_pin, non_blocking=True)
             if w_pin is not None:
                 w_dev[b].copy_(w_pin, non_blocking=True)
+            if dy_pin is not None:
+                dy_dev[b].copy_(dy_pin, non_blocking=True)
             in_done[b].record(s_in)
         s_cmp.wait_event(in_done[b])
         if i >= 2:
@@ -334,6 +354,10 @@ def e2e_steps(prob: Problem, steps: int, stream):
             od = outs_dev[b]
             if prob.kern == "per_token_cast":
                 res = tkq.per_token_cast(xb, fmt, out=od[0].view(_fp8(fmt)), out_sf=od[1])
+            elif prob.kern == "swiglu_backward_cast":
+                res = tkq.swiglu_backward_and_per_token_cast(
+                    xb, dy_dev[b].view(torch.bfloat16), fmt, topk_weights=w_dev[b],
+                    out=od[0].view(_fp8(fmt)), out_sf=od[1])
             else:
                 res = tkq.swiglu_forward_and_per_token_cast(
                     xb, fmt, topk_weights=w_dev[b], with_transpose=prob.kern == "swiglu_cast_t",
@@ -366,21 +390,28 @@ def _fp8(fmt):
     return torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
 
 
+def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
+    """The oracle for one kernel on the first `rows` rows of a workload dict."""
+    import oracle
+    x = d["x"][:rows]
+    w = None if d.get("w") is None else d["w"][:rows]
+    if kern == "per_token_cast":
+        return oracle.per_token_cast(x, fmt, threads=threads)
+    if kern == "swiglu_cast":
+        return oracle.swiglu_cast(x, w, fmt, threads=threads)
+    if kern == "swiglu_backward_cast":
+        return oracle.swiglu_backward_cast(x, d["dy"][:rows], w, fmt, threads=threads)
+    return oracle.swiglu_cast_t(x, w, fmt, threads=threads)
+
+
 def cpu_baseline_single_thread(workload: str, fmt: str, rows: int = 32768):
     """The oracle, as it stands, on one host core over the first `rows` rows."""
-    import oracle
     from fp8_activation_quantization_gb300 import synth
     d = synth.workload(workload, rows=rows)
     x, w = d["x"], d.get("w")
     T, C = x.shape
-    kern = KERNEL_OF[workload]
     t0 = time.perf_counter()
-    if kern == "per_token_cast":
-        oracle.per_token_cast(x, fmt)
-    elif kern == "swiglu_cast":
-        oracle.swiglu_cast(x, w, fmt)
-    else:
-        oracle.swiglu_cast_t(x, w, fmt)
+    run_oracle(KERNEL_OF[workload], d, T, fmt)
     dt = time.perf_counter() - t0
     b = algorithmic_bytes(workload, T, C, w is not None)
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -502,7 +533,8 @@ def other_workloads(dev, stream, peak, args):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     out = {}
     for name, fmt in [("plain_small", "e4m3"), ("plain_outlier", "e4m3"), ("plain_outlier", "e5m2"),
-                      ("swiglu", "e4m3"), ("swiglu_moe", "e4m3"), ("swiglu_t", "e4m3")]:
+                      ("swiglu", "e4m3"), ("swiglu_moe", "e4m3"), ("swiglu_t", "e4m3"),
+                      ("swiglu_bwd", "e4m3")]:
         prob = Problem(name, fmt, dev)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
@@ -540,14 +572,7 @@ def run_reference(args):
     x_all, w_all = d["x"], d.get("w")
 
     def step(r):
-        x = x_all[:r]
-        w = None if w_all is None else w_all[:r]
-        if kern == "per_token_cast":
-            oracle.per_token_cast(x, args.fmt, threads=cores)
-        elif kern == "swiglu_cast":
-            oracle.swiglu_cast(x, w, args.fmt, threads=cores)
-        else:
-            oracle.swiglu_cast_t(x, w, args.fmt, threads=cores)
+        run_oracle(kern, d, r, args.fmt, threads=cores)
 
     t0 = time.perf_counter()
     step(min(rows, x_all.shape[0]))

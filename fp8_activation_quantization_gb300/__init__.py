@@ -20,8 +20,9 @@ import threading
 
 __all__ = [
     "TkqError", "library_path", "load_library", "tkq_per_token_cast", "tkq_swiglu_cast",
-    "tkq_swiglu_cast_t", "tkq_status_string", "per_token_cast",
-    "swiglu_forward_and_per_token_cast", "FMT_E4M3", "FMT_E5M2", "GROUP",
+    "tkq_swiglu_cast_t", "tkq_swiglu_backward_cast", "tkq_status_string", "per_token_cast",
+    "swiglu_forward_and_per_token_cast", "swiglu_backward_and_per_token_cast",
+    "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
 ]
 
 FMT_E4M3 = 0
@@ -67,6 +68,8 @@ def load_library():
         lib.tkq_status_string.restype = ctypes.c_char_p
         lib.tkq_version.argtypes = []
         lib.tkq_version.restype = i
+        lib.tkq_swiglu_backward_cast.argtypes = [p, p, p, p, p, i64, i64, i, i, p]
+        lib.tkq_swiglu_backward_cast.restype = i
         lib.tkq_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
         lib.tkq_read_device_status.restype = i
         lib.tkq_selftest_wait_timeout.argtypes = [i64, p]
@@ -111,6 +114,11 @@ def tkq_swiglu_cast(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, stream=None)
 def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
                       stream=None) -> int:
     return load_library().tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group, fmt, stream)
+
+
+def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
+                             stream=None) -> int:
+    return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
 
 
 # ---------------------------------------------------------------------------
@@ -205,3 +213,34 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
         if st:
             raise TkqError(st, "tkq_swiglu_cast_t")
         return out, out_sf, out_t, out_sf_t
+
+
+def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int = GROUP,
+                                       topk_weights=None, out=None, out_sf=None):
+    """Gradients of y = silu(gate) * up [* w] from dy, cast per token.
+    x: bf16 [T, 2H] (gate | up); dy: bf16 [T, H] -> (codes [T, 2H] of [dg | du],
+    scales [T, 2H/128])."""
+    import torch
+    _check_input(x)
+    _check_input(dy, "dy")
+    f = _fmt_code(fmt)
+    T, H2 = x.shape
+    H = H2 // 2
+    if H2 % 2 or tuple(dy.shape) != (T, H) or dy.device != x.device:
+        raise ValueError("dy must be [T, H] for x [T, 2H], on the same device")
+    if topk_weights is not None:
+        if (topk_weights.dtype != torch.float32 or topk_weights.numel() != T
+                or not topk_weights.is_contiguous() or topk_weights.device != x.device):
+            raise TypeError("topk_weights must be a contiguous fp32 tensor of T elements on x's device")
+    g = max(num_per_channels, 1)
+    if out is None:
+        out = torch.empty((T, 2 * H), dtype=_fp8_dtype(f), device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty((T, 2 * H // g), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = tkq_swiglu_backward_cast(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(out),
+                                      _ptr(out_sf), T, H, num_per_channels, f,
+                                      _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_swiglu_backward_cast")
+    return out, out_sf

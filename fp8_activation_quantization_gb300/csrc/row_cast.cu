@@ -1,22 +1,26 @@
 // row_cast.cu -- the per-token-group FP8 casts with row-major outputs:
 //   * the plain per_token_cast of a bf16 [T, C] matrix ("DeepSeek开源TileKernels：
-//     用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2), and
+//     用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2);
 //   * swiglu_forward_and_per_token_cast of a bf16 [T, 2H] gate|up matrix,
-//     optionally times a per-row routing weight (same page, §3.3).
+//     optionally times a per-row routing weight (same page, §3.3);
+//   * swiglu_backward_and_per_token_cast ("TileKernels 与 DeepGEMM 的分界线"
+//     (chatdocs.ruinique.com) §2 and §6 step 13): the gradients [dg | du] of
+//     the same SwiGLU from the upstream gradient dy, cast per token.
 // Per 1x128 group: absmax -> scale s = max(amax, 1e-4) / fmt_max -> FP8 codes.
 //
-// GB300 design: a persistent CTA per (SM x 3) streams "chunks" of 32 rows x
-// one 128-channel block.  Warp 8 is the producer: one lane loads each chunk
-// with one 2-D TMA box per operand (gate, and up for SwiGLU: 8 KB each) into a
-// 64 KB ring of stages (8 plain or 4 SwiGLU chunks in flight per CTA).  Rows past
-// T are zero-filled by the TMA unit and never stored, so ragged T needs no
-// special path.  Warps 0..7 are consumers: warp w owns rows 4w..4w+3 of the
-// chunk, eight lanes per row (lane j holds elements [8j, 8j+8) and
-// [64+8j, 64+8j+8), read as two conflict-free 16-byte shared loads), the
-// group absmax is three xor shuffles, and codes leave as 8-byte stores (eight
-// lanes write one 64-byte run).  The plain cast writes the codes of the exact
-// binary32 quotient fl(x / s) (see `quotient`), so it is bit-exact; the SwiGLU
-// casts write the codes of y * fl(1 / s) as the page's kernel does.
+// GB300 design: persistent CTAs (3 per SM) stream "chunks" of 32 rows x one
+// 128-channel block.  Warp 8 is the producer: one lane loads each chunk with
+// one 2-D TMA box per operand (32 x 128 bf16 = 8 KB: x; or gate and up; or
+// gate, up and dy) into a shared ring of 64-72 KB (8 plain, 4 SwiGLU or 3
+// backward chunks in flight per CTA).  Rows past T are zero-filled by the TMA
+// unit and never stored, so ragged T needs no special path.  Warps 0..7 are
+// consumers: warp w owns rows 4w..4w+3 of the chunk, eight lanes per row
+// (lane j holds elements [8j, 8j+8) and [64+8j, 64+8j+8), read as two
+// conflict-free 16-byte shared loads per operand), the group absmax is three
+// xor shuffles, and codes leave as 8-byte stores (eight lanes write one
+// 64-byte run).  The plain cast writes the codes of the exact binary32
+// quotient fl(x / s) (see `quotient`), so it is bit-exact; the SwiGLU casts
+// write the codes of y * fl(1 / s) as the page's kernel does.
 // Every mbarrier wait is bounded (tkq_async.cuh).
 #include <cuda.h>
 
@@ -29,18 +33,18 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kGroupsPerLane = 1;               // row groups per lane per chunk
-constexpr int kRows = 32 * kGroupsPerLane;      // rows per chunk
-constexpr int kBoxBytes = kRows * 256;          // one kRows x 128 bf16 box
-constexpr int kMinBlocksPerSm = 3;
-constexpr int kRingBytes = 65536;               // shared ring per CTA
+constexpr int kRows = 32;                 // rows per chunk (4 per consumer warp)
+constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
 
-enum Mode { kPlain = 0, kSwiglu = 1, kSwigluWeighted = 2 };
+enum Mode { kPlain, kSwiglu, kSwigluWeighted, kBackward, kBackwardWeighted };
 
 template <int MODE>
 struct ModeTraits {
-    static constexpr int kOperands = MODE == kPlain ? 1 : 2;  // boxes per chunk
+    static constexpr bool kBwd = MODE == kBackward || MODE == kBackwardWeighted;
+    static constexpr bool kWeighted = MODE == kSwigluWeighted || MODE == kBackwardWeighted;
+    static constexpr int kOperands = MODE == kPlain ? 1 : (kBwd ? 3 : 2);  // boxes per chunk
     static constexpr int kStageBytes = kOperands * kBoxBytes;
+    static constexpr int kRingBytes = kBwd ? 3 * kStageBytes : 65536;
     static constexpr int kStages = kRingBytes / kStageBytes;
 };
 
@@ -52,9 +56,45 @@ struct alignas(1024) RowSmem {
     int abort;
 };
 
+// absmax of one 1x128 group held by eight lanes (16 values each), its scale,
+// and the codes and scale stored for a live row.  EXACT selects the codes of
+// the exact quotient (plain cast) or of the product by the reciprocal scale.
+template <int FMT, bool EXACT>
+__device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, float* sfp,
+                                           int j) {
+    float m = fmaxf(absmax8(v), absmax8(v + 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    float sc, inv;
+    group_scale<FMT>(m, sc, inv);
+    if (live) {
+        uint2 lo, hi;
+        if constexpr (EXACT) {
+            lo = quantize8<FMT>(v, sc, inv);
+            hi = quantize8<FMT>(v + 8, sc, inv);
+        } else {
+            lo = quantize8_mul<FMT>(v, inv);
+            hi = quantize8_mul<FMT>(v + 8, inv);
+        }
+        st_stream(o + j, lo);
+        st_stream(o + 8 + j, hi);
+        if (j == 0) st_stream(sfp, sc);
+    }
+}
+
+// 16 bf16 of one operand for lane j: elements [8j, 8j+8) and [64+8j, 64+8j+8).
+__device__ __forceinline__ void load16(const uint8_t* p, float* v) {
+    unpack8(*reinterpret_cast<const uint4*>(p), v);
+    unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
+}
+
+// tmap: x [T, C] (plain) or [T, 2H] (gate | up); tmap_dy: dy [T, H] (backward
+// only).  C_out: channels per output operand (C or H).
 template <int FMT, int MODE>
-__global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
-    row_cast_kernel(const __grid_constant__ CUtensorMap tmap, const float* __restrict__ w,
+__global__ void __launch_bounds__(kThreads, 3)
+    row_cast_kernel(const __grid_constant__ CUtensorMap tmap,
+                    const __grid_constant__ CUtensorMap tmap_dy, const float* __restrict__ w,
                     uint2* __restrict__ out, float* __restrict__ sf, int64_t T, int C_out,
                     unsigned int* __restrict__ status) {
     using MT = ModeTraits<MODE>;
@@ -89,11 +129,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
                 }
                 const int y0 = static_cast<int>(tw.row * kRows);
                 const int x0 = static_cast<int>(tw.col * 128);
+                uint8_t* dst = sm.stage[pos.stage];
                 uint64_t* full = &sm.full[pos.stage];
                 mbar_arrive_expect_tx(full, MT::kStageBytes);
-                tma_load_2d(sm.stage[pos.stage], &tmap, x0, y0, full);
-                if constexpr (MT::kOperands == 2)
-                    tma_load_2d(sm.stage[pos.stage] + kBoxBytes, &tmap, C_out + x0, y0, full);
+                tma_load_2d(dst, &tmap, x0, y0, full);
+                if constexpr (MT::kOperands >= 2)
+                    tma_load_2d(dst + kBoxBytes, &tmap, C_out + x0, y0, full);
+                if constexpr (MT::kOperands == 3)
+                    tma_load_2d(dst + 2 * kBoxBytes, &tmap_dy, x0, y0, full);
                 pos.advance();
             }
             // every copy this CTA issued must have landed before it may exit
@@ -106,69 +149,60 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
     }
 
     // ----------------------------------------------------------- consumers
-    const int sub = lane >> 3;          // row within a block of four
+    const int sub = lane >> 3;          // row within the warp's four
     const int j = lane & 7;             // position within the group
+    const int r = warp * 4 + sub;       // row within the chunk
+    // output row pitch (elements) and scales per output row
+    const int64_t out_ld = MT::kBwd ? 2 * static_cast<int64_t>(C_out) : C_out;
+    const uint32_t sf_ld = MT::kBwd ? 2 * CB : CB;
     RingPos<MT::kStages> pos;
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < RB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
         const int cb = static_cast<int>(tw.col);
-        const int64_t row_base = static_cast<int64_t>(tw.row) * kRows;
+        const int64_t row = static_cast<int64_t>(tw.row) * kRows + r;
+        const bool live = row < T;
 
-        float wt[kGroupsPerLane];
-#pragma unroll
-        for (int q = 0; q < kGroupsPerLane; ++q) {
-            wt[q] = 1.0f;
-            if constexpr (MODE == kSwigluWeighted) {
-                const int64_t row = row_base + q * 32 + warp * 4 + sub;
-                if (row < T) wt[q] = __ldg(w + row);
-            }
+        float wt = 1.0f;
+        if constexpr (MT::kWeighted) {
+            if (live) wt = __ldg(w + row);
         }
 
         if (!mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status)) {
             *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
             break;
         }
-#pragma unroll
-        for (int q = 0; q < kGroupsPerLane; ++q) {
-            const int r = q * 32 + warp * 4 + sub;  // row within the chunk
-            const int64_t row = row_base + r;
-            const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
+        const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
+        uint2* o = out + (row * out_ld + cb * 128) / 8;
+        float* sfp = sf + row * sf_ld + cb;
+        if constexpr (MODE == kPlain) {
             float v[16];
-            if constexpr (MODE == kPlain) {
-                unpack8(*reinterpret_cast<const uint4*>(p), v);
-                unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
-            } else {
-                float g[16], u[16];
-                unpack8(*reinterpret_cast<const uint4*>(p), g);
-                unpack8(*reinterpret_cast<const uint4*>(p + 128), g + 8);
-                unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes), u);
-                unpack8(*reinterpret_cast<const uint4*>(p + kBoxBytes + 128), u + 8);
+            load16(p, v);
+            emit_group<FMT, true>(v, live, o, sfp, j);
+        } else if constexpr (!MT::kBwd) {
+            float g[16], u[16], v[16];
+            load16(p, g);
+            load16(p + kBoxBytes, u);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    v[k] = swiglu(g[k], u[k]);
-                    if constexpr (MODE == kSwigluWeighted) v[k] = __fmul_rn(v[k], wt[q]);
+            for (int k = 0; k < 16; ++k) {
+                v[k] = swiglu(g[k], u[k]);
+                if constexpr (MT::kWeighted) v[k] = __fmul_rn(v[k], wt);
+            }
+            emit_group<FMT, false>(v, live, o, sfp, j);
+        } else {
+            float g[16], u[16], d[16], dg[16], du[16];
+            load16(p, g);
+            load16(p + kBoxBytes, u);
+            load16(p + 2 * kBoxBytes, d);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                swiglu_grad(g[k], u[k], d[k], dg[k], du[k]);
+                if constexpr (MT::kWeighted) {
+                    dg[k] = __fmul_rn(dg[k], wt);
+                    du[k] = __fmul_rn(du[k], wt);
                 }
             }
-            float m = fmaxf(absmax8(v), absmax8(v + 8));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-            float sc, inv;
-            group_scale<FMT>(m, sc, inv);
-            if (row < T) {
-                uint2* o = out + (row * C_out + cb * 128) / 8;
-                uint2 lo, hi;
-                if constexpr (MODE == kPlain) {
-                    lo = quantize8<FMT>(v, sc, inv);
-                    hi = quantize8<FMT>(v + 8, sc, inv);
-                } else {
-                    lo = quantize8_mul<FMT>(v, inv);
-                    hi = quantize8_mul<FMT>(v + 8, inv);
-                }
-                st_stream(o + j, lo);
-                st_stream(o + 8 + j, hi);
-                if (j == 0) st_stream(sf + row * CB + cb, sc);
-            }
+            emit_group<FMT, false>(dg, live, o, sfp, j);
+            emit_group<FMT, false>(du, live, o + C_out / 8, sfp + CB, j);
         }
         // Release the stage only now: the stores above consume every value
         // read from it, so the shared loads have completed before the arrive
@@ -183,18 +217,23 @@ __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 }
 
 template <int FMT, int MODE>
-cudaError_t launch(const void* x, const float* w, void* out, float* sf, int64_t T, int64_t C_out,
-                   cudaStream_t stream) {
+cudaError_t launch(const void* x, const void* dy, const float* w, void* out, float* sf,
+                   int64_t T, int64_t C_out, cudaStream_t stream) {
+    using MT = ModeTraits<MODE>;
     // x as a bf16 [T, cols] matrix: C columns (plain) or 2H (gate | up)
-    const int64_t cols = ModeTraits<MODE>::kOperands * C_out;
-    CUtensorMap map;
+    const int64_t cols = (MT::kOperands == 1 ? 1 : 2) * C_out;
+    CUtensorMap map, map_dy;
     if (!encode_bf16_2d(&map, x, cols, T, 128, kRows)) return cudaErrorInvalidValue;
-
+    if constexpr (MT::kBwd) {
+        if (!encode_bf16_2d(&map_dy, dy, C_out, T, 128, kRows)) return cudaErrorInvalidValue;
+    } else {
+        map_dy = map;  // unused
+    }
     auto* k = &row_cast_kernel<FMT, MODE>;
     const size_t smem = sizeof(RowSmem<MODE>) + 1024;
     const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
-    k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint2*>(out), sf, T,
+    k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, T,
                                         static_cast<int>(C_out), device_status_word());
     return cudaGetLastError();
 }
@@ -204,18 +243,29 @@ cudaError_t launch(const void* x, const float* w, void* out, float* sf, int64_t 
 cudaError_t launch_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
                                   int fmt, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    return fmt == kFmtE4M3 ? launch<kFmtE4M3, kPlain>(x, nullptr, out, sf, T, C, stream)
-                           : launch<kFmtE5M2, kPlain>(x, nullptr, out, sf, T, C, stream);
+    return fmt == kFmtE4M3 ? launch<kFmtE4M3, kPlain>(x, nullptr, nullptr, out, sf, T, C, stream)
+                           : launch<kFmtE5M2, kPlain>(x, nullptr, nullptr, out, sf, T, C, stream);
 }
 
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
                                int64_t H, int fmt, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     if (fmt == kFmtE4M3)
-        return w ? launch<kFmtE4M3, kSwigluWeighted>(x, w, out, sf, T, H, stream)
-                 : launch<kFmtE4M3, kSwiglu>(x, w, out, sf, T, H, stream);
-    return w ? launch<kFmtE5M2, kSwigluWeighted>(x, w, out, sf, T, H, stream)
-             : launch<kFmtE5M2, kSwiglu>(x, w, out, sf, T, H, stream);
+        return w ? launch<kFmtE4M3, kSwigluWeighted>(x, nullptr, w, out, sf, T, H, stream)
+                 : launch<kFmtE4M3, kSwiglu>(x, nullptr, w, out, sf, T, H, stream);
+    return w ? launch<kFmtE5M2, kSwigluWeighted>(x, nullptr, w, out, sf, T, H, stream)
+             : launch<kFmtE5M2, kSwiglu>(x, nullptr, w, out, sf, T, H, stream);
+}
+
+cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
+                                        float* sf, int64_t T, int64_t H, int fmt,
+                                        cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    if (fmt == kFmtE4M3)
+        return w ? launch<kFmtE4M3, kBackwardWeighted>(x, dy, w, out, sf, T, H, stream)
+                 : launch<kFmtE4M3, kBackward>(x, dy, w, out, sf, T, H, stream);
+    return w ? launch<kFmtE5M2, kBackwardWeighted>(x, dy, w, out, sf, T, H, stream)
+             : launch<kFmtE5M2, kBackward>(x, dy, w, out, sf, T, H, stream);
 }
 
 }  // namespace tkq

@@ -223,6 +223,26 @@ tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf, 
                                                  static_cast<cudaStream_t>(stream)));
 }
 
+tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
+                                    float* sf, int64_t T, int64_t H, int group, int fmt,
+                                    tkq_stream_t stream) {
+    tkq_status st = check_common(T, H, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !dy || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(dy, 16) || !tkq::aligned(out, 16) ||
+        !tkq::aligned(sf, 4) || (w && !tkq::aligned(w, 4)))
+        return TKQ_ERR_ALIGN;
+    const auto ro = tkq::span(out, T * 2 * H), rs = tkq::span(sf, T * (2 * H / group) * 4);
+    const tkq::Range inputs[3] = {tkq::span(x, T * H * 4), tkq::span(dy, T * H * 2),
+                                  w ? tkq::span(w, T * 4) : tkq::Range{0, 0}};
+    if (tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    for (const auto& in : inputs)
+        if (tkq::overlap(in, ro) || tkq::overlap(in, rs)) return TKQ_ERR_ALIAS;
+    return launch_status(tkq::launch_swiglu_backward_cast(x, dy, w, out, sf, T, H, fmt,
+                                                          static_cast<cudaStream_t>(stream)));
+}
+
 tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
                              float* sf_t, int64_t T, int64_t H, int group, int fmt,
                              tkq_stream_t stream) {

@@ -193,6 +193,23 @@ __device__ __forceinline__ float swiglu(float g, float u) {
     return __fmul_rn(__fmul_rn(g, rcp_approx(den)), u);
 }
 
+// Gradient of y = silu(g) * u with respect to g and u, scaled by the upstream
+// gradient d (the derivative of the SwiGLU of the same page; it gives no
+// formula, this is the textbook one):
+//   sigma = 1 / (1 + e), e = exp(-g);  1 - sigma = e * sigma (no cancellation)
+//   dg = d * u * sigma * (1 + g * (1 - sigma)),  du = d * g * sigma.
+// The exponent is clamped at 2^126 so that e * sigma stays finite for very
+// negative g (where sigma, silu and both gradients are ~0 anyway).
+__device__ __forceinline__ void swiglu_grad(float g, float u, float d, float& dg, float& du) {
+    const float t = fminf(__fmul_rn(g, -1.4426950408889634f), 126.0f);
+    const float e = ex2_approx(t);
+    const float sig = rcp_approx(__fadd_rn(1.0f, e));
+    const float one_minus_sig = __fmul_rn(e, sig);
+    const float dsilu = __fmul_rn(sig, __fmaf_rn(g, one_minus_sig, 1.0f));
+    dg = __fmul_rn(__fmul_rn(d, u), dsilu);
+    du = __fmul_rn(d, __fmul_rn(g, sig));
+}
+
 // Four bf16 packed in a uint2 -> four floats, element order preserved.
 __device__ __forceinline__ void unpack4(const uint2& q, float* v) {
     v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);

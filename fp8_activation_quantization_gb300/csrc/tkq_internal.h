@@ -34,6 +34,10 @@ cudaError_t launch_per_token_cast(const void* x, void* out, float* sf, int64_t T
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
                                int64_t H, int fmt, cudaStream_t stream);
 
+cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
+                                        float* sf, int64_t T, int64_t H, int fmt,
+                                        cudaStream_t stream);
+
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
                                  cudaStream_t stream);

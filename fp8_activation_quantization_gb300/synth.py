@@ -21,6 +21,8 @@ Workloads (all seeded, no dataset involved):
   a fp32 routing weight per row: Uniform(0.01, 1) normalised over the 8 rows of
   each token.
 * ``swiglu_t``      bf16 [131072, 4096] N(0, 1), for the cast + transposed cast.
+* ``swiglu_bwd``    bf16 [65536, 4096] N(0, 1) gate|up, an upstream gradient dy
+  bf16 [65536, 2048] N(0, 1) and the routing weights of ``swiglu_moe``.
 """
 from __future__ import annotations
 
@@ -42,6 +44,9 @@ WORKLOADS = {
                                 "bf16 [65536, 4096] ~ N(0,1), 8192 tokens x top-8, H=2048"),
     "swiglu_t": (131072, 4096, "swiglu + per-token E4M3 cast + transposed cast, "
                                "bf16 [131072, 4096] ~ N(0,1), H=2048"),
+    "swiglu_bwd": (65536, 4096, "swiglu backward x routing weight + per-token E4M3 cast of "
+                                "[dgate | dup], bf16 [65536, 4096] ~ N(0,1) and dy bf16 "
+                                "[65536, 2048] ~ N(0,1), 8192 tokens x top-8, H=2048"),
 }
 
 _WORKLOAD_IDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
@@ -176,4 +181,9 @@ def workload(name: str, seed: int = 0, rows: int | None = None) -> dict:
         return {"x": swiglu_bf16(seed, sid, T, C // 2), "w": np.ascontiguousarray(w)}
     if name == "swiglu_t":
         return {"x": swiglu_bf16(seed, sid, T, C // 2)}
+    if name == "swiglu_bwd":
+        topk = 8
+        w = routing_weights(seed, sid, -(-T // topk), topk)[:T]
+        return {"x": swiglu_bf16(seed, sid, T, C // 2),
+                "dy": normal_bf16(seed, sid + 100, T, C // 2), "w": np.ascontiguousarray(w)}
     raise KeyError(name)

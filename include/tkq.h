@@ -138,6 +138,27 @@ tkq_status tkq_read_device_status(uint32_t* flags, int clear);
  */
 tkq_status tkq_selftest_wait_timeout(int64_t limit_ns, tkq_stream_t stream);
 
+/*
+ * SwiGLU backward fused with the per-token cast ([P1] §2 operator table and
+ * §6 step 13, swiglu_backward_and_per_token_cast; the pages give no formula,
+ * so this is the derivative of y = silu(g) * u [* w]).  For every row t and
+ * channel c < H, with g = x[t, c], u = x[t, H + c], d = dy[t, c] and
+ * sigma = 1 / (1 + exp(-g)):
+ *   dg = d * u * sigma * (1 + g * (1 - sigma)) [* w[t]]
+ *   du = d * g * sigma [* w[t]]
+ * and the fp32 matrix [dg | du] is cast per token.
+ *   x   : bf16 [T, 2H] (gate | up, as given to the forward)
+ *   dy  : bf16 [T, H], gradient of the forward output y
+ *   w   : fp32 [T] or NULL
+ *   out : FP8 codes [T, 2H] (dg in columns [0, H), du in [H, 2H))
+ *   sf  : fp32 [T, 2H/128]
+ * T >= 0; H > 0, H % 128 == 0.  Codes are those of the product by the
+ * reciprocal scale, like tkq_swiglu_cast.
+ */
+tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
+                                    float* sf, int64_t T, int64_t H, int group, int fmt,
+                                    tkq_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);
 

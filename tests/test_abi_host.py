@@ -98,6 +98,18 @@ def test_swiglu_cast_t_validation(lib, T, expected):
     assert lib.tkq_swiglu_cast_t(*args) == expected
 
 
+@pytest.mark.parametrize("args,expected", [
+    ((p(), None, None, p(1 << 24), p(2 << 24), 4, 256, 128, 0), 1),          # dy NULL
+    ((p(), p(1 << 22), None, p(1 << 24), p(2 << 24), 4, 200, 128, 0), 2),    # H % 128
+    ((p(), p((1 << 22) + 8), None, p(1 << 24), p(2 << 24), 4, 256, 128, 0), 5),  # dy misaligned
+    ((p(), p(1 << 22), None, p(512), p(2 << 24), 4, 256, 128, 0), 7),        # out overlaps x
+    ((p(), p(1 << 22), None, p(1 << 24), p((1 << 24) + 64), 4, 256, 128, 0), 7),  # sf in out
+    ((None, None, None, None, None, 0, 256, 128, 0), 0),                       # empty batch
+])
+def test_swiglu_backward_validation(lib, args, expected):
+    assert lib.tkq_swiglu_backward_cast(*args, None) == expected
+
+
 def test_status_calls_validate_before_cuda(lib):
     assert lib.tkq_read_device_status(None, 0) == 1          # NULL flags
     assert lib.tkq_selftest_wait_timeout(0, None) == 2       # limit out of range

@@ -330,6 +330,79 @@ def test_swiglu_t_full_workload_sampled(cuda_device):
 
 
 # ---------------------------------------------------------------------------
+# SwiGLU backward + cast: tolerance
+# ---------------------------------------------------------------------------
+
+def run_swiglu_bwd(x_bits, dy_bits, w, fmt, dev):
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    xd = to_dev_bf16(x_bits, dev)
+    dyd = to_dev_bf16(dy_bits, dev)
+    wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
+    wp = None if wd is None else ctypes.c_void_p(wd.data_ptr())
+    out = Guarded(T * 2 * H, dev)
+    sf = Guarded(T * (2 * H // 128) * 4, dev)
+    st = tkq.tkq_swiglu_backward_cast(ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(dyd.data_ptr()),
+                                      wp, out.ptr, sf.ptr, T, H, 128, oracle.FMT[fmt],
+                                      stream_of(dev))
+    assert st == 0, tkq.tkq_status_string(st)
+    torch.cuda.synchronize()
+    out.check_guards("out")
+    sf.check_guards("sf")
+    return out.data().reshape(T, 2 * H), sf.data().view(np.float32).reshape(T, 2 * H // 128)
+
+
+def test_swiglu_backward_full_workload(cuda_device):
+    d = synth.workload("swiglu_bwd")
+    out, sf = run_swiglu_bwd(d["x"], d["dy"], d["w"], "e4m3", cuda_device)
+    ro, rs = oracle.swiglu_backward_cast(d["x"], d["dy"], d["w"], "e4m3", threads=THREADS)
+    parity.assert_scales_close("scales", sf, rs)
+    parity.assert_codes_close("codes", out, ro)
+    assert tkq.tkq_read_device_status() == 0
+
+
+@pytest.mark.parametrize("T", [1, 7, 129, 1031])
+@pytest.mark.parametrize("H", [128, 384])
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_swiglu_backward_ragged(cuda_device, T, H, weighted, fmt):
+    d = synth.workload("swiglu_bwd", rows=T)
+    x = np.ascontiguousarray(d["x"][:, np.r_[0:H, 2048:2048 + H]])
+    dy = np.ascontiguousarray(d["dy"][:, :H])
+    w = d["w"] if weighted else None
+    out, sf = run_swiglu_bwd(x, dy, w, fmt, cuda_device)
+    ro, rs = oracle.swiglu_backward_cast(x, dy, w, fmt, threads=THREADS)
+    parity.assert_scales_close("scales", sf, rs)
+    parity.assert_codes_close("codes", out, ro, max_frac=max(1e-4, 1.0 / out.size))
+
+
+def test_swiglu_backward_extreme_gates(cuda_device):
+    """Gates from -120 to 120 (exp(-g) overflows binary32 below -88): the
+    gradients must stay finite and match the oracle."""
+    T, H = 256, 256
+    rng = np.random.default_rng(8)
+    g = np.linspace(-120, 120, T * H).astype(np.float32).reshape(T, H)
+    u = rng.standard_normal((T, H)).astype(np.float32)
+    x = np.concatenate([synth.f32_to_bf16_bits(g), synth.f32_to_bf16_bits(u)], axis=1)
+    dy = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    out, sf = run_swiglu_bwd(x, dy, None, "e4m3", cuda_device)
+    ro, rs = oracle.swiglu_backward_cast(x, dy, None, "e4m3")
+    assert np.all(np.isfinite(sf))
+    parity.assert_scales_close("scales", sf, rs)
+    parity.assert_codes_close("codes", out, ro, max_frac=max(1e-4, 2.0 / out.size))
+
+
+def test_swiglu_backward_tensor_api(cuda_device):
+    d = synth.workload("swiglu_bwd", rows=256)
+    x = to_dev_bf16(d["x"], cuda_device)
+    dy = to_dev_bf16(d["dy"], cuda_device)
+    out, sf = tkq.swiglu_backward_and_per_token_cast(x, dy, "e4m3")
+    assert out.dtype == torch.float8_e4m3fn and out.shape == (256, 4096) and sf.shape == (256, 32)
+    with pytest.raises(ValueError):
+        tkq.swiglu_backward_and_per_token_cast(x, dy[:, :1024].contiguous())
+
+
+# ---------------------------------------------------------------------------
 # ABI behaviour on a GPU
 # ---------------------------------------------------------------------------
 
