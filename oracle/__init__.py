@@ -118,6 +118,12 @@ def _configure(lib):
     lib.ora_swiglu_values.argtypes = [p, p, i64, i64, p]
     lib.ora_swiglu_cast.argtypes = [p, p, i64, i64, i64, i, p, p]
     lib.ora_swiglu_cast_t.argtypes = [p, p, i64, i64, i64, i, p, p, p, p]
+    lib.ora_pow2_ceil.argtypes = [ctypes.c_float]
+    lib.ora_pow2_ceil.restype = ctypes.c_float
+    lib.ora_sf_bytes.argtypes = [i64, i64, i]
+    lib.ora_sf_bytes.restype = i64
+    lib.ora_cast_rows_f32_ex.argtypes = [p, i64, i64, i64, i, i, p, p]
+    lib.ora_cast_rows_f32_ex.restype = ctypes.c_int
     lib.ora_swiglu_backward_values.argtypes = [p, p, p, i64, i64, p]
     lib.ora_swiglu_backward_cast.argtypes = [p, p, p, i64, i64, i64, i, p, p]
     for f in ("ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
@@ -361,3 +367,67 @@ def swiglu_backward_cast(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray 
 
     _row_parallel(T, threads, body)
     return out, sf
+
+
+# --------------------------------------------------------------------------
+# scale-factor layout options
+# --------------------------------------------------------------------------
+
+SF_ROUND_POW2 = 1
+SF_UE8M0_PACKED = 2
+SF_COL_MAJOR = 4
+
+
+def pow2_ceil(s: float) -> np.float32:
+    return np.float32(_load().ora_pow2_ceil(float(np.float32(s))))
+
+
+def sf_shape(T: int, G: int, flags: int):
+    """(shape, dtype) of the scale output for T rows of G groups."""
+    T4 = (T + 3) // 4 * 4
+    W = (G + 3) // 4
+    if flags & SF_UE8M0_PACKED:
+        return ((W, T4) if flags & SF_COL_MAJOR else (T, W)), np.uint32
+    return ((G, T4) if flags & SF_COL_MAJOR else (T, G)), np.float32
+
+
+def cast_rows_f32_ex(y: np.ndarray, fmt="e4m3", group: int = 128, flags: int = 0,
+                     threads: int = 1):
+    """fp32 [T, C] -> (codes [T, C], scales in the layout `flags` selects).
+    Row blocks of 4 rows are independent, so ``threads`` splits 4-aligned row
+    ranges (column-major layouts are gathered after)."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    T, C = y.shape
+    if group <= 0 or C % group:
+        raise ValueError("group must divide C")
+    G = C // group
+    out = np.empty((T, C), np.uint8)
+    shape, dt = sf_shape(T, G, flags)
+    sf = np.empty(shape, dt)
+    f = _fmt(fmt)
+    if threads <= 1 or T < 8:
+        _check(lib.ora_cast_rows_f32_ex(_ptr(y), T, C, group, f, flags, _ptr(out), _ptr(sf)),
+               "cast_rows_f32_ex")
+        return out, sf
+
+    def body(a, b):
+        part_shape, _ = sf_shape(b - a, G, flags)
+        part = np.empty(part_shape, dt)
+        _check(lib.ora_cast_rows_f32_ex(_ptr(y[a:b]), b - a, C, group, f, flags,
+                                        _ptr(out[a:b]), _ptr(part)), "cast_rows_f32_ex")
+        if flags & SF_COL_MAJOR:
+            n = part.shape[1]
+            sf[:, a:a + n] = part
+        else:
+            sf[a:b] = part
+
+    _row_parallel(T, threads, body, align=4)
+    return out, sf
+
+
+def per_token_cast_ex(x_bits: np.ndarray, fmt="e4m3", group: int = 128, flags: int = 0,
+                      threads: int = 1):
+    """bf16 [T, C] (exact widening to fp32) -> the cast with scale options."""
+    xf = (np.ascontiguousarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    return cast_rows_f32_ex(xf, fmt, group, flags, threads)

@@ -283,3 +283,62 @@ int ora_swiglu_backward_cast(const uint16_t* x, const uint16_t* dy, const float*
     free(g);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Scale-factor layout options ("DeepSeek开源TileKernels..." §3.1 round_sf,  */
+/* use_packed_ue8m0, use_tma_aligned_col_major_sf; "TileKernels 与 DeepGEMM  */
+/* 的分界线" §4C)                                                            */
+/* ------------------------------------------------------------------------ */
+
+float ora_pow2_ceil(float s) {
+    int e;
+    const double f = frexp((double)s, &e);  /* s = f * 2^e, f in [0.5, 1) */
+    if (f == 0.5) return s;                 /* already a power of two */
+    return (float)ldexp(1.0, e);            /* the next power of two above s */
+}
+
+int64_t ora_sf_bytes(int64_t T, int64_t G, int flags) {
+    const int64_t T4 = (T + 3) / 4 * 4;
+    const int64_t W = (G + 3) / 4;
+    const int packed = (flags & ORA_SF_UE8M0_PACKED) != 0;
+    const int cm = (flags & ORA_SF_COL_MAJOR) != 0;
+    if (packed) return (cm ? W * T4 : T * W) * 4;
+    return (cm ? G * T4 : T * G) * 4;
+}
+
+int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, int fmt,
+                         int flags, uint8_t* out, void* sf) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || C < 0 || group <= 0 || C % group || (flags & ~7))
+        return -1;
+    const int packed = (flags & ORA_SF_UE8M0_PACKED) != 0;
+    const int pow2 = packed || (flags & ORA_SF_ROUND_POW2);
+    const int cm = (flags & ORA_SF_COL_MAJOR) != 0;
+    const int64_t G = C / group;
+    const int64_t T4 = (T + 3) / 4 * 4;
+    const int64_t W = (G + 3) / 4;
+    memset(sf, 0, (size_t)ora_sf_bytes(T, G, flags));
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < G; ++j) {
+            const float* v = y + t * C + j * group;
+            float amax = 0.0f;
+            for (int64_t i = 0; i < group; ++i) {
+                const float a = fabsf(v[i]);
+                if (a > amax) amax = a;
+            }
+            float s = ora_group_scale(amax, fmt);
+            if (pow2) s = ora_pow2_ceil(s);
+            for (int64_t i = 0; i < group; ++i)
+                out[t * C + j * group + i] = ora_fp8_encode(v[i] / s, fmt);
+            if (packed) {
+                uint32_t bits;
+                memcpy(&bits, &s, sizeof bits);
+                const int64_t word = cm ? (j / 4) * T4 + t : t * W + j / 4;
+                ((uint8_t*)sf)[word * 4 + j % 4] = (uint8_t)((bits >> 23) & 0xFF);
+            } else {
+                ((float*)sf)[cm ? j * T4 + t : t * G + j] = s;
+            }
+        }
+    }
+    return 0;
+}

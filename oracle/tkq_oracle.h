@@ -104,6 +104,36 @@ int ora_swiglu_cast_t(const uint16_t* x, const float* w, int64_t T, int64_t H,
                       int64_t group, int fmt, uint8_t* out, float* sf,
                       uint8_t* out_t, float* sf_t);
 
+/* Scale-factor layout options (TileKernels CastOutputConfig round_sf,
+ * use_packed_ue8m0, use_tma_aligned_col_major_sf: [P2] §3.1; their purpose,
+ * feeding the GEMM's TMA in its own layout: [P1] §4C).
+ *   ORA_SF_ROUND_POW2   s is rounded up to a power of two: 2^ceil(log2 s0),
+ *                       s0 the fp32 scale of the plain rule.
+ *   ORA_SF_UE8M0_PACKED each (power-of-two) scale is stored as its UE8M0 byte
+ *                       (the biased binary32 exponent, value 2^(e-127)); four
+ *                       consecutive groups of a row share one 32-bit word,
+ *                       group 4k+i in byte i.  Implies ORA_SF_ROUND_POW2.
+ *   ORA_SF_COL_MAJOR    scales stored column-major: element (t, j) at
+ *                       j * T4 + t with T4 = T rounded up to a multiple of 4
+ *                       (16-byte aligned columns); padding rows hold 0.
+ * Layouts of sf (G groups per row, W = ceil(G / 4) words):
+ *   default            fp32 [T, G]          ORA_SF_COL_MAJOR          fp32 [G, T4]
+ *   ORA_SF_UE8M0_PACKED int32 [T, W]        UE8M0_PACKED|COL_MAJOR   int32 [W, T4]
+ * Packed bytes of groups >= G in a row's last word are 0. */
+enum { ORA_SF_ROUND_POW2 = 1, ORA_SF_UE8M0_PACKED = 2, ORA_SF_COL_MAJOR = 4 };
+
+/* Power of two >= s (s a positive normal binary32): 2^ceil(log2 s). */
+float ora_pow2_ceil(float s);
+
+/* Bytes of the scale output for T rows of G groups under `flags`. */
+int64_t ora_sf_bytes(int64_t T, int64_t G, int flags);
+
+/* The row cast of an fp32 [T, C] matrix with scale options: codes of
+ * fl32(y / s) with s from ora_group_scale, rounded up to a power of two when
+ * asked; scales written in the layout `flags` selects (sf is raw bytes). */
+int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, int fmt,
+                         int flags, uint8_t* out, void* sf);
+
 /* Gradient of y = silu(g) * u [* w] for a bf16 [T, 2H] gate|up input and a
  * bf16 [T, H] upstream gradient dy, written as the fp32 [T, 2H] matrix
  * [dg | du]:

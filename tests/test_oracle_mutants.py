@@ -48,6 +48,12 @@ MUTANTS = [
      "grad[t * 2 * H + H + c] = (float)(d * u * dsilu * wt); continue;"),
     ("backward: weight dropped from du", "grad[t * 2 * H + H + c] = (float)(d * silu * wt);",
      "grad[t * 2 * H + H + c] = (float)(d * silu);"),
+    ("scale rounded down to a power of two", "return (float)ldexp(1.0, e);",
+     "return (float)ldexp(1.0, e - 1);"),
+    ("UE8M0 bytes in reverse order", "((uint8_t*)sf)[word * 4 + j % 4]",
+     "((uint8_t*)sf)[word * 4 + 3 - j % 4]"),
+    ("column-major scales without padding", "((float*)sf)[cm ? j * T4 + t : t * G + j] = s;",
+     "((float*)sf)[cm ? j * T + t : t * G + j] = s;"),
 ]
 
 # cheapest first: most mistakes are caught by the hand-worked fixtures
@@ -60,6 +66,11 @@ CHECKS = [
     (pins.test_swiglu_weight_one_and_weight_product, {}),
     (pins.test_swiglu_vs_binary64, {}),
     (pins.test_swiglu_backward_special_cases, {}),
+    (pins.test_round_pow2_hand_group, {}),
+    (pins.test_pow2_ceil_against_numpy_and_properties, {}),
+    (pins.test_sf_layouts_rearrange_the_row_major_scales, {"flags": oracle.SF_COL_MAJOR}),
+    (pins.test_sf_layouts_rearrange_the_row_major_scales,
+     {"flags": oracle.SF_UE8M0_PACKED | oracle.SF_COL_MAJOR}),
     (pins.test_swiglu_backward_vs_finite_differences, {}),
     (pins.test_cols_equal_rows_of_transpose, {"fmt": "e4m3"}),
     (pins.test_cols_index_orientation, {}),

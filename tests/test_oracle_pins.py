@@ -483,3 +483,84 @@ def test_swiglu_backward_cast_is_cast_of_values():
     c1, s1 = oracle.cast_rows_f32(grad)
     c2, s2 = oracle.swiglu_backward_cast(x, dy, w)
     assert np.array_equal(c1, c2) and np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# scale-factor layout options
+# ---------------------------------------------------------------------------
+
+def test_pow2_ceil_against_numpy_and_properties():
+    rng = np.random.default_rng(61)
+    s = np.concatenate([np.exp2(rng.uniform(-30, 20, 20000)),
+                        np.exp2(rng.integers(-30, 20, 200).astype(np.float64))]).astype(np.float32)
+    got = np.array([oracle.pow2_ceil(v) for v in s], np.float32)
+    ref = np.exp2(np.ceil(np.log2(s.astype(np.float64)))).astype(np.float32)
+    assert np.array_equal(got, ref)
+    m, _ = np.frexp(got)
+    assert np.all(m == 0.5) and np.all(got >= s) and np.all(got < 2 * s)
+    exact = np.frexp(s)[0] == 0.5
+    assert np.all((got == s) == exact)
+
+
+def test_round_pow2_codes_are_exact_scaling():
+    """With a power-of-two scale 2^k the quotient y / s is exact, so the codes
+    are torch's FP8 conversion of y * 2^-k (in range) and the scale is the
+    plain scale rounded up."""
+    rng = np.random.default_rng(63)
+    y = (rng.standard_normal((64, 512)) * np.exp2(rng.integers(-8, 8, (64, 1)))).astype(np.float32)
+    for fmt in FMTS:
+        c0, s0 = oracle.cast_rows_f32(y, fmt)
+        c1, s1 = oracle.cast_rows_f32_ex(y, fmt, 128, oracle.SF_ROUND_POW2)
+        assert np.array_equal(s1, np.exp2(np.ceil(np.log2(s0.astype(np.float64)))).astype(np.float32))
+        q = y.reshape(64, 4, 128) / s1[:, :, None]
+        assert np.all(np.abs(q) <= FMAX[fmt])
+        ref = torch.from_numpy(np.ascontiguousarray(q.reshape(64, 512))).to(TORCH_FP8[fmt])
+        assert np.array_equal(c1, ref.view(torch.uint8).numpy())
+
+
+def test_round_pow2_hand_group():
+    # amax 3.140625: s0 = fl(3.140625 / 448) ~ 0.00701 -> s = 2^-7; the amax
+    # element becomes 402, between 384 and 416 above the midpoint 400 -> 416
+    # (0x7d); 1.0 becomes exactly 128 (0x70).
+    y = np.zeros((1, 128), np.float32)
+    y[0, 3], y[0, 9] = 3.140625, 1.0
+    c, s = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.SF_ROUND_POW2)
+    assert s[0, 0] == np.float32(2.0 ** -7)
+    assert c[0, 3] == 0x7D and c[0, 9] == 0x70 and np.count_nonzero(c) == 2
+    c, s = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.SF_UE8M0_PACKED)
+    assert s.dtype == np.uint32 and s[0, 0] == 127 - 7   # one group: byte 0 only
+
+
+def _layout_inputs(T=13, G=7, seed=67):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((T, G * 128)) * np.exp2(rng.integers(-6, 6, (T, G * 128))
+                                                         )).astype(np.float32)
+
+
+@pytest.mark.parametrize("flags", [oracle.SF_COL_MAJOR, oracle.SF_UE8M0_PACKED,
+                                   oracle.SF_UE8M0_PACKED | oracle.SF_COL_MAJOR,
+                                   oracle.SF_ROUND_POW2 | oracle.SF_COL_MAJOR])
+def test_sf_layouts_rearrange_the_row_major_scales(flags):
+    y = _layout_inputs()
+    T, C = y.shape
+    G = C // 128
+    pow2 = flags & (oracle.SF_ROUND_POW2 | oracle.SF_UE8M0_PACKED)
+    c_ref, s_ref = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.SF_ROUND_POW2 if pow2 else 0)
+    c, s = oracle.cast_rows_f32_ex(y, "e4m3", 128, flags)
+    assert np.array_equal(c, c_ref)
+    T4 = (T + 3) // 4 * 4
+    if flags & oracle.SF_UE8M0_PACKED:
+        e = ((s_ref.view(np.uint32) >> 23) & 0xFF).astype(np.uint32)
+        assert np.array_equal(np.exp2(e.astype(np.float64) - 127).astype(np.float32), s_ref)
+        W = (G + 3) // 4
+        ep = np.zeros((T, W * 4), np.uint32)
+        ep[:, :G] = e
+        words = ep[:, 0::4] | (ep[:, 1::4] << 8) | (ep[:, 2::4] << 16) | (ep[:, 3::4] << 24)
+        if flags & oracle.SF_COL_MAJOR:
+            assert s.shape == (W, T4)
+            assert np.array_equal(s[:, :T], words.T) and np.all(s[:, T:] == 0)
+        else:
+            assert np.array_equal(s, words)
+    else:
+        assert s.shape == (G, T4)
+        assert np.array_equal(s[:, :T], s_ref.T) and np.all(s[:, T:] == 0)
