@@ -138,20 +138,31 @@ float ora_bf16_to_f32(uint16_t b) {
 /* Casts                                                                     */
 /* ------------------------------------------------------------------------ */
 
-/* One group of n values at stride `stride` (in elements) -> scale + codes.
- * The code of each value is the code of the binary32 quotient v / s. */
-static float cast_group(const float* v, int64_t n, int64_t stride, int fmt,
-                        uint8_t* codes, int64_t code_stride) {
+/* Largest |v| of n values at stride `stride` (in elements). */
+static float group_absmax(const float* v, int64_t n, int64_t stride) {
     float amax = 0.0f;
     for (int64_t i = 0; i < n; ++i) {
         const float a = fabsf(v[i * stride]);
         if (a > amax) amax = a;
     }
-    const float s = ora_group_scale(amax, fmt);
+    return amax;
+}
+
+/* The code of each value is the code of the binary32 quotient v / s. */
+static void encode_group(const float* v, int64_t n, int64_t stride, float s, int fmt,
+                         uint8_t* codes, int64_t code_stride) {
     for (int64_t i = 0; i < n; ++i) {
         const float q = v[i * stride] / s;
         codes[i * code_stride] = ora_fp8_encode(q, fmt);
     }
+}
+
+/* One group of n values at stride `stride` -> scale + codes. */
+static float cast_group(const float* v, int64_t n, int64_t stride, int fmt,
+                        uint8_t* codes, int64_t code_stride) {
+    const float amax = group_absmax(v, n, stride);
+    const float s = ora_group_scale(amax, fmt);
+    encode_group(v, n, stride, s, fmt, codes, code_stride);
     return s;
 }
 
@@ -321,15 +332,9 @@ int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, in
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t j = 0; j < G; ++j) {
             const float* v = y + t * C + j * group;
-            float amax = 0.0f;
-            for (int64_t i = 0; i < group; ++i) {
-                const float a = fabsf(v[i]);
-                if (a > amax) amax = a;
-            }
-            float s = ora_group_scale(amax, fmt);
+            float s = ora_group_scale(group_absmax(v, group, 1), fmt);
             if (pow2) s = ora_pow2_ceil(s);
-            for (int64_t i = 0; i < group; ++i)
-                out[t * C + j * group + i] = ora_fp8_encode(v[i] / s, fmt);
+            encode_group(v, group, 1, s, fmt, out + t * C + j * group, 1);
             if (packed) {
                 uint32_t bits;
                 memcpy(&bits, &s, sizeof bits);
