@@ -186,13 +186,14 @@ def dist_env():
 class Problem:
     """Device buffers + one launch closure for a named workload."""
 
-    def __init__(self, workload: str, fmt: str, dev, seed: int = 0):
+    def __init__(self, workload: str, fmt: str, dev, seed: int = 0, sf_flags: int = 0):
         import torch
         import fp8_activation_quantization_gb300 as tkq
         from fp8_activation_quantization_gb300 import synth
         self.workload = workload
         self.kern = KERNEL_OF[workload]
         self.fmt = fmt
+        self.sf_flags = sf_flags
         d = synth.workload(workload, seed=seed)
         self.x_host = d["x"]
         self.w_host = d.get("w")
@@ -236,6 +237,21 @@ class Problem:
                 args = (P(self.x), P(self.w), P(self.out), P(self.sf), P(self.out_t),
                         P(self.sf_t), T, H, 128, fcode)
                 fn = tkq.tkq_swiglu_cast_t
+        if sf_flags:
+            # the same kernel with a scale-factor layout: swap in the _ex call
+            if self.kern == "swiglu_cast_t":
+                raise ValueError("scale-layout options apply to the row casts only")
+            G = self.sf.numel() // T
+            self.sf = torch.empty(tkq.tkq_sf_bytes(T, G, sf_flags), dtype=torch.uint8, device=dev)
+            self.outputs[1] = self.sf
+            a = list(args)
+            sf_pos = {"per_token_cast": 2, "swiglu_cast": 3, "swiglu_backward_cast": 4}[self.kern]
+            a[sf_pos] = P(self.sf)
+            a.append(sf_flags)
+            fn = {"per_token_cast": tkq.tkq_per_token_cast_ex,
+                  "swiglu_cast": tkq.tkq_swiglu_cast_ex,
+                  "swiglu_backward_cast": tkq.tkq_swiglu_backward_cast_ex}[self.kern]
+            args = tuple(a)
         self._fn, self._args = fn, args
 
     def launch(self, stream):
@@ -532,14 +548,17 @@ def other_workloads(dev, stream, peak, args):
     import torch
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     out = {}
-    for name, fmt in [("plain_small", "e4m3"), ("plain_outlier", "e4m3"), ("plain_outlier", "e5m2"),
-                      ("swiglu", "e4m3"), ("swiglu_moe", "e4m3"), ("swiglu_t", "e4m3"),
-                      ("swiglu_bwd", "e4m3")]:
-        prob = Problem(name, fmt, dev)
+    for name, fmt, flags in [("plain_small", "e4m3", 0), ("plain_outlier", "e4m3", 0),
+                             ("plain_outlier", "e5m2", 0), ("plain_outlier", "e4m3", 6),
+                             ("swiglu", "e4m3", 0), ("swiglu_moe", "e4m3", 0),
+                             ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
+                             ("swiglu_bwd", "e4m3", 0)]:
+        prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
         gbs = prob.bytes / t / 1e9
-        out[f"{name}/{fmt}"] = {"kernel": prob.kern, "us": round(t * 1e6, 2),
+        key = f"{name}/{fmt}" + ("/ue8m0-col-major-sf" if flags == 6 else "")
+        out[key] = {"kernel": prob.kern, "us": round(t * 1e6, 2),
                                 "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                                 "rows_per_s": round(prob.T / t, 1), "bytes": prob.bytes}
         del prob

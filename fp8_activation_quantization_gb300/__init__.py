@@ -70,6 +70,15 @@ def load_library():
         lib.tkq_version.restype = i
         lib.tkq_swiglu_backward_cast.argtypes = [p, p, p, p, p, i64, i64, i, i, p]
         lib.tkq_swiglu_backward_cast.restype = i
+        u = ctypes.c_uint
+        lib.tkq_per_token_cast_ex.argtypes = [p, p, p, i64, i64, i, i, u, p]
+        lib.tkq_per_token_cast_ex.restype = i
+        lib.tkq_swiglu_cast_ex.argtypes = [p, p, p, p, i64, i64, i, i, u, p]
+        lib.tkq_swiglu_cast_ex.restype = i
+        lib.tkq_swiglu_backward_cast_ex.argtypes = [p, p, p, p, p, i64, i64, i, i, u, p]
+        lib.tkq_swiglu_backward_cast_ex.restype = i
+        lib.tkq_sf_bytes.argtypes = [i64, i64, u]
+        lib.tkq_sf_bytes.restype = i64
         lib.tkq_read_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i]
         lib.tkq_read_device_status.restype = i
         lib.tkq_selftest_wait_timeout.argtypes = [i64, p]
@@ -121,6 +130,44 @@ def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
     return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
 
 
+SF_ROUND_POW2 = 1
+SF_UE8M0_PACKED = 2
+SF_COL_MAJOR = 4
+
+
+def tkq_sf_bytes(T, groups_per_row, sf_flags=0) -> int:
+    return load_library().tkq_sf_bytes(T, groups_per_row, sf_flags)
+
+
+def tkq_per_token_cast_ex(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                          stream=None) -> int:
+    return load_library().tkq_per_token_cast_ex(x, out, sf, T, C, group, fmt, sf_flags, stream)
+
+
+def tkq_swiglu_cast_ex(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                       stream=None) -> int:
+    return load_library().tkq_swiglu_cast_ex(x, w, out, sf, T, H, group, fmt, sf_flags, stream)
+
+
+def tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                                stream=None) -> int:
+    return load_library().tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group, fmt,
+                                                      sf_flags, stream)
+
+
+def sf_tensor(T: int, groups_per_row: int, sf_flags: int, device):
+    """An empty scale tensor shaped for the layout `sf_flags` selects:
+    fp32 [T, G], fp32 [G, T4], int32 [T, W] or int32 [W, T4]."""
+    import torch
+    T4 = (T + 3) // 4 * 4
+    W = (groups_per_row + 3) // 4
+    if sf_flags & SF_UE8M0_PACKED:
+        shape = (W, T4) if sf_flags & SF_COL_MAJOR else (T, W)
+        return torch.empty(shape, dtype=torch.int32, device=device)
+    shape = (groups_per_row, T4) if sf_flags & SF_COL_MAJOR else (T, groups_per_row)
+    return torch.empty(shape, dtype=torch.float32, device=device)
+
+
 # ---------------------------------------------------------------------------
 # Tensor-level helpers (PyTorch supplies device memory and the stream).
 # ---------------------------------------------------------------------------
@@ -155,20 +202,38 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_sf=None):
-    """bf16 [T, C] -> (FP8 codes [T, C], fp32 scales [T, C/128])."""
+def _sf_flags(round_sf: bool, use_packed_ue8m0: bool, use_tma_aligned_col_major_sf: bool) -> int:
+    """The TileKernels cast-config options ("DeepSeek开源TileKernels..." §3.1) as
+    the C ABI's TKQ_SF_* flags."""
+    return ((SF_ROUND_POW2 if round_sf else 0) | (SF_UE8M0_PACKED if use_packed_ue8m0 else 0)
+            | (SF_COL_MAJOR if use_tma_aligned_col_major_sf else 0))
+
+
+def _check_weights(topk_weights, T, x):
+    import torch
+    if topk_weights is not None:
+        if (topk_weights.dtype != torch.float32 or topk_weights.numel() != T
+                or not topk_weights.is_contiguous() or topk_weights.device != x.device):
+            raise TypeError("topk_weights must be a contiguous fp32 tensor of T elements on x's device")
+
+
+def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_sf=None,
+                   round_sf: bool = False, use_packed_ue8m0: bool = False,
+                   use_tma_aligned_col_major_sf: bool = False):
+    """bf16 [T, C] -> (FP8 codes [T, C], scales).  Scales are fp32 [T, C/128]
+    unless a scale-layout option is set (see ``sf_tensor`` for the shapes)."""
     import torch
     _check_input(x)
     f = _fmt_code(fmt)
     T, C = x.shape
+    flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
     if out is None:
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
-        out_sf = torch.empty((T, max(C // max(num_per_channels, 1), 0)), dtype=torch.float32,
-                             device=x.device)
+        out_sf = sf_tensor(T, max(C // max(num_per_channels, 1), 0), flags, x.device)
     with torch.cuda.device(x.device):
-        st = tkq_per_token_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
-                                _stream_handle(x.device))
+        st = tkq_per_token_cast_ex(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
+                                   flags, _stream_handle(x.device))
     if st:
         raise TkqError(st, "tkq_per_token_cast")
     return out, out_sf
@@ -176,10 +241,13 @@ def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_s
 
 def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP,
                                       topk_weights=None, with_transpose: bool = False,
-                                      out=None, out_sf=None, out_t=None, out_sf_t=None):
+                                      out=None, out_sf=None, out_t=None, out_sf_t=None,
+                                      round_sf: bool = False, use_packed_ue8m0: bool = False,
+                                      use_tma_aligned_col_major_sf: bool = False):
     """bf16 [T, 2H] (gate | up) -> (codes [T, H], scales [T, H/128]) and, with
     ``with_transpose``, also (codes_t [H, T], scales_t [H, T/128]).
-    ``topk_weights``: optional fp32 [T] routing weight per row."""
+    ``topk_weights``: optional fp32 [T] routing weight per row.  The scale-layout
+    options apply to the row scales of the cast without transpose."""
     import torch
     _check_input(x)
     f = _fmt_code(fmt)
@@ -188,19 +256,19 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
         raise ValueError("x must have an even number of columns (gate | up)")
     H = H2 // 2
     g = max(num_per_channels, 1)
-    if topk_weights is not None:
-        if (topk_weights.dtype != torch.float32 or topk_weights.numel() != T
-                or not topk_weights.is_contiguous() or topk_weights.device != x.device):
-            raise TypeError("topk_weights must be a contiguous fp32 tensor of T elements on x's device")
+    _check_weights(topk_weights, T, x)
+    flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
+    if flags and with_transpose:
+        raise ValueError("scale-layout options are not available with with_transpose")
     if out is None:
         out = torch.empty((T, H), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
-        out_sf = torch.empty((T, H // g), dtype=torch.float32, device=x.device)
+        out_sf = sf_tensor(T, H // g, flags, x.device)
     with torch.cuda.device(x.device):
         stream = _stream_handle(x.device)
         if not with_transpose:
-            st = tkq_swiglu_cast(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), T, H,
-                                 num_per_channels, f, stream)
+            st = tkq_swiglu_cast_ex(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), T, H,
+                                    num_per_channels, f, flags, stream)
             if st:
                 raise TkqError(st, "tkq_swiglu_cast")
             return out, out_sf
@@ -216,10 +284,12 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
 
 
 def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int = GROUP,
-                                       topk_weights=None, out=None, out_sf=None):
+                                       topk_weights=None, out=None, out_sf=None,
+                                       round_sf: bool = False, use_packed_ue8m0: bool = False,
+                                       use_tma_aligned_col_major_sf: bool = False):
     """Gradients of y = silu(gate) * up [* w] from dy, cast per token.
     x: bf16 [T, 2H] (gate | up); dy: bf16 [T, H] -> (codes [T, 2H] of [dg | du],
-    scales [T, 2H/128])."""
+    scales [T, 2H/128] or the chosen scale layout)."""
     import torch
     _check_input(x)
     _check_input(dy, "dy")
@@ -228,19 +298,17 @@ def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int 
     H = H2 // 2
     if H2 % 2 or tuple(dy.shape) != (T, H) or dy.device != x.device:
         raise ValueError("dy must be [T, H] for x [T, 2H], on the same device")
-    if topk_weights is not None:
-        if (topk_weights.dtype != torch.float32 or topk_weights.numel() != T
-                or not topk_weights.is_contiguous() or topk_weights.device != x.device):
-            raise TypeError("topk_weights must be a contiguous fp32 tensor of T elements on x's device")
+    _check_weights(topk_weights, T, x)
     g = max(num_per_channels, 1)
+    flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
     if out is None:
         out = torch.empty((T, 2 * H), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
-        out_sf = torch.empty((T, 2 * H // g), dtype=torch.float32, device=x.device)
+        out_sf = sf_tensor(T, 2 * H // g, flags, x.device)
     with torch.cuda.device(x.device):
-        st = tkq_swiglu_backward_cast(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(out),
-                                      _ptr(out_sf), T, H, num_per_channels, f,
-                                      _stream_handle(x.device))
+        st = tkq_swiglu_backward_cast_ex(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(out),
+                                         _ptr(out_sf), T, H, num_per_channels, f, flags,
+                                         _stream_handle(x.device))
     if st:
         raise TkqError(st, "tkq_swiglu_backward_cast")
     return out, out_sf

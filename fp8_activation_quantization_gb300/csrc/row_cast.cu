@@ -56,21 +56,67 @@ struct alignas(1024) RowSmem {
     int abort;
 };
 
+// Where the scales of a launch go (tkq_sf_layout flags; see tkq.h).
+struct SfLayout {
+    unsigned flags;  // TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR
+    int groups;      // groups per row (G)
+    int words;       // ceil(G / 4), packed layouts
+    int64_t rows4;   // T rounded up to a multiple of 4, column-major layouts
+};
+constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u;
+
+// Scale of group gj of `row` in the chosen layout.  Padding rows of the
+// column-major layouts (T <= row < rows4) get 0, and the unused bytes of a
+// row's last packed word are zeroed by the lane of its last group.
+__device__ __forceinline__ void store_scale(void* sf, const SfLayout& lay, int64_t row,
+                                            bool live, int gj, float sc) {
+    const bool cm = lay.flags & kSfColMajor;
+    if (!live && !(cm && row < lay.rows4)) return;
+    if (lay.flags & kSfPacked) {
+        const uint8_t byte = live ? static_cast<uint8_t>(__float_as_uint(sc) >> 23) : 0;
+        const int64_t word = cm ? static_cast<int64_t>(gj >> 2) * lay.rows4 + row
+                                : row * lay.words + (gj >> 2);
+        uint8_t* p = static_cast<uint8_t*>(sf) + word * 4;
+        p[gj & 3] = byte;
+        if (gj == lay.groups - 1)
+            for (int k = (gj & 3) + 1; k < 4; ++k) p[k] = 0;
+    } else {
+        const int64_t idx = cm ? static_cast<int64_t>(gj) * lay.rows4 + row
+                               : row * lay.groups + gj;
+        static_cast<float*>(sf)[idx] = live ? sc : 0.0f;
+    }
+}
+
 // absmax of one 1x128 group held by eight lanes (16 values each), its scale,
 // and the codes and scale stored for a live row.  EXACT selects the codes of
 // the exact quotient (plain cast) or of the product by the reciprocal scale.
-template <int FMT, bool EXACT>
+// SFX: the launch uses scale-layout options (power-of-two scales, packed
+// UE8M0, column-major); without it the scales are row-major fp32 at sfp.
+template <int FMT, bool EXACT, bool SFX>
 __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, float* sfp,
-                                           int j) {
+                                           int j, void* sf, const SfLayout& lay, int64_t row,
+                                           int gj) {
     float m = fmaxf(absmax8(v), absmax8(v + 8));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
     float sc, inv;
     group_scale<FMT>(m, sc, inv);
+    bool exact_div = EXACT;
+    if constexpr (SFX) {
+        if (lay.flags & (kSfRoundPow2 | kSfPacked)) {
+            // round the scale up to a power of two; y / s = y * 2^-k is then
+            // exact, so the product needs no correction
+            uint32_t b = __float_as_uint(sc);
+            if (b & 0x007FFFFFu) b = (b & 0x7F800000u) + 0x00800000u;
+            sc = __uint_as_float(b);
+            inv = __uint_as_float((254u << 23) - b);
+            exact_div = false;
+        }
+    }
     if (live) {
         uint2 lo, hi;
-        if constexpr (EXACT) {
+        if (exact_div) {
             lo = quantize8<FMT>(v, sc, inv);
             hi = quantize8<FMT>(v + 8, sc, inv);
         } else {
@@ -79,7 +125,13 @@ __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, 
         }
         st_stream(o + j, lo);
         st_stream(o + 8 + j, hi);
-        if (j == 0) st_stream(sfp, sc);
+    }
+    if (j == 0) {
+        if constexpr (SFX) {
+            store_scale(sf, lay, row, live, gj, sc);
+        } else {
+            if (live) st_stream(sfp, sc);
+        }
     }
 }
 
@@ -91,12 +143,12 @@ __device__ __forceinline__ void load16(const uint8_t* p, float* v) {
 
 // tmap: x [T, C] (plain) or [T, 2H] (gate | up); tmap_dy: dy [T, H] (backward
 // only).  C_out: channels per output operand (C or H).
-template <int FMT, int MODE>
+template <int FMT, int MODE, bool SFX>
 __global__ void __launch_bounds__(kThreads, 3)
     row_cast_kernel(const __grid_constant__ CUtensorMap tmap,
                     const __grid_constant__ CUtensorMap tmap_dy, const float* __restrict__ w,
-                    uint2* __restrict__ out, float* __restrict__ sf, int64_t T, int C_out,
-                    unsigned int* __restrict__ status) {
+                    uint2* __restrict__ out, float* __restrict__ sf, SfLayout lay, int64_t T,
+                    int C_out, unsigned int* __restrict__ status) {
     using MT = ModeTraits<MODE>;
     extern __shared__ uint8_t smem_raw[];
     RowSmem<MODE>& sm = *reinterpret_cast<RowSmem<MODE>*>(
@@ -177,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         if constexpr (MODE == kPlain) {
             float v[16];
             load16(p, v);
-            emit_group<FMT, true>(v, live, o, sfp, j);
+            emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else if constexpr (!MT::kBwd) {
             float g[16], u[16], v[16];
             load16(p, g);
@@ -187,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 v[k] = swiglu(g[k], u[k]);
                 if constexpr (MT::kWeighted) v[k] = __fmul_rn(v[k], wt);
             }
-            emit_group<FMT, false>(v, live, o, sfp, j);
+            emit_group<FMT, false, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else {
             float g[16], u[16], d[16], dg[16], du[16];
             load16(p, g);
@@ -201,8 +253,9 @@ __global__ void __launch_bounds__(kThreads, 3)
                     du[k] = __fmul_rn(du[k], wt);
                 }
             }
-            emit_group<FMT, false>(dg, live, o, sfp, j);
-            emit_group<FMT, false>(du, live, o + C_out / 8, sfp + CB, j);
+            emit_group<FMT, false, SFX>(dg, live, o, sfp, j, sf, lay, row, cb);
+            emit_group<FMT, false, SFX>(du, live, o + C_out / 8, sfp + CB, j, sf, lay, row,
+                                          static_cast<int>(CB) + cb);
         }
         // Release the stage only now: the stores above consume every value
         // read from it, so the shared loads have completed before the arrive
@@ -216,9 +269,22 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
 }
 
+template <int FMT, int MODE, bool SFX>
+cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& map_dy, const float* w,
+                        void* out, float* sf, const SfLayout& lay, int64_t T, int64_t C_out,
+                        cudaStream_t stream) {
+    auto* k = &row_cast_kernel<FMT, MODE, SFX>;
+    const size_t smem = sizeof(RowSmem<MODE>) + 1024;
+    const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
+    const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
+    k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, lay, T,
+                                        static_cast<int>(C_out), device_status_word());
+    return cudaGetLastError();
+}
+
 template <int FMT, int MODE>
-cudaError_t launch(const void* x, const void* dy, const float* w, void* out, float* sf,
-                   int64_t T, int64_t C_out, cudaStream_t stream) {
+cudaError_t launch(const void* x, const void* dy, const float* w, void* out, void* sf,
+                   int64_t T, int64_t C_out, unsigned sf_flags, cudaStream_t stream) {
     using MT = ModeTraits<MODE>;
     // x as a bf16 [T, cols] matrix: C columns (plain) or 2H (gate | up)
     const int64_t cols = (MT::kOperands == 1 ? 1 : 2) * C_out;
@@ -229,43 +295,44 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, flo
     } else {
         map_dy = map;  // unused
     }
-    auto* k = &row_cast_kernel<FMT, MODE>;
-    const size_t smem = sizeof(RowSmem<MODE>) + 1024;
-    const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
-    const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
-    k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, T,
-                                        static_cast<int>(C_out), device_status_word());
-    return cudaGetLastError();
+    SfLayout lay;
+    lay.flags = sf_flags;
+    lay.groups = static_cast<int>((MT::kBwd ? 2 : 1) * C_out / 128);
+    lay.words = (lay.groups + 3) / 4;
+    lay.rows4 = (T + 3) / 4 * 4;
+    float* sff = static_cast<float*>(sf);
+    return sf_flags ? launch_mode<FMT, MODE, true>(map, map_dy, w, out, sff, lay, T, C_out, stream)
+                    : launch_mode<FMT, MODE, false>(map, map_dy, w, out, sff, lay, T, C_out, stream);
+}
+
+template <int MODE>
+cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, void* out,
+                       void* sf, int64_t T, int64_t C_out, unsigned sf_flags,
+                       cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    return fmt == kFmtE4M3
+               ? launch<kFmtE4M3, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, stream)
+               : launch<kFmtE5M2, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
-                                  int fmt, cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
-    return fmt == kFmtE4M3 ? launch<kFmtE4M3, kPlain>(x, nullptr, nullptr, out, sf, T, C, stream)
-                           : launch<kFmtE5M2, kPlain>(x, nullptr, nullptr, out, sf, T, C, stream);
+cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
+                                  int fmt, unsigned sf_flags, cudaStream_t stream) {
+    return launch_fmt<kPlain>(fmt, x, nullptr, nullptr, out, sf, T, C, sf_flags, stream);
 }
 
-cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
-                               int64_t H, int fmt, cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
-    if (fmt == kFmtE4M3)
-        return w ? launch<kFmtE4M3, kSwigluWeighted>(x, nullptr, w, out, sf, T, H, stream)
-                 : launch<kFmtE4M3, kSwiglu>(x, nullptr, w, out, sf, T, H, stream);
-    return w ? launch<kFmtE5M2, kSwigluWeighted>(x, nullptr, w, out, sf, T, H, stream)
-             : launch<kFmtE5M2, kSwiglu>(x, nullptr, w, out, sf, T, H, stream);
+cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
+                               int64_t H, int fmt, unsigned sf_flags, cudaStream_t stream) {
+    return w ? launch_fmt<kSwigluWeighted>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream)
+             : launch_fmt<kSwiglu>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream);
 }
 
 cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
-                                        float* sf, int64_t T, int64_t H, int fmt,
-                                        cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
-    if (fmt == kFmtE4M3)
-        return w ? launch<kFmtE4M3, kBackwardWeighted>(x, dy, w, out, sf, T, H, stream)
-                 : launch<kFmtE4M3, kBackward>(x, dy, w, out, sf, T, H, stream);
-    return w ? launch<kFmtE5M2, kBackwardWeighted>(x, dy, w, out, sf, T, H, stream)
-             : launch<kFmtE5M2, kBackward>(x, dy, w, out, sf, T, H, stream);
+                                        void* sf, int64_t T, int64_t H, int fmt,
+                                        unsigned sf_flags, cudaStream_t stream) {
+    return w ? launch_fmt<kBackwardWeighted>(fmt, x, dy, w, out, sf, T, H, sf_flags, stream)
+             : launch_fmt<kBackward>(fmt, x, dy, w, out, sf, T, H, sf_flags, stream);
 }
 
 }  // namespace tkq

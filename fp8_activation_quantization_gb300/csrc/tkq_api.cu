@@ -184,63 +184,105 @@ tkq_status check_common(int64_t T, int64_t C, int group, int fmt) {
 
 tkq_status launch_status(cudaError_t e) { return e == cudaSuccess ? TKQ_OK : TKQ_ERR_CUDA; }
 
+constexpr unsigned kSfAllFlags = TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR;
+
 }  // namespace
 
 extern "C" {
 
-tkq_status tkq_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
-                              int group, int fmt, tkq_stream_t stream) {
+int64_t tkq_sf_bytes(int64_t T, int64_t groups_per_row, unsigned sf_flags) {
+    if (T < 0 || groups_per_row < 0 || (sf_flags & ~kSfAllFlags)) return -1;
+    const int64_t T4 = (T + 3) / 4 * 4;
+    const int64_t W = (groups_per_row + 3) / 4;
+    const bool cm = sf_flags & TKQ_SF_COL_MAJOR;
+    if (sf_flags & TKQ_SF_UE8M0_PACKED) return (cm ? W * T4 : T * W) * 4;
+    return (cm ? groups_per_row * T4 : T * groups_per_row) * 4;
+}
+
+namespace {
+// Checks shared by the row casts: scale flags, scale-buffer alignment.
+tkq_status check_sf(const void* sf, unsigned sf_flags) {
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
+    const uintptr_t a = (sf_flags & TKQ_SF_COL_MAJOR) ? 16 : 4;
+    return tkq::aligned(sf, a) ? TKQ_OK : TKQ_ERR_ALIGN;
+}
+}  // namespace
+
+tkq_status tkq_per_token_cast_ex(const void* x, void* out, void* sf, int64_t T, int64_t C,
+                                 int group, int fmt, unsigned sf_flags, tkq_stream_t stream) {
     tkq_status st = check_common(T, C, group, fmt);
     if (st != TKQ_OK) return st;
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
     if (T == 0) return TKQ_OK;
     if (!x || !out || !sf) return TKQ_ERR_NULL;
-    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4))
-        return TKQ_ERR_ALIGN;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16)) return TKQ_ERR_ALIGN;
+    if ((st = check_sf(sf, sf_flags)) != TKQ_OK) return st;
     const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
-               rs = tkq::span(sf, T * (C / group) * 4);
+               rs = tkq::span(sf, tkq_sf_bytes(T, C / group, sf_flags));
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
-    return launch_status(tkq::launch_per_token_cast(x, out, sf, T, C, fmt,
+    return launch_status(tkq::launch_per_token_cast(x, out, sf, T, C, fmt, sf_flags,
                                                     static_cast<cudaStream_t>(stream)));
 }
 
-tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
-                           int64_t H, int group, int fmt, tkq_stream_t stream) {
+tkq_status tkq_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                              int group, int fmt, tkq_stream_t stream) {
+    return tkq_per_token_cast_ex(x, out, sf, T, C, group, fmt, 0u, stream);
+}
+
+tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf, int64_t T,
+                              int64_t H, int group, int fmt, unsigned sf_flags,
+                              tkq_stream_t stream) {
     tkq_status st = check_common(T, H, group, fmt);
     if (st != TKQ_OK) return st;
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
     if (T == 0) return TKQ_OK;
     if (!x || !out || !sf) return TKQ_ERR_NULL;
-    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4) ||
-        (w && !tkq::aligned(w, 4)))
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || (w && !tkq::aligned(w, 4)))
         return TKQ_ERR_ALIGN;
+    if ((st = check_sf(sf, sf_flags)) != TKQ_OK) return st;
     const auto rx = tkq::span(x, T * H * 4), ro = tkq::span(out, T * H),
-               rs = tkq::span(sf, T * (H / group) * 4);
+               rs = tkq::span(sf, tkq_sf_bytes(T, H / group, sf_flags));
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
     if (w) {
         const auto rw = tkq::span(w, T * 4);
         if (tkq::overlap(rw, ro) || tkq::overlap(rw, rs)) return TKQ_ERR_ALIAS;
     }
-    return launch_status(tkq::launch_swiglu_cast(x, w, out, sf, T, H, fmt,
+    return launch_status(tkq::launch_swiglu_cast(x, w, out, sf, T, H, fmt, sf_flags,
                                                  static_cast<cudaStream_t>(stream)));
 }
 
-tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
-                                    float* sf, int64_t T, int64_t H, int group, int fmt,
-                                    tkq_stream_t stream) {
+tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
+                           int64_t H, int group, int fmt, tkq_stream_t stream) {
+    return tkq_swiglu_cast_ex(x, w, out, sf, T, H, group, fmt, 0u, stream);
+}
+
+tkq_status tkq_swiglu_backward_cast_ex(const void* x, const void* dy, const float* w, void* out,
+                                       void* sf, int64_t T, int64_t H, int group, int fmt,
+                                       unsigned sf_flags, tkq_stream_t stream) {
     tkq_status st = check_common(T, H, group, fmt);
     if (st != TKQ_OK) return st;
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
     if (T == 0) return TKQ_OK;
     if (!x || !dy || !out || !sf) return TKQ_ERR_NULL;
     if (!tkq::aligned(x, 16) || !tkq::aligned(dy, 16) || !tkq::aligned(out, 16) ||
-        !tkq::aligned(sf, 4) || (w && !tkq::aligned(w, 4)))
+        (w && !tkq::aligned(w, 4)))
         return TKQ_ERR_ALIGN;
-    const auto ro = tkq::span(out, T * 2 * H), rs = tkq::span(sf, T * (2 * H / group) * 4);
+    if ((st = check_sf(sf, sf_flags)) != TKQ_OK) return st;
+    const auto ro = tkq::span(out, T * 2 * H),
+               rs = tkq::span(sf, tkq_sf_bytes(T, 2 * H / group, sf_flags));
     const tkq::Range inputs[3] = {tkq::span(x, T * H * 4), tkq::span(dy, T * H * 2),
                                   w ? tkq::span(w, T * 4) : tkq::Range{0, 0}};
     if (tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
     for (const auto& in : inputs)
         if (tkq::overlap(in, ro) || tkq::overlap(in, rs)) return TKQ_ERR_ALIAS;
-    return launch_status(tkq::launch_swiglu_backward_cast(x, dy, w, out, sf, T, H, fmt,
+    return launch_status(tkq::launch_swiglu_backward_cast(x, dy, w, out, sf, T, H, fmt, sf_flags,
                                                           static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
+                                    float* sf, int64_t T, int64_t H, int group, int fmt,
+                                    tkq_stream_t stream) {
+    return tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group, fmt, 0u, stream);
 }
 
 tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
@@ -305,6 +347,7 @@ const char* tkq_status_string(int status) {
         case TKQ_ERR_ALIGN: return "TKQ_ERR_ALIGN: misaligned pointer";
         case TKQ_ERR_CUDA: return "TKQ_ERR_CUDA: kernel launch failed";
         case TKQ_ERR_ALIAS: return "TKQ_ERR_ALIAS: buffers overlap";
+        case TKQ_ERR_FLAGS: return "TKQ_ERR_FLAGS: unknown option flags";
         default: return "TKQ_ERR_UNKNOWN";
     }
 }

@@ -28,15 +28,16 @@ unsigned int* device_status_word();
 // Persistent grid: min(blocks needed, SMs x resident blocks per SM).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
 
-cudaError_t launch_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
-                                  int fmt, cudaStream_t stream);
+// sf_flags: TKQ_SF_* options of include/tkq.h (0 = row-major fp32 scales).
+cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
+                                  int fmt, unsigned sf_flags, cudaStream_t stream);
 
-cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
-                               int64_t H, int fmt, cudaStream_t stream);
+cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
+                               int64_t H, int fmt, unsigned sf_flags, cudaStream_t stream);
 
 cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
-                                        float* sf, int64_t T, int64_t H, int fmt,
-                                        cudaStream_t stream);
+                                        void* sf, int64_t T, int64_t H, int fmt,
+                                        unsigned sf_flags, cudaStream_t stream);
 
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,

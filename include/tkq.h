@@ -66,7 +66,8 @@ typedef enum {
     TKQ_ERR_FMT = 4,
     TKQ_ERR_ALIGN = 5,
     TKQ_ERR_CUDA = 6,
-    TKQ_ERR_ALIAS = 7
+    TKQ_ERR_ALIAS = 7,
+    TKQ_ERR_FLAGS = 8
 } tkq_status;
 
 /* A cudaStream_t passed as an opaque pointer. */
@@ -94,8 +95,11 @@ tkq_status tkq_per_token_cast(const void* x, void* out, float* sf,
  *   w   : fp32 [T] or NULL (no weight)
  *   out : FP8 codes [T, H];  sf : fp32 [T, H/128]
  * T >= 0; H > 0, H % 128 == 0.
- * exp() is the CUDA math library's; y may differ from an exactly rounded
- * evaluation by a few ulp, so codes are not bit-pinned to a CPU evaluation.
+ * exp(-g) and the reciprocal come from the SM's ex2.approx / rcp.approx, so y
+ * may differ from exactly rounded binary32 steps by a few ulp, and codes are
+ * those of y times the rounded reciprocal of s (as the TileKernels kernel
+ * multiplies by sf_inv, [P2] §3.2): they are not bit-pinned to a CPU
+ * evaluation (parity: scales within 1e-6 relative, codes within one FP8 step).
  */
 tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf,
                            int64_t T, int64_t H, int group, int fmt,
@@ -116,7 +120,51 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
                              tkq_stream_t stream);
 
 /*
- * Device status word.  The pipelined kernels (tkq_swiglu_cast_t) wait on
+ * Scale-factor layouts ([P2] §3.1: the round_sf, use_packed_ue8m0 and
+ * use_tma_aligned_col_major_sf options of the cast config; [P1] §4C: the
+ * scales are written directly in the layout a TMA-fed FP8 GEMM reads, so no
+ * separate re-layout pass is needed).  Flags, combinable:
+ *   TKQ_SF_ROUND_POW2    every scale is rounded up to a power of two,
+ *                        s = 2^ceil(log2 s0) with s0 the plain fp32 scale;
+ *                        codes are those of y / s (exact: a power-of-two
+ *                        scaling).
+ *   TKQ_SF_UE8M0_PACKED  each scale is stored as its UE8M0 byte (the biased
+ *                        binary32 exponent; value 2^(byte - 127)), four
+ *                        consecutive groups of a row per 32-bit word, group
+ *                        4k+i in byte i (little-endian).  Implies ROUND_POW2.
+ *   TKQ_SF_COL_MAJOR     scales stored column-major: entry (t, j) at
+ *                        j * T4 + t, T4 = T rounded up to a multiple of 4, so
+ *                        every column starts 16-byte aligned (sf must be
+ *                        16-byte aligned); padding rows hold 0.
+ * With G groups per row (C/128, H/128, or 2H/128 for the backward) and
+ * W = ceil(G/4), sf is
+ *   fp32 [T, G] (no flags), fp32 [G, T4] (COL_MAJOR),
+ *   int32 [T, W] (UE8M0_PACKED), int32 [W, T4] (UE8M0_PACKED | COL_MAJOR);
+ * bytes of a row's last word beyond group G-1 are 0.  Unknown bits give
+ * TKQ_ERR_FLAGS.
+ */
+#define TKQ_SF_ROUND_POW2 1u
+#define TKQ_SF_UE8M0_PACKED 2u
+#define TKQ_SF_COL_MAJOR 4u
+
+/* Size in bytes of the scale buffer for T rows of groups_per_row groups under
+ * sf_flags, or -1 for invalid arguments. */
+int64_t tkq_sf_bytes(int64_t T, int64_t groups_per_row, unsigned sf_flags);
+
+/* tkq_per_token_cast, tkq_swiglu_cast and tkq_swiglu_backward_cast with a
+ * scale-factor layout (sf_flags above; sf sized by tkq_sf_bytes).  With
+ * sf_flags == 0 they are the calls above. */
+tkq_status tkq_per_token_cast_ex(const void* x, void* out, void* sf, int64_t T, int64_t C,
+                                 int group, int fmt, unsigned sf_flags, tkq_stream_t stream);
+tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf, int64_t T,
+                              int64_t H, int group, int fmt, unsigned sf_flags,
+                              tkq_stream_t stream);
+tkq_status tkq_swiglu_backward_cast_ex(const void* x, const void* dy, const float* w, void* out,
+                                       void* sf, int64_t T, int64_t H, int group, int fmt,
+                                       unsigned sf_flags, tkq_stream_t stream);
+
+/*
+ * Device status word.  The pipelined kernels (every cast above) wait on
  * shared-memory barriers for their bulk copies; every such wait gives up after
  * one second, sets TKQ_DEVICE_TIMEOUT in the current device's status word and
  * lets the kernel return (its outputs are then incomplete) instead of hanging.

@@ -110,6 +110,35 @@ def test_swiglu_backward_validation(lib, args, expected):
     assert lib.tkq_swiglu_backward_cast(*args, None) == expected
 
 
+def test_sf_bytes(lib):
+    # T = 13 rows (T4 = 16), G = 7 groups (W = 2 words)
+    assert lib.tkq_sf_bytes(13, 7, 0) == 13 * 7 * 4
+    assert lib.tkq_sf_bytes(13, 7, 4) == 7 * 16 * 4
+    assert lib.tkq_sf_bytes(13, 7, 2) == 13 * 2 * 4
+    assert lib.tkq_sf_bytes(13, 7, 6) == 2 * 16 * 4
+    assert lib.tkq_sf_bytes(13, 7, 1) == 13 * 7 * 4
+    assert lib.tkq_sf_bytes(13, 7, 8) == -1 and lib.tkq_sf_bytes(-1, 7, 0) == -1
+
+
+@pytest.mark.parametrize("flags,sf_off,expected", [
+    (8, 0, 8),            # unknown flag bit
+    (4, 4, 5),            # column-major scales must be 16-byte aligned
+    (6, 8, 5),            # packed column-major too
+    (2, 2, 5),            # packed row-major: 4-byte aligned
+])
+def test_ex_validation(lib, flags, sf_off, expected):
+    args = (p(), p(1 << 24), p((2 << 24) + sf_off), 4, 256, 128, 0, flags, None)
+    assert lib.tkq_per_token_cast_ex(*args) == expected
+
+
+def test_ex_empty_batch_and_flags(lib):
+    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 6, None) == 0
+    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 9, None) == 8
+    assert lib.tkq_swiglu_cast_ex(None, None, None, None, 0, 256, 128, 0, 16, None) == 8
+    assert lib.tkq_swiglu_backward_cast_ex(None, None, None, None, None, 0, 256, 128, 0, 4,
+                                           None) == 0
+
+
 def test_status_calls_validate_before_cuda(lib):
     assert lib.tkq_read_device_status(None, 0) == 1          # NULL flags
     assert lib.tkq_selftest_wait_timeout(0, None) == 2       # limit out of range

@@ -403,6 +403,114 @@ def test_swiglu_backward_tensor_api(cuda_device):
 
 
 # ---------------------------------------------------------------------------
+# scale-factor layouts
+# ---------------------------------------------------------------------------
+
+SF_FLAG_SETS = [0, 1, 2, 4, 5, 6]
+
+
+def sf_rowmajor(raw: np.ndarray, T: int, G: int, flags: int) -> np.ndarray:
+    """Any scale layout (raw bytes) -> fp32 [T, G] (test-side decoding)."""
+    T4 = (T + 3) // 4 * 4
+    W = (G + 3) // 4
+    if flags & 2:
+        words = raw.view(np.uint32).reshape((W, T4) if flags & 4 else (T, W))
+        if flags & 4:
+            words = np.ascontiguousarray(words.T[:T])
+        b = words.view(np.uint8).reshape(T, W * 4)[:, :G].astype(np.float64)
+        return np.exp2(b - 127).astype(np.float32)
+    s = raw.view(np.float32).reshape((G, T4) if flags & 4 else (T, G))
+    return np.ascontiguousarray(s.T[:T] if flags & 4 else s)
+
+
+def run_ex(kind, x_bits, flags, fmt, dev, w=None, dy_bits=None):
+    T = x_bits.shape[0]
+    if kind == "plain":
+        C_out, G = x_bits.shape[1], x_bits.shape[1] // 128
+    elif kind == "swiglu":
+        C_out, G = x_bits.shape[1] // 2, x_bits.shape[1] // 256
+    else:
+        C_out, G = x_bits.shape[1], x_bits.shape[1] // 128
+    xd = to_dev_bf16(x_bits, dev)
+    out = Guarded(T * C_out, dev)
+    nbytes = tkq.tkq_sf_bytes(T, G, flags)
+    sf = Guarded(nbytes, dev)
+    wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
+    wp = None if wd is None else ctypes.c_void_p(wd.data_ptr())
+    s = stream_of(dev)
+    fc = oracle.FMT[fmt]
+    if kind == "plain":
+        st = tkq.tkq_per_token_cast_ex(ctypes.c_void_p(xd.data_ptr()), out.ptr, sf.ptr, T, C_out,
+                                       128, fc, flags, s)
+    elif kind == "swiglu":
+        st = tkq.tkq_swiglu_cast_ex(ctypes.c_void_p(xd.data_ptr()), wp, out.ptr, sf.ptr, T, C_out,
+                                    128, fc, flags, s)
+    else:
+        dyd = to_dev_bf16(dy_bits, dev)
+        st = tkq.tkq_swiglu_backward_cast_ex(ctypes.c_void_p(xd.data_ptr()),
+                                             ctypes.c_void_p(dyd.data_ptr()), wp, out.ptr, sf.ptr,
+                                             T, C_out // 2, 128, fc, flags, s)
+    assert st == 0, tkq.tkq_status_string(st)
+    torch.cuda.synchronize()
+    out.check_guards("out")
+    sf.check_guards("sf")
+    return out.data().reshape(T, C_out), sf.data(), G
+
+
+@pytest.mark.parametrize("flags", SF_FLAG_SETS)
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_plain_cast_sf_layouts_bit_exact(cuda_device, flags, fmt):
+    # G = 7 groups (a partly used last packed word), T = 1031 (padding rows)
+    x = synth.workload("plain_outlier", rows=1031)["x"][:, :896].copy()
+    out, raw, G = run_ex("plain", x, flags, fmt, cuda_device)
+    ro, rs = oracle.per_token_cast_ex(x, fmt, 128, flags, threads=THREADS)
+    parity.assert_bit_exact("codes", out, ro)
+    parity.assert_bit_exact("scales (raw layout bytes)", raw, rs.view(np.uint8).ravel())
+
+
+def _pow2_boundary(s0: np.ndarray, tol=2e-6) -> np.ndarray:
+    """Groups whose plain scale lies within tol (relative) of a power of two:
+    a few ulp of SwiGLU error can move their rounded-up scale by one binade."""
+    m, _ = np.frexp(s0.astype(np.float64))
+    return (np.abs(m - 0.5) < tol) | (np.abs(m - 1.0) < tol)
+
+
+@pytest.mark.parametrize("kind", ["swiglu", "backward"])
+@pytest.mark.parametrize("flags", [1, 2, 4, 6])
+def test_swiglu_sf_layouts(cuda_device, kind, flags):
+    if kind == "swiglu":
+        d = synth.workload("swiglu_moe", rows=1031)
+        x = np.ascontiguousarray(d["x"][:, np.r_[0:896, 2048:2944]])
+        out, raw, G = run_ex("swiglu", x, flags, "e4m3", cuda_device, w=d["w"])
+        y = oracle.swiglu_values(x, d["w"], threads=THREADS)
+    else:
+        d = synth.workload("swiglu_bwd", rows=1031)
+        x = np.ascontiguousarray(d["x"][:, np.r_[0:384, 2048:2432]])
+        dy = np.ascontiguousarray(d["dy"][:, :384])
+        out, raw, G = run_ex("backward", x, flags, "e4m3", cuda_device, w=d["w"], dy_bits=dy)
+        y = oracle.swiglu_backward_values(x, dy, d["w"], threads=THREADS)
+    T = x.shape[0]
+    ro, rs = oracle.cast_rows_f32_ex(y, "e4m3", 128, flags, threads=THREADS)
+    got = sf_rowmajor(raw, T, G, flags)
+    exp = sf_rowmajor(rs.view(np.uint8).ravel(), T, G, flags)
+    if flags & 4:  # padding rows of column-major layouts are zero
+        T4 = (T + 3) // 4 * 4
+        if flags & 2:
+            pad = raw.view(np.uint32).reshape(-1, T4)[:, T:]
+        else:
+            pad = raw.view(np.float32).reshape(G, T4)[:, T:]
+        assert np.all(pad == 0)
+    _, s0 = oracle.cast_rows_f32(y, "e4m3")
+    skip = _pow2_boundary(s0) if flags & 3 else np.zeros_like(s0, bool)
+    assert skip.sum() <= 2, "too many groups at a power-of-two boundary"
+    keep = ~skip
+    parity.assert_scales_close("scales", got[keep], exp[keep])
+    ok_rows = np.repeat(keep, 128, axis=1)
+    parity.assert_codes_close("codes", out[ok_rows], ro[ok_rows],
+                              max_frac=max(1e-4, 1.0 / out.size))
+
+
+# ---------------------------------------------------------------------------
 # ABI behaviour on a GPU
 # ---------------------------------------------------------------------------
 
