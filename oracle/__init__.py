@@ -124,6 +124,12 @@ def _configure(lib):
     lib.ora_sf_bytes.restype = i64
     lib.ora_cast_rows_f32_ex.argtypes = [p, i64, i64, i64, i, i, p, p]
     lib.ora_cast_rows_f32_ex.restype = ctypes.c_int
+    lib.ora_per_channel_cast.argtypes = [p, i64, i64, i64, i, i, p, p]
+    lib.ora_per_channel_cast.restype = ctypes.c_int
+    lib.ora_per_block_cast.argtypes = [p, i64, i64, i64, i, p, p]
+    lib.ora_per_block_cast.restype = ctypes.c_int
+    lib.ora_cast_back.argtypes = [p, p, i64, i64, i64, i64, i, p]
+    lib.ora_cast_back.restype = ctypes.c_int
     lib.ora_swiglu_backward_values.argtypes = [p, p, p, i64, i64, p]
     lib.ora_swiglu_backward_cast.argtypes = [p, p, p, i64, i64, i64, i, p, p]
     for f in ("ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
@@ -431,3 +437,79 @@ def per_token_cast_ex(x_bits: np.ndarray, fmt="e4m3", group: int = 128, flags: i
     """bf16 [T, C] (exact widening to fp32) -> the cast with scale options."""
     xf = (np.ascontiguousarray(x_bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     return cast_rows_f32_ex(xf, fmt, group, flags, threads)
+
+
+# --------------------------------------------------------------------------
+# per-channel / per-block casts and cast back
+# --------------------------------------------------------------------------
+
+def per_channel_cast(x_bits: np.ndarray, fmt="e4m3", group: int = 128, transpose: bool = False,
+                     threads: int = 1):
+    """bf16 [T, C] -> codes ([T, C], or [C, T] with transpose) and scales
+    ([T/group, C], or [C, T/group]) with groups of `group` tokens per channel."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, C = x_bits.shape
+    if group <= 0 or T % group:
+        raise ValueError("T must be a multiple of group")
+    f = _fmt(fmt)
+    out = np.empty((C, T) if transpose else (T, C), np.uint8)
+    sf = np.empty((C, T // group) if transpose else (T // group, C), np.float32)
+    if threads <= 1 or C < 256:
+        _check(lib.ora_per_channel_cast(_ptr(x_bits), T, C, group, f, int(transpose),
+                                        _ptr(out), _ptr(sf)), "per_channel_cast")
+        return out, sf
+
+    # independent row blocks of `group` tokens
+    def body(a, b):
+        n = b - a
+        o = np.empty((C, n) if transpose else (n, C), np.uint8)
+        s = np.empty((C, n // group) if transpose else (n // group, C), np.float32)
+        _check(lib.ora_per_channel_cast(_ptr(np.ascontiguousarray(x_bits[a:b])), n, C, group, f,
+                                        int(transpose), _ptr(o), _ptr(s)), "per_channel_cast")
+        if transpose:
+            out[:, a:b] = o
+            sf[:, a // group:b // group] = s
+        else:
+            out[a:b] = o
+            sf[a // group:b // group] = s
+
+    _row_parallel(T, threads, body, align=group)
+    return out, sf
+
+
+def per_block_cast(x_bits: np.ndarray, fmt="e4m3", block: int = 128, threads: int = 1):
+    """bf16 [T, C] -> (codes [T, C], scales [ceil(T/block), C/block])."""
+    lib = _load()
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, C = x_bits.shape
+    if block <= 0 or C % block:
+        raise ValueError("block must divide C")
+    f = _fmt(fmt)
+    out = np.empty((T, C), np.uint8)
+    sf = np.empty((-(-T // block), C // block), np.float32)
+
+    def body(a, b):
+        _check(lib.ora_per_block_cast(_ptr(x_bits[a:b]), b - a, C, block, f, _ptr(out[a:b]),
+                                      _ptr(sf[a // block:-(-b // block)])), "per_block_cast")
+
+    _row_parallel(T, threads, body, align=block)
+    return out, sf
+
+
+def cast_back(codes: np.ndarray, sf: np.ndarray, group_rows: int = 1, group_cols: int = 128,
+              fmt="e4m3", threads: int = 1) -> np.ndarray:
+    """codes uint8 [T, C], sf fp32 [ceil(T/gr), C/gc] -> fp32 [T, C] = decode * scale."""
+    lib = _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sf = np.ascontiguousarray(sf, dtype=np.float32)
+    T, C = codes.shape
+    out = np.empty((T, C), np.float32)
+    f = _fmt(fmt)
+
+    def body(a, b):
+        _check(lib.ora_cast_back(_ptr(codes[a:b]), _ptr(sf[a // group_rows:]), b - a, C,
+                                 group_rows, group_cols, f, _ptr(out[a:b])), "cast_back")
+
+    _row_parallel(T, threads, body, align=group_rows)
+    return out

@@ -347,3 +347,73 @@ int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, in
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Per-channel and per-block casts, cast back ("TileKernels 与 DeepGEMM 的    */
+/* 分界线" §2 operator table: per_channel_cast (+transpose), per_block_cast, */
+/* cast_back)                                                                */
+/* ------------------------------------------------------------------------ */
+
+int ora_per_channel_cast(const uint16_t* x, int64_t T, int64_t C, int64_t group, int fmt,
+                         int transpose, uint8_t* out, float* sf) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || C < 0 || group <= 0 || T % group) return -1;
+    const int64_t B = T / group;
+    float* v = (float*)malloc((size_t)(group > 0 ? group : 1) * sizeof(float));
+    if (!v) return -1;
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t b = 0; b < B; ++b) {
+            for (int64_t i = 0; i < group; ++i)
+                v[i] = ora_bf16_to_f32(x[(b * group + i) * C + c]);
+            if (transpose) {
+                /* codes of channel c land contiguously in row c of [C, T] */
+                sf[c * B + b] = cast_group(v, group, 1, fmt, out + c * T + b * group, 1);
+            } else {
+                /* codes stay at [t, c] */
+                sf[b * C + c] = cast_group(v, group, 1, fmt, out + (b * group) * C + c, C);
+            }
+        }
+    }
+    free(v);
+    return 0;
+}
+
+int ora_per_block_cast(const uint16_t* x, int64_t T, int64_t C, int64_t block, int fmt,
+                       uint8_t* out, float* sf) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || C < 0 || block <= 0 || C % block) return -1;
+    const int64_t RB = (T + block - 1) / block;
+    const int64_t CB = C / block;
+    float* v = (float*)malloc((size_t)(block * block > 0 ? block * block : 1) * sizeof(float));
+    if (!v) return -1;
+    for (int64_t rb = 0; rb < RB; ++rb) {
+        const int64_t r0 = rb * block;
+        const int64_t rows = (T - r0 < block) ? T - r0 : block;
+        for (int64_t cb = 0; cb < CB; ++cb) {
+            /* the block's rows, one after the other */
+            for (int64_t r = 0; r < rows; ++r)
+                for (int64_t c = 0; c < block; ++c)
+                    v[r * block + c] = ora_bf16_to_f32(x[(r0 + r) * C + cb * block + c]);
+            const float s = ora_group_scale(group_absmax(v, rows * block, 1), fmt);
+            sf[rb * CB + cb] = s;
+            for (int64_t r = 0; r < rows; ++r)
+                encode_group(v + r * block, block, 1, s, fmt, out + (r0 + r) * C + cb * block, 1);
+        }
+    }
+    free(v);
+    return 0;
+}
+
+int ora_cast_back(const uint8_t* codes, const float* sf, int64_t T, int64_t C, int64_t gr,
+                  int64_t gc, int fmt, float* out) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || C < 0 || gr <= 0 || gc <= 0 || C % gc) return -1;
+    const int64_t G = C / gc;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            const double v = ora_fp8_decode(codes[t * C + c], fmt);
+            const float s = sf[(t / gr) * G + c / gc];
+            out[t * C + c] = (float)v * s;   /* decode is exact in binary32 */
+        }
+    return 0;
+}

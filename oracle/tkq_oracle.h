@@ -134,6 +134,28 @@ int64_t ora_sf_bytes(int64_t T, int64_t G, int flags);
 int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, int fmt,
                          int flags, uint8_t* out, void* sf);
 
+/* Per-channel cast of a bf16 [T, C] matrix ([P1] §2 per_channel_cast
+ * (+transpose)): groups of `group` consecutive tokens of one channel.
+ * transpose == 0: out [T, C] codes in place, sf fp32 [T/group, C];
+ * transpose != 0: out [C, T] (the column-major copy), sf fp32 [C, T/group].
+ * T must be a multiple of group. */
+int ora_per_channel_cast(const uint16_t* x, int64_t T, int64_t C, int64_t group, int fmt,
+                         int transpose, uint8_t* out, float* sf);
+
+/* Per-block cast of a bf16 [T, C] matrix ([P1] §2 per_block_cast): one scale
+ * per block of `block` x `block` elements (the last row block may be short:
+ * its amax covers the rows that exist).  out [T, C] codes, sf fp32
+ * [ceil(T/block), C/block]. */
+int ora_per_block_cast(const uint16_t* x, int64_t T, int64_t C, int64_t block, int fmt,
+                       uint8_t* out, float* sf);
+
+/* Cast back ([P1] §2 cast_back): y = fl32(decode(code) * s) for codes [T, C]
+ * with scales of groups of gr rows x gc columns, sf row-major
+ * [ceil(T/gr), C/gc] (gr, gc = 1 x 128 per-token, 128 x 1 per-channel,
+ * 128 x 128 per-block).  out fp32 [T, C]. */
+int ora_cast_back(const uint8_t* codes, const float* sf, int64_t T, int64_t C, int64_t gr,
+                  int64_t gc, int fmt, float* out);
+
 /* Gradient of y = silu(g) * u [* w] for a bf16 [T, 2H] gate|up input and a
  * bf16 [T, H] upstream gradient dy, written as the fp32 [T, 2H] matrix
  * [dg | du]:

@@ -54,6 +54,14 @@ MUTANTS = [
      "((uint8_t*)sf)[word * 4 + 3 - j % 4]"),
     ("column-major scales without padding", "((float*)sf)[cm ? j * T4 + t : t * G + j] = s;",
      "((float*)sf)[cm ? j * T + t : t * G + j] = s;"),
+    ("per-channel codes written along the row",
+     "sf[b * C + c] = cast_group(v, group, 1, fmt, out + (b * group) * C + c, C);",
+     "sf[b * C + c] = cast_group(v, group, 1, fmt, out + (b * group) * C + c, 1);"),
+    ("per-block scale from the first row only",
+     "const float s = ora_group_scale(group_absmax(v, rows * block, 1), fmt);",
+     "const float s = ora_group_scale(group_absmax(v, block, 1), fmt);"),
+    ("cast back ignores the column group", "const float s = sf[(t / gr) * G + c / gc];",
+     "const float s = sf[(t / gr) * G];"),
 ]
 
 # cheapest first: most mistakes are caught by the hand-worked fixtures
@@ -67,6 +75,9 @@ CHECKS = [
     (pins.test_swiglu_vs_binary64, {}),
     (pins.test_swiglu_backward_special_cases, {}),
     (pins.test_round_pow2_hand_group, {}),
+    (pins.test_cast_back_hand_values_and_granularities, {}),
+    (pins.test_per_channel_is_per_token_of_transpose, {"fmt": "e4m3"}),
+    (pins.test_per_block_is_per_token_of_flattened_blocks, {"fmt": "e4m3", "T": 300}),
     (pins.test_pow2_ceil_against_numpy_and_properties, {}),
     (pins.test_sf_layouts_rearrange_the_row_major_scales, {"flags": oracle.SF_COL_MAJOR}),
     (pins.test_sf_layouts_rearrange_the_row_major_scales,

@@ -564,3 +564,69 @@ def test_sf_layouts_rearrange_the_row_major_scales(flags):
     else:
         assert s.shape == (G, T4)
         assert np.array_equal(s[:, :T], s_ref.T) and np.all(s[:, T:] == 0)
+
+
+# ---------------------------------------------------------------------------
+# per-channel / per-block casts, cast back
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_per_channel_is_per_token_of_transpose(fmt):
+    x = _random_bits(T=256, C=384, seed=71)
+    xt = np.ascontiguousarray(x.T)
+    ct, st = oracle.per_token_cast(xt, fmt)            # [C, T], [C, T/128]
+    c1, s1 = oracle.per_channel_cast(x, fmt, 128, transpose=True)
+    assert np.array_equal(c1, ct) and np.array_equal(s1.view(np.uint32), st.view(np.uint32))
+    c0, s0 = oracle.per_channel_cast(x, fmt, 128, transpose=False)
+    assert np.array_equal(c0, ct.T) and np.array_equal(s0.view(np.uint32), st.T.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("T", [256, 300])
+def test_per_block_is_per_token_of_flattened_blocks(fmt, T):
+    """Each 128 x 128 block flattened into one row of 16384 values is one group
+    of the per-token cast (group = 16384; the short last block: rows * 128)."""
+    x = _random_bits(T=T, C=384, seed=73)
+    codes, sf = oracle.per_block_cast(x, fmt, 128)
+    for rb in range(-(-T // 128)):
+        r0, r1 = rb * 128, min(T, rb * 128 + 128)
+        for cb in range(3):
+            blk = np.ascontiguousarray(x[r0:r1, cb * 128:(cb + 1) * 128]).reshape(1, -1)
+            c, s = oracle.per_token_cast(blk, fmt, group=blk.shape[1])
+            assert s[0, 0] == sf[rb, cb]
+            assert np.array_equal(c.reshape(r1 - r0, 128), codes[r0:r1, cb * 128:(cb + 1) * 128])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_cast_back_matches_torch_decode(fmt):
+    x = _random_bits(T=64, C=512, seed=79)
+    codes, sf = oracle.per_token_cast(x, fmt)
+    y = oracle.cast_back(codes, sf, 1, 128, fmt)
+    dec = torch.from_numpy(codes).view(TORCH_FP8[fmt]).to(torch.float32).numpy()
+    ref = dec * np.repeat(sf, 128, axis=1)
+    assert np.array_equal(y.view(np.uint32), ref.view(np.uint32))
+    # round trip within half an FP8 step of each value, plus the binary32
+    # rounding of the quotient (it may land exactly on an FP8 tie and then go
+    # the even way) and of the product decode * s
+    v = synth.bf16_bits_to_f32(x).astype(np.float64)
+    s = np.repeat(sf.astype(np.float64), 128, axis=1)
+    q = np.abs(v / s)
+    e = np.maximum(np.floor(np.log2(np.maximum(q, 1e-300))), EMIN[fmt])
+    bound = 0.5 * np.exp2(e - MBITS[fmt]) * s + q * s * 2.0 ** -23 + np.abs(v) * 2.0 ** -23
+    assert np.all(np.abs(y - v) <= bound + 1e-30)
+
+
+def test_cast_back_hand_values_and_granularities():
+    codes = np.zeros((256, 256), np.uint8)
+    codes[0, 0], codes[200, 130] = 0x7E, 0x01          # 448, 2^-9 (E4M3)
+    sf_tok = np.ones((256, 2), np.float32)
+    sf_tok[200, 1] = 2.0
+    y = oracle.cast_back(codes, sf_tok, 1, 128, "e4m3")
+    assert y[0, 0] == 448.0 and y[200, 130] == 2.0 ** -8 and np.count_nonzero(y) == 2
+    sf_blk = np.array([[0.5, 1.0], [1.0, 4.0]], np.float32)    # 128 x 128 blocks
+    y = oracle.cast_back(codes, sf_blk, 128, 128, "e4m3")
+    assert y[0, 0] == 224.0 and y[200, 130] == 2.0 ** -7
+    sf_ch = np.ones((2, 256), np.float32)
+    sf_ch[1, 130] = 8.0                                        # 128 x 1 groups
+    y = oracle.cast_back(codes, sf_ch, 128, 1, "e4m3")
+    assert y[200, 130] == 2.0 ** -6
