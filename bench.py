@@ -46,12 +46,22 @@ KERNEL_OF = {
     "swiglu_moe": "swiglu_cast",
     "swiglu_t": "swiglu_cast_t",
     "swiglu_bwd": "swiglu_backward_cast",
+    "per_channel": "per_channel_cast",
+    "per_channel_t": "per_channel_cast_t",
+    "per_block": "per_block_cast",
+    "cast_back": "cast_back",
 }
+# bench workload -> seeded input set, where the names differ
+SYNTH_OF = {"per_channel_t": "per_channel"}
 KERNEL_SOURCES = {
     "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_backward_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_channel_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_channel_cast_t": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_block_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "cast_back": ["cast_back.cu", "tkq_device.cuh"],
 }
 
 
@@ -60,6 +70,13 @@ def algorithmic_bytes(workload: str, T: int, C: int, weighted: bool) -> int:
     kern = KERNEL_OF[workload]
     if kern == "per_token_cast":
         return T * C * 2 + T * C + T * (C // 128) * 4
+    if kern in ("per_channel_cast", "per_channel_cast_t"):
+        return T * C * 2 + T * C + (T // 128) * C * 4
+    if kern == "per_block_cast":
+        return T * C * 2 + T * C + -(-T // 128) * (C // 128) * 4
+    if kern == "cast_back":
+        # read codes and per-token scales, write bf16
+        return T * C + T * (C // 128) * 4 + T * C * 2
     H = C // 2
     if kern == "swiglu_backward_cast":
         # read gate|up and dy, write codes and scales of [dg | du]
@@ -183,76 +200,114 @@ def dist_env():
     return ws, rank, local
 
 
+def _to_torch(a: np.ndarray):
+    """Host array -> CPU tensor over the same memory (uint16 = bf16 bits)."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
 class Problem:
-    """Device buffers + one launch closure for a named workload."""
+    """Device buffers, one raw C-ABI launch closure and the same operation
+    through the public tensor API (for the end-to-end measurement) for a named
+    workload."""
 
     def __init__(self, workload: str, fmt: str, dev, seed: int = 0, sf_flags: int = 0):
         import torch
         import fp8_activation_quantization_gb300 as tkq
         from fp8_activation_quantization_gb300 import synth
         self.workload = workload
-        self.kern = KERNEL_OF[workload]
+        self.kern = kern = KERNEL_OF[workload]
         self.fmt = fmt
         self.sf_flags = sf_flags
-        d = synth.workload(workload, seed=seed)
-        self.x_host = d["x"]
-        self.w_host = d.get("w")
-        self.T, self.C = self.x_host.shape
-        self.weighted = self.w_host is not None
-        self.bytes = algorithmic_bytes(workload, self.T, self.C, self.weighted)
+        self.host = synth.workload(SYNTH_OF.get(workload, workload), seed=seed)
+        lead = self.host["x"] if "x" in self.host else self.host["codes"]
+        self.T, self.C = T, C = lead.shape
+        self.weighted = "w" in self.host
+        self.bytes = algorithmic_bytes(workload, T, C, self.weighted)
         self.dev = dev
-        self.x = torch.from_numpy(self.x_host.view(np.int16)).to(dev).view(torch.bfloat16)
-        self.w = None if self.w_host is None else torch.from_numpy(self.w_host).to(dev)
-        self.dy_host = d.get("dy")
-        self.dy = None if self.dy_host is None else \
-            torch.from_numpy(self.dy_host.view(np.int16)).to(dev).view(torch.bfloat16)
-        T, C = self.T, self.C
+        self.inp = {k: _to_torch(v).to(dev) for k, v in self.host.items()}
         fcode = 0 if fmt == "e4m3" else 1
+        fp8 = _fp8(fmt)
         P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
-        if self.kern == "swiglu_backward_cast":
+        x, w, dy = self.inp.get("x"), self.inp.get("w"), self.inp.get("dy")
+        u8, f32 = torch.uint8, torch.float32
+        E = lambda shape, dt=u8: torch.empty(shape, dtype=dt, device=dev)
+        opt = dict(round_sf=bool(sf_flags & 1), use_packed_ue8m0=bool(sf_flags & 2),
+                   use_tma_aligned_col_major_sf=bool(sf_flags & 4))
+        if kern == "per_token_cast":
+            self.outputs = [E((T, C)), E((T, C // 128), f32)]
+            fn, args = tkq.tkq_per_token_cast, [P(x), P(self.outputs[0]), None, T, C, 128, fcode]
+            sf_pos = 2
+            self.api = lambda i, od: tkq.per_token_cast(i["x"], fmt, out=od[0].view(fp8),
+                                                        out_sf=od[1], **opt)
+        elif kern == "swiglu_cast":
             H = C // 2
-            self.out = torch.empty((T, 2 * H), dtype=torch.uint8, device=dev)
-            self.sf = torch.empty((T, 2 * H // 128), dtype=torch.float32, device=dev)
-            self.outputs = [self.out, self.sf]
-            args = (P(self.x), P(self.dy), P(self.w), P(self.out), P(self.sf), T, H, 128, fcode)
-            fn = tkq.tkq_swiglu_backward_cast
-        elif self.kern == "per_token_cast":
-            self.out = torch.empty((T, C), dtype=torch.uint8, device=dev)
-            self.sf = torch.empty((T, C // 128), dtype=torch.float32, device=dev)
-            args = (P(self.x), P(self.out), P(self.sf), T, C, 128, fcode)
-            fn = tkq.tkq_per_token_cast
-            self.outputs = [self.out, self.sf]
+            self.outputs = [E((T, H)), E((T, H // 128), f32)]
+            fn, args = tkq.tkq_swiglu_cast, [P(x), P(w), P(self.outputs[0]), None, T, H, 128,
+                                             fcode]
+            sf_pos = 3
+            self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
+                i["x"], fmt, topk_weights=i.get("w"), out=od[0].view(fp8), out_sf=od[1], **opt)
+        elif kern == "swiglu_backward_cast":
+            H = C // 2
+            self.outputs = [E((T, 2 * H)), E((T, 2 * H // 128), f32)]
+            fn, args = tkq.tkq_swiglu_backward_cast, [P(x), P(dy), P(w), P(self.outputs[0]),
+                                                      None, T, H, 128, fcode]
+            sf_pos = 4
+            self.api = lambda i, od: tkq.swiglu_backward_and_per_token_cast(
+                i["x"], i["dy"], fmt, topk_weights=i.get("w"), out=od[0].view(fp8),
+                out_sf=od[1], **opt)
+        elif kern == "swiglu_cast_t":
+            H = C // 2
+            self.outputs = [E((T, H)), E((T, H // 128), f32), E((H, T)), E((H, T // 128), f32)]
+            o = self.outputs
+            fn, args = tkq.tkq_swiglu_cast_t, [P(x), P(w), P(o[0]), P(o[1]), P(o[2]), P(o[3]),
+                                               T, H, 128, fcode]
+            sf_pos = None
+            self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
+                i["x"], fmt, topk_weights=i.get("w"), with_transpose=True,
+                out=od[0].view(fp8), out_sf=od[1], out_t=od[2].view(fp8), out_sf_t=od[3])
+        elif kern in ("per_channel_cast", "per_channel_cast_t"):
+            tr = kern.endswith("_t")
+            self.outputs = [E((C, T) if tr else (T, C)),
+                            E((C, T // 128) if tr else (T // 128, C), f32)]
+            fn, args = tkq.tkq_per_channel_cast, [P(x), P(self.outputs[0]), P(self.outputs[1]),
+                                                  T, C, 128, fcode, int(tr)]
+            sf_pos = None
+            self.api = lambda i, od: tkq.per_channel_cast(i["x"], fmt, transpose=tr,
+                                                          out=od[0].view(fp8), out_sf=od[1])
+        elif kern == "per_block_cast":
+            self.outputs = [E((T, C)), E((-(-T // 128), C // 128), f32)]
+            fn, args = tkq.tkq_per_block_cast, [P(x), P(self.outputs[0]), P(self.outputs[1]),
+                                                T, C, 128, fcode]
+            sf_pos = None
+            self.api = lambda i, od: tkq.per_block_cast(i["x"], fmt, out=od[0].view(fp8),
+                                                        out_sf=od[1])
+        elif kern == "cast_back":
+            self.outputs = [E((T, C), torch.bfloat16)]
+            fn, args = tkq.tkq_cast_back, [P(self.inp["codes"]), P(self.inp["sf"]),
+                                           P(self.outputs[0]), T, C, 1, 128, fcode, tkq.OUT_BF16]
+            sf_pos = None
+            self.api = lambda i, od: (tkq.cast_back(i["codes"], i["sf"], fmt=fmt,
+                                                    group_size=(1, 128),
+                                                    out_dtype=torch.bfloat16, out=od[0]),)
         else:
-            H = C // 2
-            self.out = torch.empty((T, H), dtype=torch.uint8, device=dev)
-            self.sf = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
-            self.outputs = [self.out, self.sf]
-            if self.kern == "swiglu_cast":
-                args = (P(self.x), P(self.w), P(self.out), P(self.sf), T, H, 128, fcode)
-                fn = tkq.tkq_swiglu_cast
-            else:
-                self.out_t = torch.empty((H, T), dtype=torch.uint8, device=dev)
-                self.sf_t = torch.empty((H, T // 128), dtype=torch.float32, device=dev)
-                self.outputs += [self.out_t, self.sf_t]
-                args = (P(self.x), P(self.w), P(self.out), P(self.sf), P(self.out_t),
-                        P(self.sf_t), T, H, 128, fcode)
-                fn = tkq.tkq_swiglu_cast_t
-        if sf_flags:
-            # the same kernel with a scale-factor layout: swap in the _ex call
-            if self.kern == "swiglu_cast_t":
-                raise ValueError("scale-layout options apply to the row casts only")
-            G = self.sf.numel() // T
-            self.sf = torch.empty(tkq.tkq_sf_bytes(T, G, sf_flags), dtype=torch.uint8, device=dev)
-            self.outputs[1] = self.sf
-            a = list(args)
-            sf_pos = {"per_token_cast": 2, "swiglu_cast": 3, "swiglu_backward_cast": 4}[self.kern]
-            a[sf_pos] = P(self.sf)
-            a.append(sf_flags)
-            fn = {"per_token_cast": tkq.tkq_per_token_cast_ex,
-                  "swiglu_cast": tkq.tkq_swiglu_cast_ex,
-                  "swiglu_backward_cast": tkq.tkq_swiglu_backward_cast_ex}[self.kern]
-            args = tuple(a)
-        self._fn, self._args = fn, args
+            raise KeyError(kern)
+        if sf_pos is not None:
+            if sf_flags:
+                # the same kernel with a scale-factor layout: the _ex call
+                G = self.outputs[1].numel() // T
+                self.outputs[1] = E((tkq.tkq_sf_bytes(T, G, sf_flags),))
+                args.append(sf_flags)
+                fn = {"per_token_cast": tkq.tkq_per_token_cast_ex,
+                      "swiglu_cast": tkq.tkq_swiglu_cast_ex,
+                      "swiglu_backward_cast": tkq.tkq_swiglu_backward_cast_ex}[kern]
+            args[sf_pos] = P(self.outputs[1])
+        elif sf_flags:
+            raise ValueError("scale-layout options apply to the row casts only")
+        self._fn, self._args = fn, tuple(args)
 
     def launch(self, stream):
         st = self._fn(*self._args, ctypes.c_void_p(stream.cuda_stream))
@@ -324,62 +379,39 @@ SMALL_BYTES = 512e6  # below this the working set could stay in L2 between steps
 
 def e2e_steps(prob: Problem, steps: int, stream):
     """Metric through the public tensor API with host buffers.  Every step
-    copies its input from pinned host memory to the device, runs the op and
+    copies its inputs from pinned host memory to the device, runs the op and
     copies every output back to pinned host memory.  Copy-in, compute and
     copy-out run on three streams over two device buffer sets, so step i+1's
     copy-in overlaps step i's compute and copy-out (as a user streaming batches
     would run it); the timed region spans the first copy-in to the last
     copy-out."""
     import torch
-    import fp8_activation_quantization_gb300 as tkq
     dev = prob.dev
-    x_pin = torch.from_numpy(prob.x_host.view(np.int16)).pin_memory()
-    w_pin = None if prob.w_host is None else torch.from_numpy(prob.w_host).pin_memory()
+    pin = {k: _to_torch(v).pin_memory() for k, v in prob.host.items()}
     outs_pin = [[torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in prob.outputs]
                 for _ in range(2)]
-    x_dev = [torch.empty_like(prob.x.view(torch.int16)) for _ in range(2)]
-    w_dev = [None if w_pin is None else torch.empty_like(prob.w) for _ in range(2)]
+    inp_dev = [{k: torch.empty_like(v, device=dev) for k, v in pin.items()} for _ in range(2)]
     outs_dev = [[torch.empty_like(o) for o in prob.outputs] for _ in range(2)]
-    dy_pin = None if prob.dy_host is None else torch.from_numpy(prob.dy_host.view(np.int16)).pin_memory()
-    dy_dev = [None if dy_pin is None else torch.empty_like(dy_pin, device=dev) for _ in range(2)]
-    h2d = x_pin.numel() * 2 + (0 if w_pin is None else w_pin.numel() * 4) + \
-        (0 if dy_pin is None else dy_pin.numel() * 2)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
     d2h = sum(o.numel() * o.element_size() for o in prob.outputs)
     s_in, s_out, s_cmp = torch.cuda.Stream(dev), torch.cuda.Stream(dev), stream
     in_done = [torch.cuda.Event() for _ in range(2)]
     cmp_done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
-    fmt = prob.fmt
 
     def step(i):
         b = i % 2
         if i >= 2:
-            s_in.wait_event(cmp_done[b])      # step i-2 finished reading x_dev[b]
+            s_in.wait_event(cmp_done[b])      # step i-2 finished reading the inputs of set b
         with torch.cuda.stream(s_in):
-            x_dev[b].copy_(x_pin, non_blocking=True)
-            if w_pin is not None:
-                w_dev[b].copy_(w_pin, non_blocking=True)
-            if dy_pin is not None:
-                dy_dev[b].copy_(dy_pin, non_blocking=True)
+            for k, v in pin.items():
+                inp_dev[b][k].copy_(v, non_blocking=True)
             in_done[b].record(s_in)
         s_cmp.wait_event(in_done[b])
         if i >= 2:
             s_cmp.wait_event(out_done[b])     # step i-2's outputs have left the device
         with torch.cuda.stream(s_cmp):
-            xb = x_dev[b].view(torch.bfloat16)
-            od = outs_dev[b]
-            if prob.kern == "per_token_cast":
-                res = tkq.per_token_cast(xb, fmt, out=od[0].view(_fp8(fmt)), out_sf=od[1])
-            elif prob.kern == "swiglu_backward_cast":
-                res = tkq.swiglu_backward_and_per_token_cast(
-                    xb, dy_dev[b].view(torch.bfloat16), fmt, topk_weights=w_dev[b],
-                    out=od[0].view(_fp8(fmt)), out_sf=od[1])
-            else:
-                res = tkq.swiglu_forward_and_per_token_cast(
-                    xb, fmt, topk_weights=w_dev[b], with_transpose=prob.kern == "swiglu_cast_t",
-                    out=od[0].view(_fp8(fmt)), out_sf=od[1],
-                    out_t=None if len(od) < 3 else od[2].view(_fp8(fmt)),
-                    out_sf_t=None if len(od) < 4 else od[3])
+            res = prob.api(inp_dev[b], outs_dev[b])
             cmp_done[b].record(s_cmp)
         s_out.wait_event(cmp_done[b])
         with torch.cuda.stream(s_out):
@@ -409,8 +441,16 @@ def _fp8(fmt):
 def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
     """The oracle for one kernel on the first `rows` rows of a workload dict."""
     import oracle
+    if kern == "cast_back":
+        import torch
+        y = oracle.cast_back(d["codes"][:rows], d["sf"][:rows], 1, 128, fmt, threads=threads)
+        return torch.from_numpy(y).to(torch.bfloat16)
     x = d["x"][:rows]
     w = None if d.get("w") is None else d["w"][:rows]
+    if kern in ("per_channel_cast", "per_channel_cast_t"):
+        return oracle.per_channel_cast(x, fmt, transpose=kern.endswith("_t"), threads=threads)
+    if kern == "per_block_cast":
+        return oracle.per_block_cast(x, fmt, threads=threads)
     if kern == "per_token_cast":
         return oracle.per_token_cast(x, fmt, threads=threads)
     if kern == "swiglu_cast":
@@ -420,16 +460,20 @@ def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
     return oracle.swiglu_cast_t(x, w, fmt, threads=threads)
 
 
+def _lead(d: dict) -> np.ndarray:
+    """The array whose rows are the workload's tokens."""
+    return d["x"] if "x" in d else d["codes"]
+
+
 def cpu_baseline_single_thread(workload: str, fmt: str, rows: int = 32768):
     """The oracle, as it stands, on one host core over the first `rows` rows."""
     from fp8_activation_quantization_gb300 import synth
-    d = synth.workload(workload, rows=rows)
-    x, w = d["x"], d.get("w")
-    T, C = x.shape
+    d = synth.workload(SYNTH_OF.get(workload, workload), rows=rows)
+    T, C = _lead(d).shape
     t0 = time.perf_counter()
     run_oracle(KERNEL_OF[workload], d, T, fmt)
     dt = time.perf_counter() - t0
-    b = algorithmic_bytes(workload, T, C, w is not None)
+    b = algorithmic_bytes(workload, T, C, "w" in d)
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {T} rows of the {workload} workload ({b / 1e6:.0f} MB of "
                       f"algorithmic bytes), single-threaded C oracle, {dt:.1f} s",
@@ -504,7 +548,7 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic (seeded bf16 N(0,1) gate|up, generated on the host)",
+        "data": "synthetic (seeded, generated on the host; see config.workload)",
         "config": {
             "workload": _workload_desc(args.workload),
             "T": prob.T, "cols": prob.C, "fmt": args.fmt, "group": 128,
@@ -552,7 +596,9 @@ def other_workloads(dev, stream, peak, args):
                              ("plain_outlier", "e5m2", 0), ("plain_outlier", "e4m3", 6),
                              ("swiglu", "e4m3", 0), ("swiglu_moe", "e4m3", 0),
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
-                             ("swiglu_bwd", "e4m3", 0)]:
+                             ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
+                             ("per_channel_t", "e4m3", 0), ("per_block", "e4m3", 0),
+                             ("cast_back", "e4m3", 0)]:
         prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
@@ -568,7 +614,9 @@ def other_workloads(dev, stream, peak, args):
 
 def _workload_desc(name):
     from fp8_activation_quantization_gb300 import synth
-    return synth.WORKLOADS[name][2]
+    d = synth.WORKLOADS[SYNTH_OF.get(name, name)][2]
+    return d.replace("per_channel_cast (+transpose)", "per_channel_cast + transpose") \
+        if name == "per_channel_t" else d
 
 
 # ---------------------------------------------------------------------------
@@ -583,12 +631,13 @@ def run_reference(args):
     from fp8_activation_quantization_gb300 import synth
     oracle.build()
     cores = max(1, os.cpu_count() or 1)
-    T_full, C, _ = synth.WORKLOADS[args.workload]
+    syn = SYNTH_OF.get(args.workload, args.workload)
+    T_full, C, _ = synth.WORKLOADS[syn]
     kern = KERNEL_OF[args.workload]
     # calibrate: one 128-row block per core
     rows = 128 * cores
-    d = synth.workload(args.workload, rows=min(T_full, 8192))
-    x_all, w_all = d["x"], d.get("w")
+    d = synth.workload(syn, rows=min(T_full, 8192))
+    x_all, w_all = _lead(d), d.get("w")
 
     def step(r):
         run_oracle(kern, d, r, args.fmt, threads=cores)
@@ -614,7 +663,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded bf16 N(0,1) gate|up, generated on the host)",
+        "data": "synthetic (seeded, generated on the host; see config.workload)",
         "config": {"workload": _workload_desc(args.workload), "T": T_full, "cols": C,
                    "fmt": args.fmt, "group": 128},
         "rows_per_s": round(r * args.steps / dt, 1),

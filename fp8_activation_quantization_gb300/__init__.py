@@ -23,6 +23,8 @@ __all__ = [
     "tkq_swiglu_cast_t", "tkq_swiglu_backward_cast", "tkq_status_string", "per_token_cast",
     "swiglu_forward_and_per_token_cast", "swiglu_backward_and_per_token_cast",
     "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
+    "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
+    "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16",
 ]
 
 FMT_E4M3 = 0
@@ -83,6 +85,12 @@ def load_library():
         lib.tkq_read_device_status.restype = i
         lib.tkq_selftest_wait_timeout.argtypes = [i64, p]
         lib.tkq_selftest_wait_timeout.restype = i
+        lib.tkq_per_channel_cast.argtypes = [p, p, p, i64, i64, i, i, i, p]
+        lib.tkq_per_channel_cast.restype = i
+        lib.tkq_per_block_cast.argtypes = [p, p, p, i64, i64, i, i, p]
+        lib.tkq_per_block_cast.restype = i
+        lib.tkq_cast_back.argtypes = [p, p, p, i64, i64, i, i, i, i, p]
+        lib.tkq_cast_back.restype = i
         _lib = lib
         return lib
 
@@ -128,6 +136,26 @@ def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M
 def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
                              stream=None) -> int:
     return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
+
+
+def tkq_per_channel_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, transpose=0,
+                         stream=None) -> int:
+    return load_library().tkq_per_channel_cast(x, out, sf, T, C, group, fmt, int(transpose),
+                                               stream)
+
+
+def tkq_per_block_cast(x, out, sf, T, C, block=GROUP, fmt=FMT_E4M3, stream=None) -> int:
+    return load_library().tkq_per_block_cast(x, out, sf, T, C, block, fmt, stream)
+
+
+OUT_F32 = 0
+OUT_BF16 = 1
+
+
+def tkq_cast_back(codes, sf, out, T, C, group_rows=1, group_cols=GROUP, fmt=FMT_E4M3,
+                  out_dtype=OUT_F32, stream=None) -> int:
+    return load_library().tkq_cast_back(codes, sf, out, T, C, group_rows, group_cols, fmt,
+                                        out_dtype, stream)
 
 
 SF_ROUND_POW2 = 1
@@ -312,3 +340,85 @@ def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int 
     if st:
         raise TkqError(st, "tkq_swiglu_backward_cast")
     return out, out_sf
+
+
+def per_channel_cast(x, fmt="e4m3", num_per_channels: int = GROUP, transpose: bool = False,
+                     out=None, out_sf=None):
+    """bf16 [T, C] -> codes and scales of groups of 128 tokens per channel:
+    (codes [T, C], scales [T/128, C]), or with ``transpose`` the column-major
+    copy (codes [C, T], scales [C, T/128]).  T must be a multiple of 128."""
+    import torch
+    _check_input(x)
+    f = _fmt_code(fmt)
+    T, C = x.shape
+    g = max(num_per_channels, 1)
+    if out is None:
+        out = torch.empty((C, T) if transpose else (T, C), dtype=_fp8_dtype(f), device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty((C, T // g) if transpose else (T // g, C), dtype=torch.float32,
+                             device=x.device)
+    with torch.cuda.device(x.device):
+        st = tkq_per_channel_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
+                                  int(transpose), _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_per_channel_cast")
+    return out, out_sf
+
+
+def per_block_cast(x, fmt="e4m3", block_size: int = GROUP, out=None, out_sf=None):
+    """bf16 [T, C] -> (codes [T, C], scales [ceil(T/128), C/128]), one scale per
+    128 x 128 block."""
+    import torch
+    _check_input(x)
+    f = _fmt_code(fmt)
+    T, C = x.shape
+    b = max(block_size, 1)
+    if out is None:
+        out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
+    if out_sf is None:
+        out_sf = torch.empty(((T + b - 1) // b, C // b), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = tkq_per_block_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, block_size, f,
+                                _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_per_block_cast")
+    return out, out_sf
+
+
+def cast_back(x, sf, fmt=None, group_size=(1, GROUP), out_dtype=None, out=None):
+    """FP8 codes [T, C] and fp32 scales -> decode(code) * scale as fp32 (default)
+    or bf16.  ``group_size`` = (rows, cols) of one scale group: (1, 128)
+    per-token, (128, 1) per-channel, (128, 128) per-block.  ``fmt`` defaults to
+    the codes' dtype (float8_e4m3fn or float8_e5m2; uint8 codes need fmt)."""
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 2 or not x.is_contiguous():
+        raise TypeError("x must be a contiguous 2-D CUDA tensor of FP8 codes")
+    if x.element_size() != 1:
+        raise TypeError("x must hold one-byte FP8 codes")
+    if fmt is None:
+        if x.dtype == torch.float8_e4m3fn:
+            fmt = "e4m3"
+        elif x.dtype == torch.float8_e5m2:
+            fmt = "e5m2"
+        else:
+            raise ValueError("fmt is required for codes that are not an FP8 dtype")
+    f = _fmt_code(fmt)
+    if (not isinstance(sf, torch.Tensor) or sf.dtype != torch.float32 or not sf.is_contiguous()
+            or sf.device != x.device):
+        raise TypeError("sf must be a contiguous fp32 tensor on the codes' device")
+    gr, gc = group_size
+    T, C = x.shape
+    if (-(-T // max(gr, 1)), C // max(gc, 1)) != tuple(sf.shape[-2:]) or sf.dim() != 2:
+        raise ValueError(f"sf must have shape [ceil(T/{gr}), C/{gc}]")
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty((T, C), dtype=out_dtype, device=x.device)
+    code = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    with torch.cuda.device(x.device):
+        st = tkq_cast_back(_ptr(x), _ptr(sf), _ptr(out), T, C, gr, gc, f, code,
+                           _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_cast_back")
+    return out

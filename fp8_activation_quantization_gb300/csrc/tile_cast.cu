@@ -1,0 +1,264 @@
+// tile_cast.cu -- FP8 casts whose groups span 128 tokens ("TileKernels 与
+// DeepGEMM 的分界线" (chatdocs.ruinique.com) §2 operator table):
+//   * per_channel_cast: groups of 128 consecutive tokens of one channel,
+//     codes in place ([T, C]) or as the transposed copy ([C, T]);
+//   * per_block_cast: one scale per 128 x 128 block.
+// Scale s = fl32(max(amax, 1e-4) / fmt_max) ("DeepSeek开源TileKernels：用Python
+// 写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.1, §3.2); codes are those of
+// the exact binary32 quotient fl(x / s), so results are bit-exact.
+//
+// GB300 design: the persistent tile pipeline of the transposed SwiGLU cast
+// (swiglu_cast_t.cu) with a single bf16 operand: one CTA per SM, a producer
+// warp streaming 128 x 128 TMA boxes (32 KB) into a 4-stage ring, 16 consumer
+// warps each holding an 8-token x 4-channel block (warp w: tokens 8w..8w+7,
+// lane l: channels 4l..4l+3).
+//   * per-block: thread absmax -> warp butterfly (5 xor shuffles) -> one value
+//     per warp in a double-buffered 16-entry table -> one named barrier ->
+//     every thread reduces the table and forms the block scale itself.
+//   * per-channel: per-thread column maxima over 8 tokens -> 16 x 128 table
+//     -> 128 threads form the column scales.  In-place codes leave as 4-byte
+//     stores (a warp writes one 128-byte run per row); transposed codes go
+//     through the XOR-swizzled [channel][token] byte tile of the SwiGLU kernel
+//     and leave as 16-byte stores.
+// Ragged T (per-block only): rows past T are zero-filled by TMA (zeros do not
+// change an absmax) and never stored.  Every mbarrier wait is bounded.
+#include <cuda.h>
+
+#include "tkq_async.cuh"
+#include "tkq_device.cuh"
+#include "tkq_internal.h"
+
+namespace tkq {
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;
+constexpr int kStages = 4;
+constexpr int kTileBytes = 128 * 128 * 2;
+constexpr int kBarConsumers = 1;
+
+enum Mode { kChannel, kChannelT, kBlock };
+
+struct alignas(1024) TileSmem {
+    uint8_t stage[kStages][kTileBytes];
+    uint2 codes[128][16];                 // transposed codes, swizzled
+    float colmax[kConsumerWarps][128];
+    float cs[128];
+    float cinv[128];
+    float bmax[2][kConsumerWarps];        // per-block: warp maxima, by tile parity
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int abort;
+};
+
+template <int FMT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    tile_cast_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ out,
+                     float* __restrict__ sf, int64_t T, int C,
+                     unsigned int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    TileSmem& sm = *reinterpret_cast<TileSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t CB = static_cast<uint32_t>(C) >> 7;
+    const uint32_t TB = static_cast<uint32_t>((T + 127) >> 7);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kConsumerWarps);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            uint32_t issued = 0;
+            RingPos<kStages> pos;
+            for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), ++issued) {
+                if (!mbar_wait_bounded(&sm.empty[pos.stage], pos.phase ^ 1u, &sm.abort, status)) {
+                    *static_cast<volatile int*>(&sm.abort) = 1;
+                    break;
+                }
+                uint64_t* full = &sm.full[pos.stage];
+                mbar_arrive_expect_tx(full, kTileBytes);
+                tma_load_2d(sm.stage[pos.stage], &tmap, static_cast<int>(tw.col * 128),
+                            static_cast<int>(tw.row * 128), full);
+                pos.advance();
+            }
+            const uint32_t first = issued > kStages ? issued - kStages : 0;
+            for (uint32_t k = first; k < issued; ++k)
+                mbar_wait_bounded(&sm.full[k % kStages], (k / kStages) & 1u, nullptr, status);
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int ct = threadIdx.x;
+    RingPos<kStages> pos;
+    uint32_t parity = 0;
+    for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), pos.advance()) {
+        const int s = static_cast<int>(pos.stage);
+        const uint32_t tb = tw.row;
+        const int cb = static_cast<int>(tw.col);
+        const int64_t t0 = static_cast<int64_t>(tb) * 128;
+        const int c0 = cb * 128;
+        const int64_t row0 = t0 + warp * 8;
+
+        const bool ok = mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status);
+        float v[8][4];
+        {
+            const uint8_t* base = sm.stage[s] + warp * 8 * 256 + lane * 8;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                uint2 q = make_uint2(0, 0);
+                if (ok) q = *reinterpret_cast<const uint2*>(base + r * 256);
+                unpack4(q, v[r]);
+            }
+        }
+
+        if constexpr (MODE == kBlock) {
+            float m = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[r][0]), fabsf(v[r][1])),
+                                   fmaxf(fabsf(v[r][2]), fabsf(v[r][3]))));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if (lane == 0) sm.bmax[parity][warp] = m;
+            if (named_bar_or(kBarConsumers, kConsumers, !ok)) {
+                if (ct == 0) *static_cast<volatile int*>(&sm.abort) = 1;
+                break;
+            }
+            float b = sm.bmax[parity][0];
+#pragma unroll
+            for (int q = 1; q < kConsumerWarps; ++q) b = fmaxf(b, sm.bmax[parity][q]);
+            float sc, inv;
+            group_scale<FMT>(b, sc, inv);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                if (row0 + r < T)
+                    st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * C + c0) + lane,
+                                  quantize4<FMT>(v[r], sc, inv));
+            }
+            if (ct == 0) st_stream(sf + static_cast<int64_t>(tb) * CB + cb, sc);
+            parity ^= 1u;
+        } else {
+            // column maxima over this thread's 8 tokens -> shared table
+            float4 cm;
+            float* c = &cm.x;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float m = fabsf(v[0][k]);
+#pragma unroll
+                for (int r = 1; r < 8; ++r) m = fmaxf(m, fabsf(v[r][k]));
+                c[k] = m;
+            }
+            *reinterpret_cast<float4*>(&sm.colmax[warp][lane * 4]) = cm;
+            if (named_bar_or(kBarConsumers, kConsumers, !ok)) {
+                if (ct == 0) *static_cast<volatile int*>(&sm.abort) = 1;
+                break;
+            }
+            if (ct < 128) {
+                float m = sm.colmax[0][ct];
+#pragma unroll
+                for (int q = 1; q < kConsumerWarps; ++q) m = fmaxf(m, sm.colmax[q][ct]);
+                float s_c, inv_c;
+                group_scale<FMT>(m, s_c, inv_c);
+                sm.cs[ct] = s_c;
+                sm.cinv[ct] = inv_c;
+                if constexpr (MODE == kChannel)
+                    st_stream(sf + static_cast<int64_t>(tb) * C + c0 + ct, s_c);
+                else
+                    st_stream(sf + static_cast<int64_t>(c0 + ct) * TB + tb, s_c);
+            }
+            named_bar_sync(kBarConsumers, kConsumers);
+            const float4 cs4 = *reinterpret_cast<const float4*>(&sm.cs[lane * 4]);
+            const float4 ci4 = *reinterpret_cast<const float4*>(&sm.cinv[lane * 4]);
+            const float csv[4] = {cs4.x, cs4.y, cs4.z, cs4.w};
+            const float civ[4] = {ci4.x, ci4.y, ci4.z, ci4.w};
+            if constexpr (MODE == kChannel) {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const uint32_t code = pack4<FMT>(
+                        quotient(v[r][0], csv[0], civ[0]), quotient(v[r][1], csv[1], civ[1]),
+                        quotient(v[r][2], csv[2], civ[2]), quotient(v[r][3], csv[3], civ[3]));
+                    st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * C + c0) + lane,
+                                  code);
+                }
+            } else {
+                const int unit = warp ^ (lane & 15);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float col[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) col[r] = v[r][k];
+                    sm.codes[lane * 4 + k][unit] = quantize8<FMT>(col, csv[k], civ[k]);
+                }
+            }
+        }
+        // Release the stage once the values read from it are consumed (the
+        // stores above depend on all of them), behind an async-proxy fence:
+        // see the stage-release note of the row kernel.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+
+        if constexpr (MODE == kChannelT) {
+            named_bar_sync(kBarConsumers, kConsumers);  // code tile complete
+            uint4* out_t = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                const int c = p * 64 + (ct >> 3);
+                const int ch = ct & 7;
+                const int sw = (c >> 2) & 15;
+                uint4 q = *reinterpret_cast<const uint4*>(&sm.codes[c][2 * (ch ^ (sw >> 1))]);
+                if (sw & 1) q = make_uint4(q.z, q.w, q.x, q.y);
+                st_stream(out_t + ((static_cast<int64_t>(c0 + c) * T + t0) >> 4) + ch, q);
+            }
+        }
+    }
+}
+
+template <int FMT, int MODE>
+cudaError_t launch(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                   cudaStream_t stream) {
+    CUtensorMap map;
+    if (!encode_bf16_2d(&map, x, C, T, 128, 128)) return cudaErrorInvalidValue;
+    auto* k = &tile_cast_kernel<FMT, MODE>;
+    const size_t smem = sizeof(TileSmem) + 1024;
+    const int64_t n_tiles = ((T + 127) / 128) * (C / 128);
+    const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
+    k<<<grid, kThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
+                                        static_cast<int>(C), device_status_word());
+    return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_fmt(int fmt, const void* x, void* out, float* sf, int64_t T, int64_t C,
+                       cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    return fmt == kFmtE4M3 ? launch<kFmtE4M3, MODE>(x, out, sf, T, C, stream)
+                           : launch<kFmtE5M2, MODE>(x, out, sf, T, C, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                    int fmt, bool transpose, cudaStream_t stream) {
+    return transpose ? launch_fmt<kChannelT>(fmt, x, out, sf, T, C, stream)
+                     : launch_fmt<kChannel>(fmt, x, out, sf, T, C, stream);
+}
+
+cudaError_t launch_per_block_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                  int fmt, cudaStream_t stream) {
+    return launch_fmt<kBlock>(fmt, x, out, sf, T, C, stream);
+}
+
+}  // namespace tkq

@@ -313,6 +313,63 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
                                                    static_cast<cudaStream_t>(stream)));
 }
 
+tkq_status tkq_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                int group, int fmt, int transpose, tkq_stream_t stream) {
+    tkq_status st = check_common(T, C, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (T % group) return TKQ_ERR_SHAPE;
+    if (T == 0) return TKQ_OK;
+    if (!x || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
+               rs = tkq::span(sf, (T / group) * C * 4);
+    if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    return launch_status(tkq::launch_per_channel_cast(x, out, sf, T, C, fmt, transpose != 0,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_per_block_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                              int block, int fmt, tkq_stream_t stream) {
+    tkq_status st = check_common(T, C, block, fmt);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(sf, 4))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
+               rs = tkq::span(sf, (T + block - 1) / block * (C / block) * 4);
+    if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    return launch_status(
+        tkq::launch_per_block_cast(x, out, sf, T, C, fmt, static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t T, int64_t C,
+                         int group_rows, int group_cols, int fmt, int out_dtype,
+                         tkq_stream_t stream) {
+    if (T < 0 || C <= 0 || C % 128 || T > INT32_MAX || C > (int64_t{1} << 30))
+        return TKQ_ERR_SHAPE;
+    const bool per_token = group_rows == 1 && group_cols == 128;
+    const bool per_channel = group_rows == 128 && group_cols == 1;
+    const bool per_block = group_rows == 128 && group_cols == 128;
+    if (!per_token && !per_channel && !per_block) return TKQ_ERR_GROUP;
+    if (fmt != TKQ_FMT_E4M3 && fmt != TKQ_FMT_E5M2) return TKQ_ERR_FMT;
+    if (out_dtype != TKQ_OUT_F32 && out_dtype != TKQ_OUT_BF16) return TKQ_ERR_FMT;
+    if (T == 0) return TKQ_OK;
+    if (!codes || !sf || !out) return TKQ_ERR_NULL;
+    if (!tkq::aligned(codes, 16) || !tkq::aligned(out, 16) ||
+        !tkq::aligned(sf, group_cols == 1 ? 16 : 4))
+        return TKQ_ERR_ALIGN;
+    const int64_t out_bytes = T * C * (out_dtype == TKQ_OUT_F32 ? 4 : 2);
+    const int64_t sf_bytes = (T + group_rows - 1) / group_rows * (C / group_cols) * 4;
+    const auto ro = tkq::span(out, out_bytes);
+    if (tkq::overlap(ro, tkq::span(codes, T * C)) || tkq::overlap(ro, tkq::span(sf, sf_bytes)))
+        return TKQ_ERR_ALIAS;
+    return launch_status(tkq::launch_cast_back(codes, sf, out, T, C, group_rows, group_cols, fmt,
+                                               out_dtype == TKQ_OUT_BF16,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
     if (!flags) return TKQ_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;

@@ -239,20 +239,4 @@ __device__ __forceinline__ uint2 quantize8_mul(const float* v, float inv) {
     return make_uint2(quantize4_mul<FMT>(v, inv), quantize4_mul<FMT>(v + 4, inv));
 }
 
-// ---------------------------------------------------------------------------
-// Unsigned 32-bit division by a run-time invariant divisor with a multiply and
-// shifts (Granlund & Montgomery, "Division by invariant integers using
-// multiplication", PLDI 1994, the round-up method).  The host computes
-// (m, sh1, sh2) once per launch.
-// ---------------------------------------------------------------------------
-
-struct FastDiv {
-    uint32_t d, m, sh1, sh2;
-};
-
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
-    const uint32_t t1 = __umulhi(f.m, n);
-    return (t1 + ((n - t1) >> f.sh1)) >> f.sh2;
-}
-
 }  // namespace tkq

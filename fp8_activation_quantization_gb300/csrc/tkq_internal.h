@@ -43,4 +43,18 @@ cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
                                  cudaStream_t stream);
 
+// Per-channel cast (128-token groups; T % 128 == 0): codes [T, C] with sf
+// [T/128, C], or codes [C, T] with sf [C, T/128] when transpose.
+cudaError_t launch_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                    int fmt, bool transpose, cudaStream_t stream);
+
+// Per-block cast (128 x 128 blocks, ragged T): codes [T, C], sf [ceil(T/128), C/128].
+cudaError_t launch_per_block_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                  int fmt, cudaStream_t stream);
+
+// Cast back: out (fp32, or bf16 when out_bf16) = decode(code) * scale, with
+// scales of gr x gc groups (1x128, 128x1 or 128x128).
+cudaError_t launch_cast_back(const void* codes, const float* sf, void* out, int64_t T, int64_t C,
+                             int gr, int gc, int fmt, bool out_bf16, cudaStream_t stream);
+
 }  // namespace tkq

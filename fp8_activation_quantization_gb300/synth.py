@@ -23,6 +23,13 @@ Workloads (all seeded, no dataset involved):
 * ``swiglu_t``      bf16 [131072, 4096] N(0, 1), for the cast + transposed cast.
 * ``swiglu_bwd``    bf16 [65536, 4096] N(0, 1) gate|up, an upstream gradient dy
   bf16 [65536, 2048] N(0, 1) and the routing weights of ``swiglu_moe``.
+* ``per_channel``   bf16 [16384, 7168] N(0, 1) with every 64th channel (from
+  channel 0) multiplied by 20: a few outlier channels, the case a per-channel
+  scale serves.
+* ``per_block``     bf16 [16320, 7168] drawn like ``plain_outlier`` (without the
+  zero rows); 16320 tokens leave a last block row of 64 tokens.
+* ``cast_back``     uint8 [16384, 7168] codes, uniform over all 256 byte values,
+  and fp32 per-token scales [16384, 56] log-uniform in [2^-22, 2^4].
 """
 from __future__ import annotations
 
@@ -47,6 +54,13 @@ WORKLOADS = {
     "swiglu_bwd": (65536, 4096, "swiglu backward x routing weight + per-token E4M3 cast of "
                                 "[dgate | dup], bf16 [65536, 4096] ~ N(0,1) and dy bf16 "
                                 "[65536, 2048] ~ N(0,1), 8192 tokens x top-8, H=2048"),
+    "per_channel": (16384, 7168, "per_channel_cast (+transpose) E4M3, x bf16 [16384, 7168] "
+                                 "~ N(0,1), every 64th channel x20"),
+    "per_block": (16320, 7168, "per_block_cast E4M3, x bf16 [16320, 7168] ~ N(0,1), 0.1% "
+                               "outliers x100, last block row 64 tokens"),
+    "cast_back": (16384, 7168, "cast_back E4M3 -> bf16 with per-token scales, codes uint8 "
+                               "[16384, 7168] uniform bytes, scales fp32 [16384, 56] "
+                               "log-uniform in [2^-22, 2^4]"),
 }
 
 _WORKLOAD_IDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
@@ -152,6 +166,37 @@ def swiglu_bf16(seed: int, stream: int, T: int, H: int, gate_std: float = 1.0,
     return out
 
 
+def channel_outlier_bf16(seed: int, stream: int, T: int, C: int, every: int = 64,
+                         factor: float = 20.0) -> np.ndarray:
+    """N(0,1) with every ``every``-th channel (from channel 0) multiplied by ``factor``."""
+    out = np.empty((int(T), int(C)), np.uint16)
+
+    def fill(i, a, b):
+        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
+        v[:, ::every] *= np.float32(factor)
+        _to_bf16_into(v, out[a:b])
+
+    _chunked(int(T), fill)
+    return out
+
+
+def random_bytes(seed: int, stream: int, T: int, C: int) -> np.ndarray:
+    """uint8 [T, C], every byte value equally likely."""
+    out = np.empty((int(T), int(C)), np.uint8)
+
+    def fill(i, a, b):
+        out[a:b] = rng_for(seed, stream, i).integers(0, 256, (CHUNK_ROWS, C), np.uint8)[:b - a]
+
+    _chunked(int(T), fill)
+    return out
+
+
+def log_uniform_f32(seed: int, stream: int, shape, lo_exp: float, hi_exp: float) -> np.ndarray:
+    """fp32 values 2^u with u ~ Uniform(lo_exp, hi_exp)."""
+    u = rng_for(seed, stream, 1 << 21).uniform(lo_exp, hi_exp, size=shape)
+    return np.ascontiguousarray(np.exp2(u).astype(np.float32))
+
+
 def routing_weights(seed: int, stream: int, tokens: int, topk: int = 8) -> np.ndarray:
     """fp32 [tokens * topk]: Uniform(0.01, 1) normalised over each token's rows."""
     raw = rng_for(seed, stream, 1 << 20).uniform(0.01, 1.0, size=(int(tokens), int(topk)))
@@ -186,4 +231,11 @@ def workload(name: str, seed: int = 0, rows: int | None = None) -> dict:
         w = routing_weights(seed, sid, -(-T // topk), topk)[:T]
         return {"x": swiglu_bf16(seed, sid, T, C // 2),
                 "dy": normal_bf16(seed, sid + 100, T, C // 2), "w": np.ascontiguousarray(w)}
+    if name == "per_channel":
+        return {"x": channel_outlier_bf16(seed, sid, T, C)}
+    if name == "per_block":
+        return {"x": outlier_bf16(seed, sid, T, C, zero_row_every=0)}
+    if name == "cast_back":
+        return {"codes": random_bytes(seed, sid, T, C),
+                "sf": log_uniform_f32(seed, sid, (T, C // 128), -22.0, 4.0)}
     raise KeyError(name)

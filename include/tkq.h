@@ -207,6 +207,53 @@ tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* 
                                     float* sf, int64_t T, int64_t H, int group, int fmt,
                                     tkq_stream_t stream);
 
+/*
+ * Per-channel cast ([P1] §2 operator table, per_channel_cast (+transpose)):
+ * groups of 128 consecutive tokens of one channel, with the scale and code
+ * rules of the common definitions (exact quotient, bit-exact).
+ *   x   : bf16 [T, C], row-major
+ *   transpose == 0:  out FP8 codes [T, C] (in place of x's layout),
+ *                    sf fp32 [T/128, C]; sf[b, c] scales x[128b : 128b+128, c]
+ *   transpose != 0:  out FP8 codes [C, T] (the column-major copy, row c holds
+ *                    channel c), sf fp32 [C, T/128]
+ * T >= 0, T % 128 == 0; C > 0, C % 128 == 0.  Alignment: x, out 16 bytes,
+ * sf 4 bytes.
+ */
+tkq_status tkq_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                                int group, int fmt, int transpose, tkq_stream_t stream);
+
+/*
+ * Per-block cast ([P1] §2 operator table, per_block_cast): one scale per
+ * block of 128 tokens x 128 channels; the last block row may be short (its
+ * amax covers the rows that exist).
+ *   x   : bf16 [T, C], row-major
+ *   out : FP8 codes [T, C]
+ *   sf  : fp32 [ceil(T/128), C/128]; sf[b, j] scales x[128b:128b+128, 128j:128j+128]
+ * T >= 0; C > 0, C % 128 == 0.  Alignment: x, out 16 bytes, sf 4 bytes.
+ */
+tkq_status tkq_per_block_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                              int block, int fmt, tkq_stream_t stream);
+
+/*
+ * Cast back ([P1] §2 operator table, cast_back): dequantization
+ *   out[t, c] = fl32(decode(codes[t, c]) * sf[t / group_rows, c / group_cols])
+ * where decode is the exact value of the FP8 code (NaN codes give NaN).
+ *   codes : FP8 codes [T, C], row-major
+ *   sf    : fp32 [ceil(T/group_rows), C/group_cols], row-major
+ *   out   : fp32 [T, C] (out_dtype TKQ_OUT_F32) or bf16 [T, C]
+ *           (TKQ_OUT_BF16: the fp32 result rounded to nearest even)
+ * (group_rows, group_cols) is (1, 128) for per-token scales, (128, 1) for
+ * per-channel scales and (128, 128) for per-block scales; anything else is
+ * TKQ_ERR_GROUP.  T >= 0; C > 0, C % 128 == 0.  Alignment: codes, out 16
+ * bytes; sf 16 bytes when group_cols == 1, else 4.  out_dtype other than the
+ * two below is TKQ_ERR_FMT.
+ */
+#define TKQ_OUT_F32 0
+#define TKQ_OUT_BF16 1
+tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t T, int64_t C,
+                         int group_rows, int group_cols, int fmt, int out_dtype,
+                         tkq_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);
 

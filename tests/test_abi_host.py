@@ -149,3 +149,50 @@ def test_swiglu_cast_t_output_alias(lib):
     # out_t overlapping out
     assert lib.tkq_swiglu_cast_t(p(), None, p(1 << 24), p(2 << 24), p((1 << 24) + 256),
                                  p(4 << 24), 128, 256, 128, 0, None) == 7
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((None, p(1 << 20), p(2 << 20), 256, 256, 128, 0, 0), 1),         # NULL input
+    ((p(), p(1 << 20), p(2 << 20), 200, 256, 128, 0, 0), 2),          # T % 128
+    ((p(), p(1 << 20), p(2 << 20), 256, 200, 128, 0, 1), 2),          # C % 128
+    ((p(), p(1 << 20), p(2 << 20), 256, 256, 32, 0, 0), 3),           # group
+    ((p(), p(1 << 20), p(2 << 20), 256, 256, 128, 5, 0), 4),          # fmt
+    ((p(), p((1 << 20) + 8), p(2 << 20), 256, 256, 128, 0, 1), 5),    # out misaligned
+    ((p(), p(1 << 20), p((2 << 20) + 1), 256, 256, 128, 0, 0), 5),    # sf misaligned
+    ((p(), p(1 << 16), p(2 << 20), 256, 256, 128, 0, 0), 7),          # out overlaps x
+    ((p(), p(1 << 20), p((1 << 20) + 4096), 256, 256, 128, 0, 1), 7), # sf overlaps out
+    ((None, None, None, 0, 256, 128, 0, 1), 0),                       # empty batch
+])
+def test_per_channel_cast_validation(lib, args, expected):
+    assert lib.tkq_per_channel_cast(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((p(), None, p(2 << 20), 300, 256, 128, 0), 1),                   # NULL out
+    ((p(), p(1 << 20), p(2 << 20), 300, 200, 128, 0), 2),             # C % 128
+    ((p(), p(1 << 20), p(2 << 20), 300, 256, 256, 0), 3),             # block
+    ((p(), p(1 << 20), p(2 << 20), 300, 256, 128, -1), 4),            # fmt
+    ((p(4), p(1 << 20), p(2 << 20), 300, 256, 128, 0), 5),            # x misaligned
+    ((p(), p(1 << 20), p((1 << 20) + 65536), 300, 256, 128, 0), 7),   # sf overlaps out
+    ((None, None, None, 0, 256, 128, 0), 0),                          # empty batch
+])
+def test_per_block_cast_validation(lib, args, expected):
+    assert lib.tkq_per_block_cast(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((None, p(1 << 20), p(2 << 20), 4, 256, 1, 128, 0, 0), 1),        # NULL codes
+    ((p(), p(1 << 20), p(2 << 20), 4, 200, 1, 128, 0, 0), 2),         # C % 128
+    ((p(), p(1 << 20), p(2 << 20), -2, 256, 1, 128, 0, 0), 2),        # T < 0
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 1, 1, 0, 0), 3),           # 1 x 1 groups
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 64, 0, 0), 3),        # 128 x 64 groups
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 1, 128, 3, 0), 4),         # fmt
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 1, 128, 0, 2), 4),         # out dtype
+    ((p(), p((1 << 20) + 4), p(2 << 20), 4, 256, 128, 1, 0, 0), 5),   # per-channel sf / 16
+    ((p(), p(1 << 20), p((2 << 20) + 8), 4, 256, 1, 128, 0, 1), 5),   # out misaligned
+    ((p(), p(1 << 20), p(512), 4, 256, 1, 128, 0, 0), 7),             # out overlaps codes
+    ((p(), p(1 << 20), p((1 << 20) - 1024), 4, 256, 1, 128, 0, 1), 7),  # out overlaps sf
+    ((None, None, None, 0, 256, 128, 128, 1, 1), 0),                  # empty batch
+])
+def test_cast_back_validation(lib, args, expected):
+    assert lib.tkq_cast_back(*args, None) == expected
