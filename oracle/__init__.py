@@ -132,7 +132,11 @@ def _configure(lib):
     lib.ora_cast_back.restype = ctypes.c_int
     lib.ora_swiglu_backward_values.argtypes = [p, p, p, i64, i64, p]
     lib.ora_swiglu_backward_cast.argtypes = [p, p, p, i64, i64, i64, i, p, p]
-    for f in ("ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
+    lib.ora_swiglu_values_clamp.argtypes = [p, p, i64, i64, p, p, p]
+    lib.ora_swiglu_cast_clamp.argtypes = [p, p, i64, i64, i64, i, p, p, p, p]
+    lib.ora_swiglu_cast_t_clamp.argtypes = [p, p, i64, i64, i64, i, p, p, p, p, p, p]
+    for f in ("ora_swiglu_values_clamp", "ora_swiglu_cast_clamp", "ora_swiglu_cast_t_clamp",
+              "ora_per_token_cast", "ora_cast_rows_f32", "ora_cast_cols_f32",
               "ora_swiglu_values", "ora_swiglu_cast", "ora_swiglu_cast_t",
               "ora_swiglu_backward_values", "ora_swiglu_backward_cast"):
         getattr(lib, f).restype = ctypes.c_int
@@ -256,26 +260,54 @@ def cast_cols_f32(y: np.ndarray, fmt="e4m3", group: int = 128):
     return out_t, sf_t
 
 
-def swiglu_values(x_bits: np.ndarray, w: np.ndarray | None = None, threads: int = 1):
-    """x_bits: uint16 [T, 2H] (gate | up) -> fp32 y [T, H]."""
+class _Clamp:
+    """The clamp arguments of the oracle's SwiGLU calls: a pointer to the fp32
+    clamp value (None = no clamp) and a per-call counter of clamped values."""
+
+    def __init__(self, clamp):
+        self.on = clamp is not None
+        self.value = ctypes.c_float(0.0 if clamp is None else float(clamp))
+        self.lock = threading.Lock()
+        self.total = 0
+
+    def ptr(self):
+        return ctypes.byref(self.value) if self.on else None
+
+    def counter(self):
+        return ctypes.c_int64(0)
+
+    def add(self, c):
+        with self.lock:
+            self.total += int(c.value)
+
+
+def swiglu_values(x_bits: np.ndarray, w: np.ndarray | None = None, threads: int = 1,
+                  clamp: float | None = None):
+    """x_bits: uint16 [T, 2H] (gate | up) -> fp32 y [T, H]; with ``clamp``,
+    (y, number of clamped input values)."""
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, H2 = x_bits.shape
     H = H2 // 2
     w = None if w is None else np.ascontiguousarray(w, dtype=np.float32)
     y = np.empty((T, H), np.float32)
+    cl = _Clamp(clamp)
 
     def body(a, b):
-        _check(lib.ora_swiglu_values(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
-                                     b - a, H, _ptr(y[a:b])), "swiglu_values")
+        n = cl.counter()
+        _check(lib.ora_swiglu_values_clamp(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                           b - a, H, cl.ptr(), _ptr(y[a:b]), ctypes.byref(n)),
+               "swiglu_values")
+        cl.add(n)
 
     _row_parallel(T, threads, body)
-    return y
+    return (y, cl.total) if cl.on else y
 
 
 def swiglu_cast(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
-                group: int = 128, threads: int = 1):
-    """-> (codes [T, H], sf [T, H/group])."""
+                group: int = 128, threads: int = 1, clamp: float | None = None):
+    """-> (codes [T, H], sf [T, H/group]); with ``clamp``, also the number of
+    clamped input values."""
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, H2 = x_bits.shape
@@ -284,19 +316,23 @@ def swiglu_cast(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
     out = np.empty((T, H), np.uint8)
     sf = np.empty((T, H // group), np.float32)
     f = _fmt(fmt)
+    cl = _Clamp(clamp)
 
     def body(a, b):
-        _check(lib.ora_swiglu_cast(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
-                                   b - a, H, group, f, _ptr(out[a:b]), _ptr(sf[a:b])),
-               "swiglu_cast")
+        n = cl.counter()
+        _check(lib.ora_swiglu_cast_clamp(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                         b - a, H, group, f, cl.ptr(), _ptr(out[a:b]),
+                                         _ptr(sf[a:b]), ctypes.byref(n)), "swiglu_cast")
+        cl.add(n)
 
     _row_parallel(T, threads, body)
-    return out, sf
+    return (out, sf, cl.total) if cl.on else (out, sf)
 
 
 def swiglu_cast_t(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
-                  group: int = 128, threads: int = 1):
-    """-> (codes [T, H], sf [T, H/group], codes_t [H, T], sf_t [H, T/group])."""
+                  group: int = 128, threads: int = 1, clamp: float | None = None):
+    """-> (codes [T, H], sf [T, H/group], codes_t [H, T], sf_t [H, T/group]);
+    with ``clamp``, also the number of clamped input values."""
     lib = _load()
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, H2 = x_bits.shape
@@ -309,10 +345,7 @@ def swiglu_cast_t(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
     out_t = np.empty((H, T), np.uint8)
     sf_t = np.empty((H, T // group), np.float32)
     f = _fmt(fmt)
-    if threads <= 1:
-        _check(lib.ora_swiglu_cast_t(_ptr(x_bits), _ptr(w), T, H, group, f, _ptr(out),
-                                     _ptr(sf), _ptr(out_t), _ptr(sf_t)), "swiglu_cast_t")
-        return out, sf, out_t, sf_t
+    cl = _Clamp(clamp)
 
     # Row blocks of `group` tokens are independent: run each block as its own
     # oracle problem and scatter its column outputs into the [H, T] arrays.
@@ -320,14 +353,18 @@ def swiglu_cast_t(x_bits: np.ndarray, w: np.ndarray | None = None, fmt="e4m3",
         n = b - a
         o_t = np.empty((H, n), np.uint8)
         s_t = np.empty((H, n // group), np.float32)
-        _check(lib.ora_swiglu_cast_t(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
-                                     n, H, group, f, _ptr(out[a:b]), _ptr(sf[a:b]),
-                                     _ptr(o_t), _ptr(s_t)), "swiglu_cast_t")
+        cnt = cl.counter()
+        _check(lib.ora_swiglu_cast_t_clamp(_ptr(x_bits[a:b]), None if w is None else _ptr(w[a:b]),
+                                           n, H, group, f, cl.ptr(), _ptr(out[a:b]),
+                                           _ptr(sf[a:b]), _ptr(o_t), _ptr(s_t),
+                                           ctypes.byref(cnt)), "swiglu_cast_t")
+        cl.add(cnt)
         out_t[:, a:b] = o_t
         sf_t[:, a // group:b // group] = s_t
 
     _row_parallel(T, threads, body, align=group)
-    return out, sf, out_t, sf_t
+    res = (out, sf, out_t, sf_t)
+    return res + (cl.total,) if cl.on else res
 
 
 def swiglu_backward_values(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray | None = None,

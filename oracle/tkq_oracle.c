@@ -212,14 +212,23 @@ int ora_cast_cols_f32(const float* y, int64_t T, int64_t C, int64_t group,
 
 /* SwiGLU: silu(g) * u with silu(g) = g / (1 + exp(-g)) ([P2] §3.3), then the
  * optional per-row routing weight, each step rounded to binary32. */
-int ora_swiglu_values(const uint16_t* x, const float* w, int64_t T, int64_t H,
-                      float* y) {
-    if (T < 0 || H < 0) return -1;
+int ora_swiglu_values_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                            const float* clamp, float* y, int64_t* n_clamped) {
+    if (T < 0 || H < 0 || (clamp && !(*clamp > 0.0f && *clamp < INFINITY))) return -1;
+    int64_t n = 0;
     for (int64_t t = 0; t < T; ++t) {
         const uint16_t* row = x + t * 2 * H;
         for (int64_t c = 0; c < H; ++c) {
-            const float g = ora_bf16_to_f32(row[c]);
-            const float u = ora_bf16_to_f32(row[H + c]);
+            float g = ora_bf16_to_f32(row[c]);
+            float u = ora_bf16_to_f32(row[H + c]);
+            if (clamp) {
+                /* [P2] §3.3: the gate is clamped from above only, the up
+                 * projection on both sides; every value changed is counted */
+                const float cv = *clamp;
+                if (g > cv) { g = cv; ++n; }
+                if (u > cv) { u = cv; ++n; }
+                if (u < -cv) { u = -cv; ++n; }
+            }
             const float e = (float)exp(-(double)g);
             const float den = 1.0f + e;
             const float silu = g / den;
@@ -228,17 +237,44 @@ int ora_swiglu_values(const uint16_t* x, const float* w, int64_t T, int64_t H,
             y[t * H + c] = val;
         }
     }
+    if (n_clamped) *n_clamped = n;
     return 0;
 }
 
-int ora_swiglu_cast(const uint16_t* x, const float* w, int64_t T, int64_t H,
-                    int64_t group, int fmt, uint8_t* out, float* sf) {
+int ora_swiglu_values(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                      float* y) {
+    return ora_swiglu_values_clamp(x, w, T, H, NULL, y, NULL);
+}
+
+int ora_swiglu_cast_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                          int64_t group, int fmt, const float* clamp, uint8_t* out, float* sf,
+                          int64_t* n_clamped) {
     fp8_desc d;
     if (get_desc(fmt, &d) || T < 0 || H < 0 || group <= 0 || H % group) return -1;
     float* y = (float*)malloc((size_t)(T * H > 0 ? T * H : 1) * sizeof(float));
     if (!y) return -1;
-    int rc = ora_swiglu_values(x, w, T, H, y);
+    int rc = ora_swiglu_values_clamp(x, w, T, H, clamp, y, n_clamped);
     if (!rc) rc = ora_cast_rows_f32(y, T, H, group, fmt, out, sf);
+    free(y);
+    return rc;
+}
+
+int ora_swiglu_cast(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                    int64_t group, int fmt, uint8_t* out, float* sf) {
+    return ora_swiglu_cast_clamp(x, w, T, H, group, fmt, NULL, out, sf, NULL);
+}
+
+int ora_swiglu_cast_t_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                            int64_t group, int fmt, const float* clamp, uint8_t* out,
+                            float* sf, uint8_t* out_t, float* sf_t, int64_t* n_clamped) {
+    fp8_desc d;
+    if (get_desc(fmt, &d) || T < 0 || H < 0 || group <= 0 || H % group || T % group)
+        return -1;
+    float* y = (float*)malloc((size_t)(T * H > 0 ? T * H : 1) * sizeof(float));
+    if (!y) return -1;
+    int rc = ora_swiglu_values_clamp(x, w, T, H, clamp, y, n_clamped);
+    if (!rc) rc = ora_cast_rows_f32(y, T, H, group, fmt, out, sf);
+    if (!rc) rc = ora_cast_cols_f32(y, T, H, group, fmt, out_t, sf_t);
     free(y);
     return rc;
 }
@@ -246,16 +282,7 @@ int ora_swiglu_cast(const uint16_t* x, const float* w, int64_t T, int64_t H,
 int ora_swiglu_cast_t(const uint16_t* x, const float* w, int64_t T, int64_t H,
                       int64_t group, int fmt, uint8_t* out, float* sf,
                       uint8_t* out_t, float* sf_t) {
-    fp8_desc d;
-    if (get_desc(fmt, &d) || T < 0 || H < 0 || group <= 0 || H % group || T % group)
-        return -1;
-    float* y = (float*)malloc((size_t)(T * H > 0 ? T * H : 1) * sizeof(float));
-    if (!y) return -1;
-    int rc = ora_swiglu_values(x, w, T, H, y);
-    if (!rc) rc = ora_cast_rows_f32(y, T, H, group, fmt, out, sf);
-    if (!rc) rc = ora_cast_cols_f32(y, T, H, group, fmt, out_t, sf_t);
-    free(y);
-    return rc;
+    return ora_swiglu_cast_t_clamp(x, w, T, H, group, fmt, NULL, out, sf, out_t, sf_t, NULL);
 }
 
 /* SwiGLU backward: the derivative of y = silu(g) * u [* w] ("TileKernels 与

@@ -93,6 +93,16 @@ int ora_cast_cols_f32(const float* y, int64_t T, int64_t C, int64_t group,
 int ora_swiglu_values(const uint16_t* x, const float* w, int64_t T, int64_t H,
                       float* y);
 
+/* SwiGLU with the optional clamp of [P2] §3.3 (use_clamp,
+ * swiglu_clamp_value): before the SwiGLU, g = min(g, c) and
+ * u = max(min(u, c), -c).  clamp == NULL: no clamp (ora_swiglu_values);
+ * otherwise *clamp = c, finite and > 0.  If n_clamped is not NULL it receives
+ * the number of input values the clamp changed (gates above c, ups above c or
+ * below -c).  The pages say only that clamps are counted with a sum reducer
+ * and an atomic add; counting each changed value is the plain reading. */
+int ora_swiglu_values_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                            const float* clamp, float* y, int64_t* n_clamped);
+
 /* SwiGLU followed by the per-token cast of y: out [T, H], sf [T, H/group]. */
 int ora_swiglu_cast(const uint16_t* x, const float* w, int64_t T, int64_t H,
                     int64_t group, int fmt, uint8_t* out, float* sf);
@@ -103,6 +113,15 @@ int ora_swiglu_cast(const uint16_t* x, const float* w, int64_t T, int64_t H,
 int ora_swiglu_cast_t(const uint16_t* x, const float* w, int64_t T, int64_t H,
                       int64_t group, int fmt, uint8_t* out, float* sf,
                       uint8_t* out_t, float* sf_t);
+
+/* ora_swiglu_cast and ora_swiglu_cast_t with the clamp of
+ * ora_swiglu_values_clamp (same clamp and n_clamped arguments). */
+int ora_swiglu_cast_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                          int64_t group, int fmt, const float* clamp, uint8_t* out, float* sf,
+                          int64_t* n_clamped);
+int ora_swiglu_cast_t_clamp(const uint16_t* x, const float* w, int64_t T, int64_t H,
+                            int64_t group, int fmt, const float* clamp, uint8_t* out,
+                            float* sf, uint8_t* out_t, float* sf_t, int64_t* n_clamped);
 
 /* Scale-factor layout options (TileKernels CastOutputConfig round_sf,
  * use_packed_ue8m0, use_tma_aligned_col_major_sf: [P2] §3.1; their purpose,

@@ -60,6 +60,12 @@ MUTANTS = [
     ("per-block scale from the first row only",
      "const float s = ora_group_scale(group_absmax(v, rows * block, 1), fmt);",
      "const float s = ora_group_scale(group_absmax(v, block, 1), fmt);"),
+    ("clamp: gate clamped from below too", "if (g > cv) { g = cv; ++n; }",
+     "if (g > cv) { g = cv; ++n; }\n                if (g < -cv) { g = -cv; ++n; }"),
+    ("clamp: up clamped from above only", "if (u < -cv) { u = -cv; ++n; }", ""),
+    ("clamp: clamped ups not counted", "if (u > cv) { u = cv; ++n; }", "if (u > cv) { u = cv; }"),
+    ("clamp: values at the bound counted", "if (g > cv) { g = cv; ++n; }",
+     "if (g >= cv) { g = cv; ++n; }"),
     ("cast back ignores the column group", "const float s = sf[(t / gr) * G + c / gc];",
      "const float s = sf[(t / gr) * G];"),
 ]
@@ -75,6 +81,7 @@ CHECKS = [
     (pins.test_swiglu_vs_binary64, {}),
     (pins.test_swiglu_backward_special_cases, {}),
     (pins.test_round_pow2_hand_group, {}),
+    (pins.test_swiglu_clamp_hand_values, {}),
     (pins.test_cast_back_hand_values_and_granularities, {}),
     (pins.test_per_channel_is_per_token_of_transpose, {"fmt": "e4m3"}),
     (pins.test_per_block_is_per_token_of_flattened_blocks, {"fmt": "e4m3", "T": 300}),

@@ -406,6 +406,75 @@ def test_swiglu_cast_t_consistency():
         assert np.array_equal(a, b)
 
 
+# ---------------------------------------------------------------------------
+# SwiGLU clamp ("DeepSeek开源TileKernels..." §3.3: gate clamped from above,
+# up clamped on both sides, clamps counted)
+# ---------------------------------------------------------------------------
+
+def _bf(v):
+    return synth.f32_to_bf16_bits(np.asarray(v, np.float32))
+
+
+def test_swiglu_clamp_hand_values():
+    H, c = 128, 5.0
+    x = np.zeros((4, 2 * H), np.uint16)
+    x[0, 0], x[0, H] = _bf(10.0), _bf(1.0)      # gate above c -> clamped to c
+    x[1, 0], x[1, H] = _bf(-10.0), _bf(1.0)     # gate below -c: gates are not clamped from below
+    x[2, 0], x[2, H] = _bf(1.0), _bf(8.0)       # up above c -> c
+    x[3, 0], x[3, H] = _bf(1.0), _bf(-8.0)      # up below -c -> -c
+    x[3, 1], x[3, H + 1] = _bf(5.0), _bf(-5.0)  # exactly at the bound: unchanged, not counted
+    y, n = oracle.swiglu_values(x, clamp=c)
+    silu = lambda g: g / (1.0 + math.exp(-g))
+    assert abs(y[0, 0] - silu(5.0)) < 1e-5
+    assert abs(y[1, 0] - silu(-10.0)) < 1e-9
+    assert abs(y[2, 0] - 5.0 * silu(1.0)) < 1e-5
+    assert abs(y[3, 0] + 5.0 * silu(1.0)) < 1e-5
+    assert abs(y[3, 1] + 5.0 * silu(5.0)) < 1e-4
+    assert n == 3
+
+
+@pytest.mark.parametrize("c", [0.5, 1.5, 3.0])
+def test_swiglu_clamp_is_the_swiglu_of_the_clipped_input(c):
+    """With a bf16-representable bound, clamping inside the oracle equals the
+    unclamped oracle on an input clipped beforehand with numpy, and the count is
+    the number of entries np.clip changes."""
+    x = _swiglu_input(T=64, H=256, seed=61)
+    H = x.shape[1] // 2
+    f = synth.bf16_bits_to_f32(x)
+    g, u = f[:, :H], f[:, H:]
+    clipped = np.concatenate([np.minimum(g, c), np.clip(u, -c, c)], axis=1)
+    xc = synth.f32_to_bf16_bits(clipped)
+    w = np.random.default_rng(5).uniform(0.01, 1.0, x.shape[0]).astype(np.float32)
+    for ww in (None, w):
+        y, n = oracle.swiglu_values(x, ww, clamp=c)
+        assert np.array_equal(y.view(np.uint32), oracle.swiglu_values(xc, ww).view(np.uint32))
+        assert n == int(np.count_nonzero(g > c) + np.count_nonzero(np.abs(u) > c))
+    assert n > 0
+
+
+def test_swiglu_clamp_beyond_the_data_changes_nothing():
+    x = _swiglu_input(T=32, H=128, seed=62)
+    y0 = oracle.swiglu_values(x)
+    y1, n = oracle.swiglu_values(x, clamp=1e30)
+    assert n == 0 and np.array_equal(y0.view(np.uint32), y1.view(np.uint32))
+    with pytest.raises(ValueError):
+        oracle.swiglu_values(x, clamp=-1.0)
+
+
+def test_swiglu_clamp_casts_compose():
+    """The clamped casts are the casts of the clamped values; the threaded
+    split sums the per-block counts."""
+    x = _swiglu_input(T=256, H=256, seed=63)
+    y, n = oracle.swiglu_values(x, clamp=1.0)
+    out, sf, n1 = oracle.swiglu_cast(x, clamp=1.0)
+    o2, s2 = oracle.cast_rows_f32(y)
+    assert n1 == n and np.array_equal(out, o2) and np.array_equal(sf, s2)
+    res = oracle.swiglu_cast_t(x, clamp=1.0, threads=2)
+    ct, st = oracle.cast_rows_f32(np.ascontiguousarray(y.T))
+    assert np.array_equal(res[0], o2) and np.array_equal(res[2], ct) and np.array_equal(res[3], st)
+    assert res[4] == n
+
+
 def test_invalid_arguments_raise():
     with pytest.raises(ValueError):
         oracle.per_token_cast(np.zeros((2, 100), np.uint16))
