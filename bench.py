@@ -50,9 +50,13 @@ KERNEL_OF = {
     "per_channel_t": "per_channel_cast_t",
     "per_block": "per_block_cast",
     "cast_back": "cast_back",
+    "swiglu_clamp": "swiglu_cast_clamp",
 }
 # bench workload -> seeded input set, where the names differ
-SYNTH_OF = {"per_channel_t": "per_channel"}
+SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu"}
+# SwiGLU clamp bound of the swiglu_clamp workload (gate ~ N(0, 2^2): ~2.3 % of
+# the gates lie above it)
+CLAMP_VALUE = 4.0
 KERNEL_SOURCES = {
     "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
@@ -62,6 +66,7 @@ KERNEL_SOURCES = {
     "per_channel_cast_t": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_block_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "cast_back": ["cast_back.cu", "tkq_device.cuh"],
+    "swiglu_cast_clamp": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
 }
 
 
@@ -250,6 +255,17 @@ class Problem:
             sf_pos = 3
             self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
                 i["x"], fmt, topk_weights=i.get("w"), out=od[0].view(fp8), out_sf=od[1], **opt)
+        elif kern == "swiglu_cast_clamp":
+            H = C // 2
+            self.count = E((1,), torch.int64).zero_()
+            self.outputs = [E((T, H)), E((T, H // 128), f32)]
+            fn, args = tkq.tkq_swiglu_cast_clamp, [P(x), P(w), P(self.outputs[0]), None, T, H,
+                                                   128, fcode, sf_flags, CLAMP_VALUE,
+                                                   P(self.count)]
+            sf_pos = 3
+            self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
+                i["x"], fmt, topk_weights=i.get("w"), out=od[0].view(fp8), out_sf=od[1],
+                use_clamp=True, swiglu_clamp_value=CLAMP_VALUE, clamp_count=self.count, **opt)
         elif kern == "swiglu_backward_cast":
             H = C // 2
             self.outputs = [E((T, 2 * H)), E((T, 2 * H // 128), f32)]
@@ -295,7 +311,12 @@ class Problem:
                                                     out_dtype=torch.bfloat16, out=od[0]),)
         else:
             raise KeyError(kern)
-        if sf_pos is not None:
+        if sf_pos is not None and kern == "swiglu_cast_clamp":
+            if sf_flags:
+                G = self.outputs[1].numel() // T
+                self.outputs[1] = E((tkq.tkq_sf_bytes(T, G, sf_flags),))
+            args[sf_pos] = P(self.outputs[1])
+        elif sf_pos is not None:
             if sf_flags:
                 # the same kernel with a scale-factor layout: the _ex call
                 G = self.outputs[1].numel() // T
@@ -455,6 +476,8 @@ def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
         return oracle.per_token_cast(x, fmt, threads=threads)
     if kern == "swiglu_cast":
         return oracle.swiglu_cast(x, w, fmt, threads=threads)
+    if kern == "swiglu_cast_clamp":
+        return oracle.swiglu_cast(x, w, fmt, threads=threads, clamp=CLAMP_VALUE)
     if kern == "swiglu_backward_cast":
         return oracle.swiglu_backward_cast(x, d["dy"][:rows], w, fmt, threads=threads)
     return oracle.swiglu_cast_t(x, w, fmt, threads=threads)
@@ -598,7 +621,7 @@ def other_workloads(dev, stream, peak, args):
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
                              ("per_channel_t", "e4m3", 0), ("per_block", "e4m3", 0),
-                             ("cast_back", "e4m3", 0)]:
+                             ("cast_back", "e4m3", 0), ("swiglu_clamp", "e4m3", 0)]:
         prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)

@@ -24,7 +24,8 @@ __all__ = [
     "swiglu_forward_and_per_token_cast", "swiglu_backward_and_per_token_cast",
     "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
     "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
-    "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16",
+    "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
+    "tkq_swiglu_cast_t_clamp",
 ]
 
 FMT_E4M3 = 0
@@ -91,6 +92,11 @@ def load_library():
         lib.tkq_per_block_cast.restype = i
         lib.tkq_cast_back.argtypes = [p, p, p, i64, i64, i, i, i, i, p]
         lib.tkq_cast_back.restype = i
+        f32 = ctypes.c_float
+        lib.tkq_swiglu_cast_clamp.argtypes = [p, p, p, p, i64, i64, i, i, u, f32, p, p]
+        lib.tkq_swiglu_cast_clamp.restype = i
+        lib.tkq_swiglu_cast_t_clamp.argtypes = [p, p, p, p, p, p, i64, i64, i, i, f32, p, p]
+        lib.tkq_swiglu_cast_t_clamp.restype = i
         _lib = lib
         return lib
 
@@ -136,6 +142,18 @@ def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M
 def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
                              stream=None) -> int:
     return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
+
+
+def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                          clamp_value=0.0, clamp_count=None, stream=None) -> int:
+    return load_library().tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group, fmt, sf_flags,
+                                                clamp_value, clamp_count, stream)
+
+
+def tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
+                            clamp_value=0.0, clamp_count=None, stream=None) -> int:
+    return load_library().tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group, fmt,
+                                                  clamp_value, clamp_count, stream)
 
 
 def tkq_per_channel_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, transpose=0,
@@ -271,13 +289,29 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
                                       topk_weights=None, with_transpose: bool = False,
                                       out=None, out_sf=None, out_t=None, out_sf_t=None,
                                       round_sf: bool = False, use_packed_ue8m0: bool = False,
-                                      use_tma_aligned_col_major_sf: bool = False):
+                                      use_tma_aligned_col_major_sf: bool = False,
+                                      use_clamp: bool = False, swiglu_clamp_value=None,
+                                      clamp_count=None):
     """bf16 [T, 2H] (gate | up) -> (codes [T, H], scales [T, H/128]) and, with
     ``with_transpose``, also (codes_t [H, T], scales_t [H, T/128]).
     ``topk_weights``: optional fp32 [T] routing weight per row.  The scale-layout
-    options apply to the row scales of the cast without transpose."""
+    options apply to the row scales of the cast without transpose.
+    ``use_clamp``: clamp the gate to <= swiglu_clamp_value and the up projection
+    to [-swiglu_clamp_value, swiglu_clamp_value] before the SwiGLU; the number of
+    changed values is added to ``clamp_count`` (a zeroed int64 CUDA tensor of one
+    element) when given."""
     import torch
     _check_input(x)
+    clamp = None
+    if use_clamp:
+        if swiglu_clamp_value is None:
+            raise ValueError("use_clamp needs swiglu_clamp_value")
+        clamp = float(swiglu_clamp_value)
+        if clamp_count is not None and (clamp_count.dtype != torch.int64 or clamp_count.numel() != 1
+                                        or clamp_count.device != x.device):
+            raise TypeError("clamp_count must be a one-element int64 tensor on x's device")
+    elif clamp_count is not None:
+        raise ValueError("clamp_count needs use_clamp")
     f = _fmt_code(fmt)
     T, H2 = x.shape
     if H2 % 2:
@@ -295,8 +329,13 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
     with torch.cuda.device(x.device):
         stream = _stream_handle(x.device)
         if not with_transpose:
-            st = tkq_swiglu_cast_ex(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), T, H,
-                                    num_per_channels, f, flags, stream)
+            if clamp is None:
+                st = tkq_swiglu_cast_ex(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), T,
+                                        H, num_per_channels, f, flags, stream)
+            else:
+                st = tkq_swiglu_cast_clamp(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
+                                           T, H, num_per_channels, f, flags, clamp,
+                                           _ptr(clamp_count), stream)
             if st:
                 raise TkqError(st, "tkq_swiglu_cast")
             return out, out_sf
@@ -304,8 +343,13 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
             out_t = torch.empty((H, T), dtype=_fp8_dtype(f), device=x.device)
         if out_sf_t is None:
             out_sf_t = torch.empty((H, T // g), dtype=torch.float32, device=x.device)
-        st = tkq_swiglu_cast_t(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf), _ptr(out_t),
-                               _ptr(out_sf_t), T, H, num_per_channels, f, stream)
+        if clamp is None:
+            st = tkq_swiglu_cast_t(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
+                                   _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f, stream)
+        else:
+            st = tkq_swiglu_cast_t_clamp(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
+                                         _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f,
+                                         clamp, _ptr(clamp_count), stream)
         if st:
             raise TkqError(st, "tkq_swiglu_cast_t")
         return out, out_sf, out_t, out_sf_t

@@ -2,7 +2,9 @@
 //   * the plain per_token_cast of a bf16 [T, C] matrix ("DeepSeek开源TileKernels：
 //     用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2);
 //   * swiglu_forward_and_per_token_cast of a bf16 [T, 2H] gate|up matrix,
-//     optionally times a per-row routing weight (same page, §3.3);
+//     optionally times a per-row routing weight and with the optional clamp
+//     (gate <= c, -c <= up <= c) whose changed values are counted (same page,
+//     §3.3);
 //   * swiglu_backward_and_per_token_cast ("TileKernels 与 DeepGEMM 的分界线"
 //     (chatdocs.ruinique.com) §2 and §6 step 13): the gradients [dg | du] of
 //     the same SwiGLU from the upstream gradient dy, cast per token.
@@ -36,12 +38,17 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRows = 32;                 // rows per chunk (4 per consumer warp)
 constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
 
-enum Mode { kPlain, kSwiglu, kSwigluWeighted, kBackward, kBackwardWeighted };
+enum Mode {
+    kPlain, kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kBackward,
+    kBackwardWeighted
+};
 
 template <int MODE>
 struct ModeTraits {
     static constexpr bool kBwd = MODE == kBackward || MODE == kBackwardWeighted;
-    static constexpr bool kWeighted = MODE == kSwigluWeighted || MODE == kBackwardWeighted;
+    static constexpr bool kClamp = MODE == kSwigluClamp || MODE == kSwigluWeightedClamp;
+    static constexpr bool kWeighted =
+        MODE == kSwigluWeighted || MODE == kSwigluWeightedClamp || MODE == kBackwardWeighted;
     static constexpr int kOperands = MODE == kPlain ? 1 : (kBwd ? 3 : 2);  // boxes per chunk
     static constexpr int kStageBytes = kOperands * kBoxBytes;
     static constexpr int kRingBytes = kBwd ? 3 * kStageBytes : 65536;
@@ -141,6 +148,13 @@ __device__ __forceinline__ void load16(const uint8_t* p, float* v) {
     unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
 }
 
+// The SwiGLU clamp of one launch: bound c (> 0) and the counter that the
+// number of changed input values is added to (may be null).
+struct Clamp {
+    float value;
+    unsigned long long* count;
+};
+
 // tmap: x [T, C] (plain) or [T, 2H] (gate | up); tmap_dy: dy [T, H] (backward
 // only).  C_out: channels per output operand (C or H).
 template <int FMT, int MODE, bool SFX>
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     row_cast_kernel(const __grid_constant__ CUtensorMap tmap,
                     const __grid_constant__ CUtensorMap tmap_dy, const float* __restrict__ w,
                     uint2* __restrict__ out, float* __restrict__ sf, SfLayout lay, int64_t T,
-                    int C_out, unsigned int* __restrict__ status) {
+                    int C_out, Clamp clamp, unsigned int* __restrict__ status) {
     using MT = ModeTraits<MODE>;
     extern __shared__ uint8_t smem_raw[];
     RowSmem<MODE>& sm = *reinterpret_cast<RowSmem<MODE>*>(
@@ -207,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // output row pitch (elements) and scales per output row
     const int64_t out_ld = MT::kBwd ? 2 * static_cast<int64_t>(C_out) : C_out;
     const uint32_t sf_ld = MT::kBwd ? 2 * CB : CB;
+    uint64_t n_clamped = 0;
     RingPos<MT::kStages> pos;
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < RB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
@@ -219,8 +234,11 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (live) wt = __ldg(w + row);
         }
 
-        if (!mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status)) {
-            *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
+        // the warp leaves as a whole if any lane's wait gave up, so that no
+        // lane is left behind at a shuffle
+        const bool ok = mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
             break;
         }
         const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
@@ -234,6 +252,17 @@ __global__ void __launch_bounds__(kThreads, 3)
             float g[16], u[16], v[16];
             load16(p, g);
             load16(p + kBoxBytes, u);
+            if constexpr (MT::kClamp) {
+                const float c = clamp.value;
+                uint32_t n = 0;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    n += (g[k] > c) + (u[k] > c) + (u[k] < -c);
+                    g[k] = fminf(g[k], c);
+                    u[k] = fmaxf(fminf(u[k], c), -c);
+                }
+                if (live) n_clamped += n;
+            }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 v[k] = swiglu(g[k], u[k]);
@@ -267,24 +296,32 @@ __global__ void __launch_bounds__(kThreads, 3)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);
     }
+    if constexpr (MT::kClamp) {
+        // one atomic per warp, and none when nothing was clamped
+        unsigned long long t = n_clamped;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0 && t && clamp.count) atomicAdd(clamp.count, t);
+    }
 }
 
 template <int FMT, int MODE, bool SFX>
 cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& map_dy, const float* w,
                         void* out, float* sf, const SfLayout& lay, int64_t T, int64_t C_out,
-                        cudaStream_t stream) {
+                        Clamp clamp, cudaStream_t stream) {
     auto* k = &row_cast_kernel<FMT, MODE, SFX>;
     const size_t smem = sizeof(RowSmem<MODE>) + 1024;
     const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
     k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, lay, T,
-                                        static_cast<int>(C_out), device_status_word());
+                                        static_cast<int>(C_out), clamp, device_status_word());
     return cudaGetLastError();
 }
 
 template <int FMT, int MODE>
 cudaError_t launch(const void* x, const void* dy, const float* w, void* out, void* sf,
-                   int64_t T, int64_t C_out, unsigned sf_flags, cudaStream_t stream) {
+                   int64_t T, int64_t C_out, unsigned sf_flags, Clamp clamp,
+                   cudaStream_t stream) {
     using MT = ModeTraits<MODE>;
     // x as a bf16 [T, cols] matrix: C columns (plain) or 2H (gate | up)
     const int64_t cols = (MT::kOperands == 1 ? 1 : 2) * C_out;
@@ -301,18 +338,20 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, voi
     lay.words = (lay.groups + 3) / 4;
     lay.rows4 = (T + 3) / 4 * 4;
     float* sff = static_cast<float*>(sf);
-    return sf_flags ? launch_mode<FMT, MODE, true>(map, map_dy, w, out, sff, lay, T, C_out, stream)
-                    : launch_mode<FMT, MODE, false>(map, map_dy, w, out, sff, lay, T, C_out, stream);
+    return sf_flags
+               ? launch_mode<FMT, MODE, true>(map, map_dy, w, out, sff, lay, T, C_out, clamp, stream)
+               : launch_mode<FMT, MODE, false>(map, map_dy, w, out, sff, lay, T, C_out, clamp,
+                                               stream);
 }
 
 template <int MODE>
 cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, void* out,
                        void* sf, int64_t T, int64_t C_out, unsigned sf_flags,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, Clamp clamp = Clamp{0.0f, nullptr}) {
     if (T == 0) return cudaSuccess;
     return fmt == kFmtE4M3
-               ? launch<kFmtE4M3, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, stream)
-               : launch<kFmtE5M2, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, stream);
+               ? launch<kFmtE4M3, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, clamp, stream)
+               : launch<kFmtE5M2, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, clamp, stream);
 }
 
 }  // namespace
@@ -323,7 +362,14 @@ cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T,
 }
 
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
-                               int64_t H, int fmt, unsigned sf_flags, cudaStream_t stream) {
+                               int64_t H, int fmt, unsigned sf_flags, const float* clamp,
+                               unsigned long long* clamp_count, cudaStream_t stream) {
+    if (clamp) {
+        const Clamp c{*clamp, clamp_count};
+        return w ? launch_fmt<kSwigluWeightedClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags,
+                                                    stream, c)
+                 : launch_fmt<kSwigluClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream, c);
+    }
     return w ? launch_fmt<kSwigluWeighted>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream)
              : launch_fmt<kSwiglu>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream);
 }

@@ -7,7 +7,9 @@
 // GPU算子逼近硬件性能上限" (itsolotime.com) §3.3) plus a per_channel_cast of the
 // transposed y ("TileKernels 与 DeepGEMM 的分界线" (chatdocs.ruinique.com) §2,
 // "per_channel_cast (+transpose / fused)").  Both outputs are quantized from the
-// same fp32 y.
+// same fp32 y.  With CLAMP the gate is clamped to <= c and the up projection to
+// [-c, c] before the SwiGLU, and the number of changed values is added to a
+// counter (one atomic per warp), as in §3.3 of the second page.
 //
 // GB300 design: one persistent CTA per SM walks 128-token x 128-channel tiles
 // of y.  Warp 16 is the producer: one lane streams the gate and up tiles of the
@@ -63,11 +65,12 @@ struct alignas(1024) SharedStorage {
     int abort;
 };
 
-template <int FMT, bool WEIGHTED>
+template <int FMT, bool WEIGHTED, bool CLAMP>
 __global__ void __launch_bounds__(kThreads, 1)
     swiglu_cast_t_kernel(const __grid_constant__ CUtensorMap tmap, const float* __restrict__ w,
                          uint8_t* __restrict__ out, float* __restrict__ sf,
                          uint4* __restrict__ out_t, float* __restrict__ sf_t, int64_t T, int H,
+                         float clamp, unsigned long long* __restrict__ clamp_count,
                          unsigned int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     SharedStorage& sm = *reinterpret_cast<SharedStorage*>(
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ----------------------------------------------------------- consumers
     const int ct = threadIdx.x;  // 0 .. kConsumers-1
+    uint64_t n_clamped = 0;
     RingPos<kStages> pos;
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
@@ -149,6 +153,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float gv[4], uv[4];
                 unpack4(gq, gv);
                 unpack4(uq, uv);
+                if constexpr (CLAMP) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        n_clamped += (gv[k] > clamp) + (uv[k] > clamp) + (uv[k] < -clamp);
+                        gv[k] = fminf(gv[k], clamp);
+                        uv[k] = fmaxf(fminf(uv[k], clamp), -clamp);
+                    }
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     y[r][k] = swiglu(gv[k], uv[k]);
@@ -277,36 +289,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // codes only after its second, so every read of this tile's shared data
         // is complete before it is overwritten.
     }
+    if constexpr (CLAMP) {
+        // one atomic per warp, and none when nothing was clamped
+        unsigned long long t = n_clamped;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0 && t && clamp_count) atomicAdd(clamp_count, t);
+    }
 }
 
-template <int FMT, bool WEIGHTED>
+template <int FMT, bool WEIGHTED, bool CLAMP>
 cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* out_t,
-                   float* sf_t, int64_t T, int64_t H, cudaStream_t stream) {
+                   float* sf_t, int64_t T, int64_t H, float clamp,
+                   unsigned long long* clamp_count, cudaStream_t stream) {
     // x as a bf16 [T, 2H] matrix (gate | up), read in 128 x 128 boxes
     CUtensorMap map;
     if (!encode_bf16_2d(&map, x, 2 * H, T, 128, 128)) return cudaErrorInvalidValue;
 
-    auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED>;
+    auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED, CLAMP>;
     const size_t smem = sizeof(SharedStorage) + 1024;
     const int64_t n_tiles = (T / 128) * (H / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,
                                         static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H),
-                                        device_status_word());
+                                        clamp, clamp_count, device_status_word());
     return cudaGetLastError();
 }
 
 }  // namespace
 
+namespace {
+template <int FMT, bool CLAMP>
+cudaError_t launch_w(const void* x, const float* w, void* out, float* sf, void* out_t,
+                     float* sf_t, int64_t T, int64_t H, float clamp,
+                     unsigned long long* clamp_count, cudaStream_t stream) {
+    return w ? launch<FMT, true, CLAMP>(x, w, out, sf, out_t, sf_t, T, H, clamp, clamp_count,
+                                        stream)
+             : launch<FMT, false, CLAMP>(x, w, out, sf, out_t, sf_t, T, H, clamp, clamp_count,
+                                         stream);
+}
+}  // namespace
+
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
+                                 const float* clamp, unsigned long long* clamp_count,
                                  cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
+    const float c = clamp ? *clamp : 0.0f;
     if (fmt == kFmtE4M3)
-        return w ? launch<kFmtE4M3, true>(x, w, out, sf, out_t, sf_t, T, H, stream)
-                 : launch<kFmtE4M3, false>(x, w, out, sf, out_t, sf_t, T, H, stream);
-    return w ? launch<kFmtE5M2, true>(x, w, out, sf, out_t, sf_t, T, H, stream)
-             : launch<kFmtE5M2, false>(x, w, out, sf, out_t, sf_t, T, H, stream);
+        return clamp ? launch_w<kFmtE4M3, true>(x, w, out, sf, out_t, sf_t, T, H, c, clamp_count,
+                                                stream)
+                     : launch_w<kFmtE4M3, false>(x, w, out, sf, out_t, sf_t, T, H, c, nullptr,
+                                                 stream);
+    return clamp ? launch_w<kFmtE5M2, true>(x, w, out, sf, out_t, sf_t, T, H, c, clamp_count,
+                                            stream)
+                 : launch_w<kFmtE5M2, false>(x, w, out, sf, out_t, sf_t, T, H, c, nullptr, stream);
 }
 
 }  // namespace tkq

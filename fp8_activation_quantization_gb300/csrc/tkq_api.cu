@@ -2,6 +2,7 @@
 // validation, status codes and dispatch to the kernel launchers.  Nothing here
 // allocates device memory.
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -229,12 +230,26 @@ tkq_status tkq_per_token_cast(const void* x, void* out, float* sf, int64_t T, in
     return tkq_per_token_cast_ex(x, out, sf, T, C, group, fmt, 0u, stream);
 }
 
-tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf, int64_t T,
-                              int64_t H, int group, int fmt, unsigned sf_flags,
-                              tkq_stream_t stream) {
+namespace {
+// The SwiGLU clamp arguments: a finite bound > 0 and, if given, an 8-byte
+// aligned counter that overlaps none of the call's other buffers.
+tkq_status check_clamp(float clamp, const uint64_t* count, const tkq::Range* others, int n) {
+    if (!(clamp > 0.0f && clamp < INFINITY)) return TKQ_ERR_VALUE;
+    if (!count) return TKQ_OK;
+    if (!tkq::aligned(count, 8)) return TKQ_ERR_ALIGN;
+    const auto rc = tkq::span(count, 8);
+    for (int i = 0; i < n; ++i)
+        if (tkq::overlap(rc, others[i])) return TKQ_ERR_ALIAS;
+    return TKQ_OK;
+}
+
+tkq_status swiglu_cast_impl(const void* x, const float* w, void* out, void* sf, int64_t T,
+                            int64_t H, int group, int fmt, unsigned sf_flags, const float* clamp,
+                            uint64_t* clamp_count, tkq_stream_t stream) {
     tkq_status st = check_common(T, H, group, fmt);
     if (st != TKQ_OK) return st;
     if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
+    if (clamp && !(*clamp > 0.0f && *clamp < INFINITY)) return TKQ_ERR_VALUE;
     if (T == 0) return TKQ_OK;
     if (!x || !out || !sf) return TKQ_ERR_NULL;
     if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || (w && !tkq::aligned(w, 4)))
@@ -243,17 +258,34 @@ tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf
     const auto rx = tkq::span(x, T * H * 4), ro = tkq::span(out, T * H),
                rs = tkq::span(sf, tkq_sf_bytes(T, H / group, sf_flags));
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
-    if (w) {
-        const auto rw = tkq::span(w, T * 4);
-        if (tkq::overlap(rw, ro) || tkq::overlap(rw, rs)) return TKQ_ERR_ALIAS;
+    const auto rw = w ? tkq::span(w, T * 4) : tkq::Range{0, 0};
+    if (tkq::overlap(rw, ro) || tkq::overlap(rw, rs)) return TKQ_ERR_ALIAS;
+    if (clamp) {
+        const tkq::Range others[4] = {rx, ro, rs, rw};
+        if ((st = check_clamp(*clamp, clamp_count, others, 4)) != TKQ_OK) return st;
     }
-    return launch_status(tkq::launch_swiglu_cast(x, w, out, sf, T, H, fmt, sf_flags,
-                                                 static_cast<cudaStream_t>(stream)));
+    return launch_status(tkq::launch_swiglu_cast(
+        x, w, out, sf, T, H, fmt, sf_flags, clamp,
+        reinterpret_cast<unsigned long long*>(clamp_count), static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf, int64_t T,
+                              int64_t H, int group, int fmt, unsigned sf_flags,
+                              tkq_stream_t stream) {
+    return swiglu_cast_impl(x, w, out, sf, T, H, group, fmt, sf_flags, nullptr, nullptr, stream);
 }
 
 tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf, int64_t T,
                            int64_t H, int group, int fmt, tkq_stream_t stream) {
-    return tkq_swiglu_cast_ex(x, w, out, sf, T, H, group, fmt, 0u, stream);
+    return swiglu_cast_impl(x, w, out, sf, T, H, group, fmt, 0u, nullptr, nullptr, stream);
+}
+
+tkq_status tkq_swiglu_cast_clamp(const void* x, const float* w, void* out, void* sf, int64_t T,
+                                 int64_t H, int group, int fmt, unsigned sf_flags,
+                                 float clamp_value, uint64_t* clamp_count, tkq_stream_t stream) {
+    return swiglu_cast_impl(x, w, out, sf, T, H, group, fmt, sf_flags, &clamp_value,
+                            clamp_count, stream);
 }
 
 tkq_status tkq_swiglu_backward_cast_ex(const void* x, const void* dy, const float* w, void* out,
@@ -285,12 +317,14 @@ tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* 
     return tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group, fmt, 0u, stream);
 }
 
-tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
-                             float* sf_t, int64_t T, int64_t H, int group, int fmt,
-                             tkq_stream_t stream) {
+namespace {
+tkq_status swiglu_cast_t_impl(const void* x, const float* w, void* out, float* sf, void* out_t,
+                              float* sf_t, int64_t T, int64_t H, int group, int fmt,
+                              const float* clamp, uint64_t* clamp_count, tkq_stream_t stream) {
     tkq_status st = check_common(T, H, group, fmt);
     if (st != TKQ_OK) return st;
     if (T % group) return TKQ_ERR_SHAPE;
+    if (clamp && !(*clamp > 0.0f && *clamp < INFINITY)) return TKQ_ERR_VALUE;
     if (T == 0) return TKQ_OK;
     // TMA box coordinates are 32-bit
     if (H > (int64_t{1} << 30) || T > INT32_MAX) return TKQ_ERR_SHAPE;
@@ -304,13 +338,32 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
     for (int i = 0; i < 5; ++i)
         for (int k = i + 1; k < 5; ++k)
             if (tkq::overlap(r[i], r[k])) return TKQ_ERR_ALIAS;
-    if (w) {
-        const auto rw = tkq::span(w, T * 4);
-        for (int i = 1; i < 5; ++i)
-            if (tkq::overlap(rw, r[i])) return TKQ_ERR_ALIAS;
+    const auto rw = w ? tkq::span(w, T * 4) : tkq::Range{0, 0};
+    for (int i = 1; i < 5; ++i)
+        if (tkq::overlap(rw, r[i])) return TKQ_ERR_ALIAS;
+    if (clamp) {
+        const tkq::Range others[6] = {r[0], r[1], r[2], r[3], r[4], rw};
+        if ((st = check_clamp(*clamp, clamp_count, others, 6)) != TKQ_OK) return st;
     }
-    return launch_status(tkq::launch_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, fmt,
-                                                   static_cast<cudaStream_t>(stream)));
+    return launch_status(tkq::launch_swiglu_cast_t(
+        x, w, out, sf, out_t, sf_t, T, H, fmt, clamp,
+        reinterpret_cast<unsigned long long*>(clamp_count), static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
+                             float* sf_t, int64_t T, int64_t H, int group, int fmt,
+                             tkq_stream_t stream) {
+    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, nullptr, nullptr,
+                              stream);
+}
+
+tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, float* sf,
+                                   void* out_t, float* sf_t, int64_t T, int64_t H, int group,
+                                   int fmt, float clamp_value, uint64_t* clamp_count,
+                                   tkq_stream_t stream) {
+    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, &clamp_value,
+                              clamp_count, stream);
 }
 
 tkq_status tkq_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
@@ -405,6 +458,7 @@ const char* tkq_status_string(int status) {
         case TKQ_ERR_CUDA: return "TKQ_ERR_CUDA: kernel launch failed";
         case TKQ_ERR_ALIAS: return "TKQ_ERR_ALIAS: buffers overlap";
         case TKQ_ERR_FLAGS: return "TKQ_ERR_FLAGS: unknown option flags";
+        case TKQ_ERR_VALUE: return "TKQ_ERR_VALUE: invalid scalar argument";
         default: return "TKQ_ERR_UNKNOWN";
     }
 }

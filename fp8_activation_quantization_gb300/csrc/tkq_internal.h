@@ -32,8 +32,11 @@ int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks
 cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
                                   int fmt, unsigned sf_flags, cudaStream_t stream);
 
+// clamp: null (no clamp) or the SwiGLU clamp bound c > 0; clamp_count (may be
+// null) receives the number of clamped input values by atomic addition.
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
-                               int64_t H, int fmt, unsigned sf_flags, cudaStream_t stream);
+                               int64_t H, int fmt, unsigned sf_flags, const float* clamp,
+                               unsigned long long* clamp_count, cudaStream_t stream);
 
 cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
                                         void* sf, int64_t T, int64_t H, int fmt,
@@ -41,6 +44,7 @@ cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const flo
 
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
+                                 const float* clamp, unsigned long long* clamp_count,
                                  cudaStream_t stream);
 
 // Per-channel cast (128-token groups; T % 128 == 0): codes [T, C] with sf

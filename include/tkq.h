@@ -67,7 +67,8 @@ typedef enum {
     TKQ_ERR_ALIGN = 5,
     TKQ_ERR_CUDA = 6,
     TKQ_ERR_ALIAS = 7,
-    TKQ_ERR_FLAGS = 8
+    TKQ_ERR_FLAGS = 8,
+    TKQ_ERR_VALUE = 9
 } tkq_status;
 
 /* A cudaStream_t passed as an opaque pointer. */
@@ -253,6 +254,27 @@ tkq_status tkq_per_block_cast(const void* x, void* out, float* sf, int64_t T, in
 tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t T, int64_t C,
                          int group_rows, int group_cols, int fmt, int out_dtype,
                          tkq_stream_t stream);
+
+/*
+ * SwiGLU casts with the clamp of [P2] §3.3 (use_clamp, swiglu_clamp_value):
+ * before the SwiGLU, the gate is clamped from above, g = min(g, c), and the up
+ * projection on both sides, u = max(min(u, c), -c).  The number of input
+ * values the clamp changes (gates above c, ups above c or below -c; a value
+ * equal to c is unchanged) is ADDED to *clamp_count: the caller zeroes the
+ * counter, and consecutive calls accumulate (the page counts clamps with a sum
+ * reducer and an atomic add; counting each changed value is this library's
+ * reading).  Otherwise these are tkq_swiglu_cast_ex and tkq_swiglu_cast_t.
+ *   clamp_value : c, finite and > 0, else TKQ_ERR_VALUE
+ *   clamp_count : DEVICE pointer to one uint64 (8-byte aligned, overlapping
+ *                 no other buffer of the call), or NULL for no count.
+ */
+tkq_status tkq_swiglu_cast_clamp(const void* x, const float* w, void* out, void* sf, int64_t T,
+                                 int64_t H, int group, int fmt, unsigned sf_flags,
+                                 float clamp_value, uint64_t* clamp_count, tkq_stream_t stream);
+tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, float* sf,
+                                   void* out_t, float* sf_t, int64_t T, int64_t H, int group,
+                                   int fmt, float clamp_value, uint64_t* clamp_count,
+                                   tkq_stream_t stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);

@@ -196,3 +196,28 @@ def test_per_block_cast_validation(lib, args, expected):
 ])
 def test_cast_back_validation(lib, args, expected):
     assert lib.tkq_cast_back(*args, None) == expected
+
+
+@pytest.mark.parametrize("clamp,count_off,expected", [
+    (0.0, 0, 9),              # bound must be > 0
+    (-1.0, 0, 9),
+    (float("inf"), 0, 9),
+    (float("nan"), 0, 9),
+    (4.0, 4, 5),              # counter not 8-byte aligned
+    (4.0, -(4 << 20) + 64, 7),   # counter inside x
+    (4.0, -(1 << 20) + 64, 7),   # counter inside out
+])
+def test_swiglu_clamp_validation(lib, clamp, count_off, expected):
+    T, H = 256, 256
+    count = p((4 << 20) + count_off)
+    args = (p(), None, p(3 << 20), p(5 << 20), T, H, 128, 0, 0, clamp, count, None)
+    assert lib.tkq_swiglu_cast_clamp(*args) == expected
+    args_t = (p(), None, p(3 << 20), p(5 << 20), p(6 << 20), p(7 << 20), T, H, 128, 0, clamp,
+              count, None)
+    assert lib.tkq_swiglu_cast_t_clamp(*args_t) == expected
+
+
+def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
+    assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 1.0, None, None) == 0
+    assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 0.0, None, None) == 9
+    assert "VALUE" in __import__("fp8_activation_quantization_gb300").tkq_status_string(9)

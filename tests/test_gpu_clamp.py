@@ -1,0 +1,174 @@
+"""Parity of the clamped SwiGLU casts (through the C ABI) with the oracle.
+
+Scales within 1e-6 relative; codes equal except by one FP8 step where the
+oracle's quotient y / s lies at an FP8 rounding tie (clamping makes such ties
+common: see parity.assert_codes_differ_only_at_ties); the clamp count is an
+integer decided by exact comparisons of bf16 inputs with the bound, so it must
+equal the oracle's count exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_activation_quantization_gb300 as tkq
+from fp8_activation_quantization_gb300 import synth
+from tests import parity
+from tests.test_gpu_parity import Guarded, stream_of, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    tkq.load_library()
+    yield
+
+
+def q_rows(x, w, clamp, sf):
+    """The oracle's quotients y / s of the row cast."""
+    y, _ = oracle.swiglu_values(x, w, THREADS, clamp=clamp)
+    return y / np.repeat(sf, 128, axis=1)
+
+
+def q_cols(x, w, clamp, sf_t):
+    """The oracle's quotients y[t, c] / s_t of the transposed cast, as [H, T]."""
+    y, _ = oracle.swiglu_values(x, w, THREADS, clamp=clamp)
+    return y.T / np.repeat(sf_t, 128, axis=1)
+
+
+def run_clamp(x_bits, w, fmt, clamp, dev, transposed=False, count=None, sf_flags=0):
+    """One clamped launch; returns the outputs and the counter's value (the
+    counter starts at `count` if given, else at 0)."""
+    T, H2 = x_bits.shape
+    H = H2 // 2
+    xd = to_dev_bf16(x_bits, dev)
+    wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
+    wp = None if wd is None else ctypes.c_void_p(wd.data_ptr())
+    cnt = torch.full((1,), 0 if count is None else count, dtype=torch.int64, device=dev)
+    out = Guarded(T * H, dev)
+    f = oracle.FMT[fmt]
+    cp = ctypes.c_void_p(cnt.data_ptr())
+    if not transposed:
+        sf = Guarded(tkq.tkq_sf_bytes(T, H // 128, sf_flags), dev)
+        st = tkq.tkq_swiglu_cast_clamp(ctypes.c_void_p(xd.data_ptr()), wp, out.ptr, sf.ptr, T, H,
+                                       128, f, sf_flags, clamp, cp, stream_of(dev))
+        assert st == 0, tkq.tkq_status_string(st)
+        torch.cuda.synchronize()
+        out.check_guards("out")
+        sf.check_guards("sf")
+        return out.data().reshape(T, H), sf.data(), int(cnt.item())
+    sf = Guarded(T * (H // 128) * 4, dev)
+    out_t = Guarded(T * H, dev)
+    sf_t = Guarded(H * (T // 128) * 4, dev)
+    st = tkq.tkq_swiglu_cast_t_clamp(ctypes.c_void_p(xd.data_ptr()), wp, out.ptr, sf.ptr,
+                                     out_t.ptr, sf_t.ptr, T, H, 128, f, clamp, cp, stream_of(dev))
+    assert st == 0, tkq.tkq_status_string(st)
+    torch.cuda.synchronize()
+    for g, n in ((out, "out"), (sf, "sf"), (out_t, "out_t"), (sf_t, "sf_t")):
+        g.check_guards(n)
+    return (out.data().reshape(T, H), sf.data().view(np.float32).reshape(T, H // 128),
+            out_t.data().reshape(H, T), sf_t.data().view(np.float32).reshape(H, T // 128),
+            int(cnt.item()))
+
+
+@pytest.mark.parametrize("clamp", [0.5, 3.0])
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("T,H", [(1, 128), (1031, 384)])
+def test_clamped_swiglu_cast(cuda_device, clamp, weighted, fmt, T, H):
+    x = synth.swiglu_bf16(71, T + H, T, H, gate_std=2.0)
+    w = synth.routing_weights(72, T, -(-T // 8))[:T] if weighted else None
+    codes, sf_raw, n = run_clamp(x, w, fmt, clamp, cuda_device)
+    e_codes, e_sf, e_n = oracle.swiglu_cast(x, w, fmt, threads=THREADS, clamp=clamp)
+    assert n == e_n
+    parity.assert_scales_close("sf", sf_raw.view(np.float32).reshape(T, H // 128), e_sf)
+    parity.assert_codes_differ_only_at_ties("codes", codes, e_codes, q_rows(x, w, clamp, e_sf), fmt)
+
+
+def test_clamped_swiglu_full_workload(cuda_device):
+    d = synth.workload("swiglu")
+    x = d["x"]
+    T, H = x.shape[0], x.shape[1] // 2
+    codes, sf_raw, n = run_clamp(x, None, "e4m3", 4.0, cuda_device)
+    e_codes, e_sf, e_n = oracle.swiglu_cast(x, None, "e4m3", threads=THREADS, clamp=4.0)
+    assert n == e_n and n > 0
+    parity.assert_scales_close("sf", sf_raw.view(np.float32).reshape(T, H // 128), e_sf)
+    parity.assert_codes_differ_only_at_ties("codes", codes, e_codes,
+                                            q_rows(x, None, 4.0, e_sf), "e4m3")
+
+
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("T,H", [(128, 128), (1024, 384)])
+def test_clamped_swiglu_cast_t(cuda_device, weighted, T, H):
+    x = synth.swiglu_bf16(73, T + H, T, H, gate_std=2.0)
+    w = synth.routing_weights(74, T, T // 8) if weighted else None
+    o, s, ot, st, n = run_clamp(x, w, "e4m3", 2.0, cuda_device, transposed=True)
+    eo, es, eot, est, e_n = oracle.swiglu_cast_t(x, w, "e4m3", threads=THREADS, clamp=2.0)
+    assert n == e_n
+    parity.assert_scales_close("sf", s, es)
+    parity.assert_codes_differ_only_at_ties("codes", o, eo, q_rows(x, w, 2.0, es), "e4m3")
+    parity.assert_scales_close("sf_t", st, est)
+    parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, w, 2.0, est), "e4m3")
+    # the row outputs equal the clamped row cast's bit for bit
+    o2, s2, n2 = run_clamp(x, w, "e4m3", 2.0, cuda_device)
+    parity.assert_bit_exact("rows", o, o2)
+    parity.assert_bit_exact("row scales", s, s2.view(np.float32).reshape(s.shape))
+    assert n2 == n
+
+
+def test_clamped_swiglu_cast_t_full_workload(cuda_device):
+    x = synth.workload("swiglu")["x"]
+    o, s, ot, st, n = run_clamp(x, None, "e4m3", 4.0, cuda_device, transposed=True)
+    eo, es, eot, est, e_n = oracle.swiglu_cast_t(x, None, "e4m3", threads=THREADS, clamp=4.0)
+    assert n == e_n and n > 0
+    parity.assert_scales_close("sf_t", st, est)
+    parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, None, 4.0, est), "e4m3")
+
+
+def test_clamp_count_accumulates_and_null_counter_is_allowed(cuda_device):
+    x = synth.swiglu_bf16(75, 76, 512, 256, gate_std=2.0)
+    _, _, n1 = run_clamp(x, None, "e4m3", 1.0, cuda_device)
+    _, _, n2 = run_clamp(x, None, "e4m3", 1.0, cuda_device, count=n1)
+    assert n1 > 0 and n2 == 2 * n1
+    xd = to_dev_bf16(x, cuda_device)
+    q, s = tkq.swiglu_forward_and_per_token_cast(xd, use_clamp=True, swiglu_clamp_value=1.0)
+    c, _, _ = run_clamp(x, None, "e4m3", 1.0, cuda_device)
+    assert np.array_equal(q.view(torch.uint8).cpu().numpy(), c)
+    cnt = torch.zeros(1, dtype=torch.int64, device=cuda_device)
+    tkq.swiglu_forward_and_per_token_cast(xd, use_clamp=True, swiglu_clamp_value=1.0,
+                                          clamp_count=cnt, with_transpose=True)
+    assert int(cnt.item()) == n1
+
+
+def test_clamp_beyond_the_data_is_the_unclamped_cast(cuda_device):
+    x = synth.swiglu_bf16(77, 78, 300, 256)
+    xd = to_dev_bf16(x, cuda_device)
+    q0, s0 = tkq.swiglu_forward_and_per_token_cast(xd)
+    q1, s1, n = run_clamp(x, None, "e4m3", 1e30, cuda_device)
+    assert n == 0
+    assert np.array_equal(q0.view(torch.uint8).cpu().numpy(), q1)
+    assert np.array_equal(s0.cpu().numpy().view(np.uint32).ravel(), s1.view(np.uint32))
+
+
+def test_clamp_with_column_major_scales(cuda_device):
+    """The clamp composes with a scale layout: column-major fp32 scales are the
+    row-major scales of the same clamped launch, transposed (and padded)."""
+    T, H = 301, 384
+    x = synth.swiglu_bf16(79, 80, T, H, gate_std=2.0)
+    c0, s0, n0 = run_clamp(x, None, "e4m3", 2.0, cuda_device)
+    c1, s1, n1 = run_clamp(x, None, "e4m3", 2.0, cuda_device, sf_flags=tkq.SF_COL_MAJOR)
+    T4 = (T + 3) // 4 * 4
+    rm = s0.view(np.float32).reshape(T, H // 128)
+    cm = s1.view(np.float32).reshape(H // 128, T4)
+    assert n0 == n1 and np.array_equal(c0, c1)
+    assert np.array_equal(cm[:, :T], rm.T) and np.all(cm[:, T:] == 0)
