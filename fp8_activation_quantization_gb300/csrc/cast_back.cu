@@ -10,7 +10,8 @@
 //
 // An HBM-bound stream (1 byte in, 4 or 2 bytes out per element): persistent
 // CTAs of 256 threads walk units of rows; one thread turns 16 codes (one
-// 16-byte load) into 16 outputs (64 or 32 bytes of 16-byte stores).
+// 16-byte load) of each of four rows into 16 outputs per row (64 or 32 bytes of
+// 16-byte stores), with the four loads in flight together.
 #include <cuda_runtime.h>
 
 #include "tkq_device.cuh"
@@ -60,87 +61,107 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return r;
 }
 
-// A unit is R rows (R = max(1, 256 / V), V = C / 16 vectors per row).  Thread
-// i serves row i / V of the unit and the vectors i % V, i % V + 256, ... of
-// that row, so a row of any width C keeps the threads busy.
-template <int FMT, int GC, bool BF16>
-__global__ void __launch_bounds__(kThreads)
+// Rows per thread and unit: the loads of kRowsPerThread rows are issued before
+// any of them is used, so each thread keeps 4 x 16 bytes in flight.
+constexpr int kRowsPerThread = 4;
+
+// Work is split into units of R x kRowsPerThread rows (R = max(1, 256 / V),
+// V = C / 16 vectors per row).  Thread i serves vector column i % V (and
+// i % V + 256, ... for wide rows) of rows r, r + R, r + 2R, r + 3R of the unit,
+// r = i / V, so rows of any width keep the threads busy.  GR_SHIFT: log2 of the
+// scale group's rows (0 or 7).
+template <int FMT, int GC, int GR_SHIFT, bool BF16>
+__global__ void __launch_bounds__(kThreads, 3)
     cast_back_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ sf,
-                     void* __restrict__ out, int64_t T, int64_t C, int gr, int rows_per_unit) {
+                     void* __restrict__ out, int64_t T, int64_t C, int R) {
     const int64_t V = C >> 4;
-    const int r_in_unit = static_cast<int>(threadIdx.x / V);  // < rows_per_unit when active
-    const int v0 = static_cast<int>(threadIdx.x - static_cast<int64_t>(r_in_unit) * V);
-    if (r_in_unit >= rows_per_unit) return;
+    const int r_in = static_cast<int>(threadIdx.x / V);  // < R when the thread is used
+    const int v0 = static_cast<int>(threadIdx.x - static_cast<int64_t>(r_in) * V);
+    if (r_in >= R) return;
     const int64_t G = C / GC;  // scales per row of sf
-    const int64_t n_units = (T + rows_per_unit - 1) / rows_per_unit;
+    const int64_t unit_rows = static_cast<int64_t>(R) * kRowsPerThread;
+    const int64_t n_units = (T + unit_rows - 1) / unit_rows;
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const int64_t t = u * rows_per_unit + r_in_unit;
-        if (t >= T) continue;
-        const uint4* src = reinterpret_cast<const uint4*>(codes + t * C);
-        const float* srow = sf + (t / gr) * G;
-#pragma unroll 2
+        const int64_t t0 = u * unit_rows + r_in;
         for (int64_t v = v0; v < V; v += kThreads) {
-            const uint4 q = ld_stream(src + v);
-            const int64_t c = v * 16;
-            float s[16];
-            if constexpr (GC == 1) {
-                const float4* s4 = reinterpret_cast<const float4*>(srow + c);
+            uint4 q[kRowsPerThread];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float4 f = __ldg(s4 + k);
-                    s[4 * k] = f.x; s[4 * k + 1] = f.y; s[4 * k + 2] = f.z; s[4 * k + 3] = f.w;
-                }
-            } else {
-                const float one = __ldg(srow + c / GC);
-#pragma unroll
-                for (int k = 0; k < 16; ++k) s[k] = one;
+            for (int k = 0; k < kRowsPerThread; ++k) {
+                const int64_t t = t0 + static_cast<int64_t>(k) * R;
+                q[k] = t < T ? ld_stream(reinterpret_cast<const uint4*>(codes + t * C) + v)
+                             : make_uint4(0, 0, 0, 0);
             }
-            float y[16];
-            decode16<FMT>(q, y);
+            const int64_t c = v * 16;
 #pragma unroll
-            for (int k = 0; k < 16; ++k) y[k] = __fmul_rn(y[k], s[k]);
-            if constexpr (BF16) {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + t * C + c);
+            for (int k = 0; k < kRowsPerThread; ++k) {
+                const int64_t t = t0 + static_cast<int64_t>(k) * R;
+                if (t >= T) break;
+                const float* srow = sf + (t >> GR_SHIFT) * G;
+                float s[16];
+                if constexpr (GC == 1) {
+                    const float4* s4 = reinterpret_cast<const float4*>(srow + c);
 #pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    st_stream(dst + k, make_uint4(pack_bf16x2(y[8 * k], y[8 * k + 1]),
-                                                  pack_bf16x2(y[8 * k + 2], y[8 * k + 3]),
-                                                  pack_bf16x2(y[8 * k + 4], y[8 * k + 5]),
-                                                  pack_bf16x2(y[8 * k + 6], y[8 * k + 7])));
-            } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(out) + t * C + c);
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = __ldg(s4 + i);
+                        s[4 * i] = f.x; s[4 * i + 1] = f.y; s[4 * i + 2] = f.z; s[4 * i + 3] = f.w;
+                    }
+                } else {
+                    const float one = __ldg(srow + c / GC);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    st_stream(dst + k, make_uint4(__float_as_uint(y[4 * k]),
-                                                  __float_as_uint(y[4 * k + 1]),
-                                                  __float_as_uint(y[4 * k + 2]),
-                                                  __float_as_uint(y[4 * k + 3])));
+                    for (int i = 0; i < 16; ++i) s[i] = one;
+                }
+                float y[16];
+                decode16<FMT>(q[k], y);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], s[i]);
+                if constexpr (BF16) {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + t * C + c);
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        st_stream(dst + i, make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]),
+                                                      pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
+                                                      pack_bf16x2(y[8 * i + 4], y[8 * i + 5]),
+                                                      pack_bf16x2(y[8 * i + 6], y[8 * i + 7])));
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(out) + t * C + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_stream(dst + i, make_uint4(__float_as_uint(y[4 * i]),
+                                                      __float_as_uint(y[4 * i + 1]),
+                                                      __float_as_uint(y[4 * i + 2]),
+                                                      __float_as_uint(y[4 * i + 3])));
+                }
             }
         }
     }
 }
 
-template <int FMT, int GC, bool BF16>
-cudaError_t launch(const void* codes, const float* sf, void* out, int64_t T, int64_t C, int gr,
+template <int FMT, int GC, int GR_SHIFT, bool BF16>
+cudaError_t launch(const void* codes, const float* sf, void* out, int64_t T, int64_t C,
                    cudaStream_t stream) {
-    auto* k = &cast_back_kernel<FMT, GC, BF16>;
+    auto* k = &cast_back_kernel<FMT, GC, GR_SHIFT, BF16>;
     const int64_t V = C / 16;
-    const int rows_per_unit = V >= kThreads ? 1 : static_cast<int>(kThreads / V);
-    const int64_t n_units = (T + rows_per_unit - 1) / rows_per_unit;
+    const int R = V >= kThreads ? 1 : static_cast<int>(kThreads / V);
+    const int64_t unit_rows = static_cast<int64_t>(R) * kRowsPerThread;
+    const int64_t n_units = (T + unit_rows - 1) / unit_rows;
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0, n_units);
-    k<<<grid, kThreads, 0, stream>>>(static_cast<const uint8_t*>(codes), sf, out, T, C, gr,
-                                     rows_per_unit);
+    k<<<grid, kThreads, 0, stream>>>(static_cast<const uint8_t*>(codes), sf, out, T, C, R);
     return cudaGetLastError();
+}
+
+template <int FMT, bool BF16>
+cudaError_t launch_g(const void* codes, const float* sf, void* out, int64_t T, int64_t C, int gr,
+                     int gc, cudaStream_t stream) {
+    if (gc == 1) return launch<FMT, 1, 7, BF16>(codes, sf, out, T, C, stream);  // 128 x 1
+    if (gr == 1) return launch<FMT, 128, 0, BF16>(codes, sf, out, T, C, stream);  // 1 x 128
+    return launch<FMT, 128, 7, BF16>(codes, sf, out, T, C, stream);              // 128 x 128
 }
 
 template <int FMT>
 cudaError_t launch_gc(const void* codes, const float* sf, void* out, int64_t T, int64_t C, int gr,
                       int gc, bool bf16, cudaStream_t stream) {
-    if (gc == 1)
-        return bf16 ? launch<FMT, 1, true>(codes, sf, out, T, C, gr, stream)
-                    : launch<FMT, 1, false>(codes, sf, out, T, C, gr, stream);
-    return bf16 ? launch<FMT, 128, true>(codes, sf, out, T, C, gr, stream)
-                : launch<FMT, 128, false>(codes, sf, out, T, C, gr, stream);
+    return bf16 ? launch_g<FMT, true>(codes, sf, out, T, C, gr, gc, stream)
+                : launch_g<FMT, false>(codes, sf, out, T, C, gr, gc, stream);
 }
 
 }  // namespace

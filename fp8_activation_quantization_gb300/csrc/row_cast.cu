@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 uint32_t n = 0;
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    n += (g[k] > c) + (u[k] > c) + (u[k] < -c);
+                    n += (g[k] > c) + (fabsf(u[k]) > c);
                     g[k] = fminf(g[k], c);
                     u[k] = fmaxf(fminf(u[k], c), -c);
                 }

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (CLAMP) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        n_clamped += (gv[k] > clamp) + (uv[k] > clamp) + (uv[k] < -clamp);
+                        n_clamped += (gv[k] > clamp) + (fabsf(uv[k]) > clamp);
                         gv[k] = fminf(gv[k], clamp);
                         uv[k] = fmaxf(fminf(uv[k], clamp), -clamp);
                     }

@@ -12,14 +12,16 @@
 // warp streaming 128 x 128 TMA boxes (32 KB) into a 4-stage ring, 16 consumer
 // warps each holding an 8-token x 4-channel block (warp w: tokens 8w..8w+7,
 // lane l: channels 4l..4l+3).
-//   * per-block: thread absmax -> warp butterfly (5 xor shuffles) -> one value
-//     per warp in a double-buffered 16-entry table -> one named barrier ->
-//     every thread reduces the table and forms the block scale itself.
+//   * per-block: thread absmax -> warp max (one redux.sync on the bit patterns)
+//     -> one value per warp in a double-buffered 16-entry table -> one named
+//     barrier -> every warp reduces the table (one load, one redux.sync) and
+//     forms the block scale itself.
 //   * per-channel: per-thread column maxima over 8 tokens -> 16 x 128 table
 //     -> 128 threads form the column scales.  In-place codes leave as 4-byte
 //     stores (a warp writes one 128-byte run per row); transposed codes go
 //     through the XOR-swizzled [channel][token] byte tile of the SwiGLU kernel
-//     and leave as 16-byte stores.
+//     and leave as 16-byte stores.  (Double-buffering that tile to save the
+//     third barrier measured slower: the store then lengthens the scale step.)
 // Ragged T (per-block only): rows past T are zero-filled by TMA (zeros do not
 // change an absmax) and never stored.  Every mbarrier wait is bounded.
 #include <cuda.h>
@@ -46,11 +48,28 @@ struct alignas(1024) TileSmem {
     float colmax[kConsumerWarps][128];
     float cs[128];
     float cinv[128];
-    float bmax[2][kConsumerWarps];        // per-block: warp maxima, by tile parity
+    uint32_t bmax[2][kConsumerWarps];     // per-block: warp maxima (bits), by tile parity
     uint64_t full[kStages];
     uint64_t empty[kStages];
     int abort;
 };
+
+// One 128 x 128 tile of transposed codes (swizzled [channel][8-token unit]) ->
+// out_t rows c0 .. c0+127, tokens t0 .. t0+127: 16-byte stores, eight lanes
+// per 128-byte row.
+__device__ __forceinline__ void store_code_tile(const uint2 (*codes)[16], uint8_t* out, int64_t T,
+                                                int c0, int64_t t0, int ct) {
+    uint4* out_t = reinterpret_cast<uint4*>(out);
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int c = p * 64 + (ct >> 3);
+        const int ch = ct & 7;            // tokens 16ch .. 16ch+15
+        const int sw = (c >> 2) & 15;     // swizzle of row c
+        uint4 q = *reinterpret_cast<const uint4*>(&codes[c][2 * (ch ^ (sw >> 1))]);
+        if (sw & 1) q = make_uint4(q.z, q.w, q.x, q.y);
+        st_stream(out_t + ((static_cast<int64_t>(c0 + c) * T + t0) >> 4) + ch, q);
+    }
+}
 
 template <int FMT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -102,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- consumers
     const int ct = threadIdx.x;
     RingPos<kStages> pos;
-    uint32_t parity = 0;
+    uint32_t parity = 0;      // per-block: table in use
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
         const uint32_t tb = tw.row;
@@ -124,26 +143,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         if constexpr (MODE == kBlock) {
+            // Absolute values are >= 0, and the bit patterns of non-negative
+            // binary32 values order like the unsigned integers they spell, so
+            // one warp-wide unsigned max reduction (redux.sync) takes the max.
             float m = 0.0f;
 #pragma unroll
             for (int r = 0; r < 8; ++r)
                 m = fmaxf(m, fmaxf(fmaxf(fabsf(v[r][0]), fabsf(v[r][1])),
                                    fmaxf(fabsf(v[r][2]), fabsf(v[r][3]))));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if (lane == 0) sm.bmax[parity][warp] = m;
+            const uint32_t mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+            if (lane == 0) sm.bmax[parity][warp] = mw;
             if (named_bar_or(kBarConsumers, kConsumers, !ok)) {
                 if (ct == 0) *static_cast<volatile int*>(&sm.abort) = 1;
                 break;
             }
-            float b = sm.bmax[parity][0];
-#pragma unroll
-            for (int q = 1; q < kConsumerWarps; ++q) b = fmaxf(b, sm.bmax[parity][q]);
+            // lanes l and l + 16 read warp l's maximum
+            const uint32_t bw = __reduce_max_sync(0xffffffffu, sm.bmax[parity][lane & 15]);
             float sc, inv;
-            group_scale<FMT>(b, sc, inv);
+            group_scale<FMT>(__uint_as_float(bw), sc, inv);
+            // rows of this warp that exist (fewer than 8 only in a last, short
+            // block row)
+            const int64_t left = T - row0;
+            const int live = left < 8 ? static_cast<int>(left) : 8;
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
-                if (row0 + r < T)
+                if (r < live)
                     st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * C + c0) + lane,
                                   quantize4<FMT>(v[r], sc, inv));
             }
@@ -212,16 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if constexpr (MODE == kChannelT) {
             named_bar_sync(kBarConsumers, kConsumers);  // code tile complete
-            uint4* out_t = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                const int c = p * 64 + (ct >> 3);
-                const int ch = ct & 7;
-                const int sw = (c >> 2) & 15;
-                uint4 q = *reinterpret_cast<const uint4*>(&sm.codes[c][2 * (ch ^ (sw >> 1))]);
-                if (sw & 1) q = make_uint4(q.z, q.w, q.x, q.y);
-                st_stream(out_t + ((static_cast<int64_t>(c0 + c) * T + t0) >> 4) + ch, q);
-            }
+            store_code_tile(sm.codes, out, T, c0, t0, ct);
+            // The next tile writes colmax before its first barrier and the code
+            // tile only after its second, so these reads are complete first.
         }
     }
 }
