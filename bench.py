@@ -51,6 +51,7 @@ KERNEL_OF = {
     "per_block": "per_block_cast",
     "cast_back": "cast_back",
     "swiglu_clamp": "swiglu_cast_clamp",
+    "plain_f32": "per_token_cast_f32",
 }
 # bench workload -> seeded input set, where the names differ
 SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu"}
@@ -67,6 +68,7 @@ KERNEL_SOURCES = {
     "per_block_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "cast_back": ["cast_back.cu", "tkq_device.cuh"],
     "swiglu_cast_clamp": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_token_cast_f32": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
 }
 
 
@@ -75,6 +77,8 @@ def algorithmic_bytes(workload: str, T: int, C: int, weighted: bool) -> int:
     kern = KERNEL_OF[workload]
     if kern == "per_token_cast":
         return T * C * 2 + T * C + T * (C // 128) * 4
+    if kern == "per_token_cast_f32":
+        return T * C * 4 + T * C + T * (C // 128) * 4
     if kern in ("per_channel_cast", "per_channel_cast_t"):
         return T * C * 2 + T * C + (T // 128) * C * 4
     if kern == "per_block_cast":
@@ -255,6 +259,13 @@ class Problem:
             sf_pos = 3
             self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
                 i["x"], fmt, topk_weights=i.get("w"), out=od[0].view(fp8), out_sf=od[1], **opt)
+        elif kern == "per_token_cast_f32":
+            self.outputs = [E((T, C)), E((T, C // 128), f32)]
+            fn, args = tkq.tkq_per_token_cast_f32, [P(x), P(self.outputs[0]), None, T, C, 128,
+                                                    fcode, sf_flags]
+            sf_pos = 2
+            self.api = lambda i, od: tkq.per_token_cast(i["x"], fmt, out=od[0].view(fp8),
+                                                        out_sf=od[1], **opt)
         elif kern == "swiglu_cast_clamp":
             H = C // 2
             self.count = E((1,), torch.int64).zero_()
@@ -311,7 +322,7 @@ class Problem:
                                                     out_dtype=torch.bfloat16, out=od[0]),)
         else:
             raise KeyError(kern)
-        if sf_pos is not None and kern == "swiglu_cast_clamp":
+        if sf_pos is not None and kern in ("swiglu_cast_clamp", "per_token_cast_f32"):
             if sf_flags:
                 G = self.outputs[1].numel() // T
                 self.outputs[1] = E((tkq.tkq_sf_bytes(T, G, sf_flags),))
@@ -474,6 +485,8 @@ def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
         return oracle.per_block_cast(x, fmt, threads=threads)
     if kern == "per_token_cast":
         return oracle.per_token_cast(x, fmt, threads=threads)
+    if kern == "per_token_cast_f32":
+        return oracle.cast_rows_f32_ex(x, fmt, threads=threads)
     if kern == "swiglu_cast":
         return oracle.swiglu_cast(x, w, fmt, threads=threads)
     if kern == "swiglu_cast_clamp":
@@ -601,6 +614,13 @@ def run_ours(args):
         res["e2e"] = {"value": round(prob.bytes * e_steps / edt / 1e9, 2), "unit": "GB/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": round(edt / e_steps * 1e3, 3)}
+        with torch.cuda.stream(stream):
+            tc = d2d_copy_reference(prob, stream, flush)
+        res["d2d_copy"] = {"us": round(tc * 1e6, 2), "GB/s": round(prob.bytes / tc / 1e9, 1),
+                           "bytes": prob.bytes - prob.bytes % 2,
+                           "kernel_time_over_copy_time": round(per_launch / tc, 3),
+                           "note": "cudaMemcpyAsync device-to-device of half the algorithmic "
+                                   "bytes (read + write = the same traffic), timed like the kernel"}
         res["cpu_baseline"] = cpu_baseline_single_thread(args.workload, args.fmt)
         res["per_workload"] = other_workloads(dev, stream, peak, args)
     print(json.dumps(res), flush=True)
@@ -608,6 +628,30 @@ def run_ours(args):
         barrier()
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def d2d_copy_reference(prob: Problem, stream, flush):
+    """A device-to-device cudaMemcpyAsync (torch copy_) moving the same bytes
+    as one launch (half read, half written), timed like the kernel: median of
+    L2-flushed copies for small problems, back-to-back copies otherwise."""
+    import torch
+    n = prob.bytes // 2
+    src = torch.empty(n, dtype=torch.uint8, device=prob.dev)
+    dst = torch.empty_like(src)
+    ts = []
+    for i in range(13):
+        if flush is not None:
+            flush.max()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        dst.copy_(src)
+        e.record(stream)
+        e.synchronize()
+        if i >= 3:
+            ts.append(s.elapsed_time(e) / 1000.0)
+    t = float(np.median(ts))
+    return t
 
 
 def other_workloads(dev, stream, peak, args):
@@ -621,7 +665,8 @@ def other_workloads(dev, stream, peak, args):
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
                              ("per_channel_t", "e4m3", 0), ("per_block", "e4m3", 0),
-                             ("cast_back", "e4m3", 0), ("swiglu_clamp", "e4m3", 0)]:
+                             ("cast_back", "e4m3", 0), ("swiglu_clamp", "e4m3", 0),
+                             ("plain_f32", "e4m3", 0)]:
         prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)

@@ -25,7 +25,7 @@ __all__ = [
     "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
     "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
-    "tkq_swiglu_cast_t_clamp",
+    "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32",
 ]
 
 FMT_E4M3 = 0
@@ -97,6 +97,8 @@ def load_library():
         lib.tkq_swiglu_cast_clamp.restype = i
         lib.tkq_swiglu_cast_t_clamp.argtypes = [p, p, p, p, p, p, i64, i64, i, i, f32, p, p]
         lib.tkq_swiglu_cast_t_clamp.restype = i
+        lib.tkq_per_token_cast_f32.argtypes = [p, p, p, i64, i64, i, i, u, p]
+        lib.tkq_per_token_cast_f32.restype = i
         _lib = lib
         return lib
 
@@ -142,6 +144,11 @@ def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M
 def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
                              stream=None) -> int:
     return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
+
+
+def tkq_per_token_cast_f32(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                           stream=None) -> int:
+    return load_library().tkq_per_token_cast_f32(x, out, sf, T, C, group, fmt, sf_flags, stream)
 
 
 def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
@@ -231,12 +238,14 @@ def _fp8_dtype(fmt_code: int):
     return torch.float8_e4m3fn if fmt_code == FMT_E4M3 else torch.float8_e5m2
 
 
-def _check_input(x, name="x"):
+def _check_input(x, name="x", allow_f32=False):
     import torch
     if not isinstance(x, torch.Tensor) or not x.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
-    if x.dtype != torch.bfloat16 or x.dim() != 2 or not x.is_contiguous():
-        raise TypeError(f"{name} must be a contiguous 2-D bfloat16 tensor")
+    ok = (torch.bfloat16, torch.float32) if allow_f32 else (torch.bfloat16,)
+    if x.dtype not in ok or x.dim() != 2 or not x.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous 2-D "
+                        + ("bfloat16 or float32" if allow_f32 else "bfloat16") + " tensor")
 
 
 def _stream_handle(dev):
@@ -266,10 +275,11 @@ def _check_weights(topk_weights, T, x):
 def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_sf=None,
                    round_sf: bool = False, use_packed_ue8m0: bool = False,
                    use_tma_aligned_col_major_sf: bool = False):
-    """bf16 [T, C] -> (FP8 codes [T, C], scales).  Scales are fp32 [T, C/128]
-    unless a scale-layout option is set (see ``sf_tensor`` for the shapes)."""
+    """bf16 or fp32 [T, C] -> (FP8 codes [T, C], scales).  Scales are fp32
+    [T, C/128] unless a scale-layout option is set (see ``sf_tensor`` for the
+    shapes)."""
     import torch
-    _check_input(x)
+    _check_input(x, allow_f32=True)
     f = _fmt_code(fmt)
     T, C = x.shape
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
@@ -278,8 +288,9 @@ def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_s
     if out_sf is None:
         out_sf = sf_tensor(T, max(C // max(num_per_channels, 1), 0), flags, x.device)
     with torch.cuda.device(x.device):
-        st = tkq_per_token_cast_ex(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
-                                   flags, _stream_handle(x.device))
+        call = tkq_per_token_cast_f32 if x.dtype == torch.float32 else tkq_per_token_cast_ex
+        st = call(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f, flags,
+                  _stream_handle(x.device))
     if st:
         raise TkqError(st, "tkq_per_token_cast")
     return out, out_sf

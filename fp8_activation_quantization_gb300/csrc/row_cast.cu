@@ -1,6 +1,6 @@
 // row_cast.cu -- the per-token-group FP8 casts with row-major outputs:
-//   * the plain per_token_cast of a bf16 [T, C] matrix ("DeepSeek开源TileKernels：
-//     用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2);
+//   * the plain per_token_cast of a bf16 or fp32 [T, C] matrix ("DeepSeek开源
+//     TileKernels：用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2);
 //   * swiglu_forward_and_per_token_cast of a bf16 [T, 2H] gate|up matrix,
 //     optionally times a per-row routing weight and with the optional clamp
 //     (gate <= c, -c <= up <= c) whose changed values are counted (same page,
@@ -40,7 +40,7 @@ constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
 
 enum Mode {
     kPlain, kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kBackward,
-    kBackwardWeighted
+    kBackwardWeighted, kPlainF32
 };
 
 template <int MODE>
@@ -49,8 +49,10 @@ struct ModeTraits {
     static constexpr bool kClamp = MODE == kSwigluClamp || MODE == kSwigluWeightedClamp;
     static constexpr bool kWeighted =
         MODE == kSwigluWeighted || MODE == kSwigluWeightedClamp || MODE == kBackwardWeighted;
-    static constexpr int kOperands = MODE == kPlain ? 1 : (kBwd ? 3 : 2);  // boxes per chunk
-    static constexpr int kStageBytes = kOperands * kBoxBytes;
+    static constexpr bool kF32 = MODE == kPlainF32;   // fp32 input, 32 x 128 fp32 boxes
+    static constexpr int kOperands = (MODE == kPlain || kF32) ? 1 : (kBwd ? 3 : 2);  // boxes
+    static constexpr int kRowBytes = kF32 ? 512 : 256;  // one box row in shared memory
+    static constexpr int kStageBytes = kOperands * kRows * kRowBytes;
     static constexpr int kRingBytes = kBwd ? 3 * kStageBytes : 65536;
     static constexpr int kStages = kRingBytes / kStageBytes;
 };
@@ -148,6 +150,18 @@ __device__ __forceinline__ void load16(const uint8_t* p, float* v) {
     unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
 }
 
+// The same 16 elements of an fp32 box row (p = row + 32 j): four 16-byte loads.
+// (Eight lanes of a row then read 256 bytes at a 32-byte stride, a 2-way bank
+// conflict; shared-memory bandwidth is not what bounds this mode.)
+__device__ __forceinline__ void load16_f32(const uint8_t* p, float* v) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+    const float4* h = reinterpret_cast<const float4*>(p + 256);
+    *reinterpret_cast<float4*>(v) = q[0];
+    *reinterpret_cast<float4*>(v + 4) = q[1];
+    *reinterpret_cast<float4*>(v + 8) = h[0];
+    *reinterpret_cast<float4*>(v + 12) = h[1];
+}
+
 // The SwiGLU clamp of one launch: bound c (> 0) and the counter that the
 // number of changed input values is added to (may be null).
 struct Clamp {
@@ -241,12 +255,16 @@ __global__ void __launch_bounds__(kThreads, 3)
             if (lane == 0) *static_cast<volatile int*>(&sm.abort) = 1;  // stop the producer
             break;
         }
-        const uint8_t* p = sm.stage[s] + r * 256 + j * 16;
+        const uint8_t* p = sm.stage[s] + r * MT::kRowBytes + j * (MT::kRowBytes / 16);
         uint2* o = out + (row * out_ld + cb * 128) / 8;
         float* sfp = sf + row * sf_ld + cb;
         if constexpr (MODE == kPlain) {
             float v[16];
             load16(p, v);
+            emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
+        } else if constexpr (MT::kF32) {
+            float v[16];
+            load16_f32(p, v);
             emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else if constexpr (!MT::kBwd) {
             float g[16], u[16], v[16];
@@ -326,7 +344,9 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, voi
     // x as a bf16 [T, cols] matrix: C columns (plain) or 2H (gate | up)
     const int64_t cols = (MT::kOperands == 1 ? 1 : 2) * C_out;
     CUtensorMap map, map_dy;
-    if (!encode_bf16_2d(&map, x, cols, T, 128, kRows)) return cudaErrorInvalidValue;
+    const bool mapped = MT::kF32 ? encode_f32_2d(&map, x, cols, T, 128, kRows)
+                                 : encode_bf16_2d(&map, x, cols, T, 128, kRows);
+    if (!mapped) return cudaErrorInvalidValue;
     if constexpr (MT::kBwd) {
         if (!encode_bf16_2d(&map_dy, dy, C_out, T, 128, kRows)) return cudaErrorInvalidValue;
     } else {
@@ -359,6 +379,11 @@ cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, v
 cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
                                   int fmt, unsigned sf_flags, cudaStream_t stream) {
     return launch_fmt<kPlain>(fmt, x, nullptr, nullptr, out, sf, T, C, sf_flags, stream);
+}
+
+cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
+                                      int fmt, unsigned sf_flags, cudaStream_t stream) {
+    return launch_fmt<kPlainF32>(fmt, x, nullptr, nullptr, out, sf, T, C, sf_flags, stream);
 }
 
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,

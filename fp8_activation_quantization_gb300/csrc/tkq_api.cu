@@ -92,18 +92,32 @@ EncodeTiledFn encode_tiled() {
 }
 }  // namespace
 
-bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                    uint32_t box_cols, uint32_t box_rows) {
+namespace {
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, int64_t elem_bytes, const void* base,
+               int64_t cols, int64_t rows, uint32_t box_cols, uint32_t box_rows) {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elem_bytes)};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    return enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                    uint32_t box_cols, uint32_t box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, box_cols,
+                     box_rows);
+}
+
+bool encode_f32_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                   uint32_t box_cols, uint32_t box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, box_cols,
+                     box_rows);
 }
 
 unsigned int* device_status_word() {
@@ -223,6 +237,22 @@ tkq_status tkq_per_token_cast_ex(const void* x, void* out, void* sf, int64_t T, 
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
     return launch_status(tkq::launch_per_token_cast(x, out, sf, T, C, fmt, sf_flags,
                                                     static_cast<cudaStream_t>(stream)));
+}
+
+tkq_status tkq_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
+                                  int group, int fmt, unsigned sf_flags, tkq_stream_t stream) {
+    tkq_status st = check_common(T, C, group, fmt);
+    if (st != TKQ_OK) return st;
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
+    if (T == 0) return TKQ_OK;
+    if (!x || !out || !sf) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16)) return TKQ_ERR_ALIGN;
+    if ((st = check_sf(sf, sf_flags)) != TKQ_OK) return st;
+    const auto rx = tkq::span(x, T * C * 4), ro = tkq::span(out, T * C),
+               rs = tkq::span(sf, tkq_sf_bytes(T, C / group, sf_flags));
+    if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    return launch_status(tkq::launch_per_token_cast_f32(x, out, sf, T, C, fmt, sf_flags,
+                                                        static_cast<cudaStream_t>(stream)));
 }
 
 tkq_status tkq_per_token_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,

@@ -15,6 +15,9 @@ namespace tkq {
 // or rejects the arguments.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
                     uint32_t box_cols, uint32_t box_rows);
+// The same for a row-major fp32 matrix (row stride cols * 4 bytes).
+bool encode_f32_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                   uint32_t box_cols, uint32_t box_rows);
 
 // Number of SMs of the current device (cached per device; the environment
 // variable TKQ_NUM_SMS overrides it for grid sizing experiments).
@@ -31,6 +34,10 @@ int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks
 // sf_flags: TKQ_SF_* options of include/tkq.h (0 = row-major fp32 scales).
 cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
                                   int fmt, unsigned sf_flags, cudaStream_t stream);
+
+// The per-token cast of a row-major fp32 [T, C] matrix.
+cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
+                                      int fmt, unsigned sf_flags, cudaStream_t stream);
 
 // clamp: null (no clamp) or the SwiGLU clamp bound c > 0; clamp_count (may be
 // null) receives the number of clamped input values by atomic addition.

@@ -30,6 +30,8 @@ Workloads (all seeded, no dataset involved):
   zero rows); 16320 tokens leave a last block row of 64 tokens.
 * ``cast_back``     uint8 [16384, 7168] codes, uniform over all 256 byte values,
   and fp32 per-token scales [16384, 56] log-uniform in [2^-22, 2^4].
+* ``plain_f32``     fp32 [8192, 7168] drawn like ``plain_outlier`` but kept in
+  binary32 (an fp32 activation, e.g. a gradient before its cast).
 """
 from __future__ import annotations
 
@@ -61,6 +63,8 @@ WORKLOADS = {
     "cast_back": (16384, 7168, "cast_back E4M3 -> bf16 with per-token scales, codes uint8 "
                                "[16384, 7168] uniform bytes, scales fp32 [16384, 56] "
                                "log-uniform in [2^-22, 2^4]"),
+    "plain_f32": (8192, 7168, "per_token_cast E4M3 of an fp32 input, x fp32 [8192, 7168] "
+                              "~ N(0,1), 0.1% outliers x100, one all-zero row per 1024"),
 }
 
 _WORKLOAD_IDS = {name: i + 1 for i, name in enumerate(WORKLOADS)}
@@ -128,17 +132,22 @@ def normal_bf16(seed: int, stream: int, T: int, C: int, std: float = 1.0) -> np.
 
 
 def outlier_bf16(seed: int, stream: int, T: int, C: int, frac: float = 1e-3,
-                 factor: float = 100.0, zero_row_every: int = 1024) -> np.ndarray:
+                 factor: float = 100.0, zero_row_every: int = 1024,
+                 as_f32: bool = False) -> np.ndarray:
     """N(0,1) with a fraction ``frac`` of entries, chosen by the generator,
-    multiplied by ``factor`` and every ``zero_row_every``-th row (from row 0) zero."""
-    out = np.empty((int(T), int(C)), np.uint16)
+    multiplied by ``factor`` and every ``zero_row_every``-th row (from row 0) zero.
+    bf16 bits, or the binary32 values themselves with ``as_f32``."""
+    out = np.empty((int(T), int(C)), np.float32 if as_f32 else np.uint16)
 
     def fill(i, a, b):
         rng = rng_for(seed, stream, i)
         v = rng.standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
         mask = rng.random((CHUNK_ROWS, C), dtype=np.float32)[:b - a] < np.float32(frac)
         v[mask] *= np.float32(factor)
-        _to_bf16_into(v, out[a:b])
+        if as_f32:
+            out[a:b] = v
+        else:
+            _to_bf16_into(v, out[a:b])
 
     _chunked(int(T), fill)
     if zero_row_every:
@@ -235,6 +244,8 @@ def workload(name: str, seed: int = 0, rows: int | None = None) -> dict:
         return {"x": channel_outlier_bf16(seed, sid, T, C)}
     if name == "per_block":
         return {"x": outlier_bf16(seed, sid, T, C, zero_row_every=0)}
+    if name == "plain_f32":
+        return {"x": outlier_bf16(seed, sid, T, C, as_f32=True)}
     if name == "cast_back":
         return {"codes": random_bytes(seed, sid, T, C),
                 "sf": log_uniform_f32(seed, sid, (T, C // 128), -22.0, 4.0)}

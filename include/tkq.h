@@ -152,6 +152,15 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
  * sf_flags, or -1 for invalid arguments. */
 int64_t tkq_sf_bytes(int64_t T, int64_t groups_per_row, unsigned sf_flags);
 
+/*
+ * Per-token cast of an fp32 input ([P1] §2 operator table: the casts take fp32
+ * as well as bf16 activations): x fp32 [T, C], row-major, 16-byte aligned;
+ * otherwise tkq_per_token_cast_ex (codes of the exact quotient fl32(x / s),
+ * bit-exact; sf in the layout sf_flags selects).
+ */
+tkq_status tkq_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
+                                  int group, int fmt, unsigned sf_flags, tkq_stream_t stream);
+
 /* tkq_per_token_cast, tkq_swiglu_cast and tkq_swiglu_backward_cast with a
  * scale-factor layout (sf_flags above; sf sized by tkq_sf_bytes).  With
  * sf_flags == 0 they are the calls above. */

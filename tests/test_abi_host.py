@@ -221,3 +221,17 @@ def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
     assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 1.0, None, None) == 0
     assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 0.0, None, None) == 9
     assert "VALUE" in __import__("fp8_activation_quantization_gb300").tkq_status_string(9)
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((None, p(1 << 20), p(2 << 20), 4, 256, 128, 0, 0), 1),            # NULL input
+    ((p(), p(1 << 20), p(2 << 20), 4, 200, 128, 0, 0), 2),             # C % 128
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 64, 0, 0), 3),              # group
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 7, 0), 4),             # fmt
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 8), 8),             # flags
+    ((p(4), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 0), 5),            # x misaligned
+    ((p(), p(2048), p(2 << 20), 4, 256, 128, 0, 0), 7),                # out inside x (4 B/elem)
+    ((None, None, None, 0, 256, 128, 0, 0), 0),                        # empty batch
+])
+def test_per_token_cast_f32_validation(lib, args, expected):
+    assert lib.tkq_per_token_cast_f32(*args, None) == expected
