@@ -249,3 +249,80 @@ def test_tensor_api_shapes_and_dtypes(cuda_device):
         tkq.cast_back(q, s, group_size=(1, 128))
     with pytest.raises(tkq.TkqError):
         tkq.per_channel_cast(x[:300])                    # T % 128
+
+
+@pytest.mark.slow
+def test_beyond_2_31_elements(cuda_device):
+    """x of 131,200 x 16,384 bf16 (2.15e9 elements, 4.3 GB): byte offsets beyond
+    2^32 in every kernel.  The per-channel cast (transposed and in place), the
+    per-block cast (with a short last block row) and cast back of the per-block
+    result are checked bit-exact on sampled 128-token blocks at both ends and in
+    the middle."""
+    T, C = 131_200, 16_384
+    dev = cuda_device
+    rng = np.random.default_rng(78)
+    nb = T // 128
+    blocks = sorted({0, 1, nb // 2, nb - 2, nb - 1})
+    keep = {}
+    xd = torch.empty((T, C), dtype=torch.int16, device=dev)
+    chunk = 16384
+    for a in range(0, T, chunk):
+        b = min(T, a + chunk)
+        bits = rng.integers(0, 1 << 16, size=(b - a, C), dtype=np.uint16)
+        e = rng.integers(127 - 20, 127 + 12, size=(b - a, C), dtype=np.uint16)
+        bits = (bits & np.uint16(0x807F)) | (e << np.uint16(7)).astype(np.uint16)
+        xd[a:b] = torch.from_numpy(bits.view(np.int16)).to(dev)
+        for k in blocks:
+            if a <= 128 * k < b:
+                keep[k] = bits[128 * k - a:128 * k - a + 128].copy()
+    xb = xd.view(torch.bfloat16)
+    st = stream_of(dev)
+
+    # per-channel, transposed: out_t [C, T], sf_t [C, T/128]
+    out = torch.empty((C, T), dtype=torch.uint8, device=dev)
+    sf = torch.empty((C, nb), dtype=torch.float32, device=dev)
+    assert tkq.tkq_per_channel_cast(ctypes.c_void_p(xb.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                    ctypes.c_void_p(sf.data_ptr()), T, C, 128, 0, 1, st) == 0
+    torch.cuda.synchronize()
+    for k in blocks:
+        ro, rs = oracle.per_channel_cast(keep[k], "e4m3", transpose=True, threads=THREADS)
+        parity.assert_bit_exact(f"transposed codes, block {k}",
+                                out[:, 128 * k:128 * k + 128].cpu().numpy(), ro)
+        parity.assert_bit_exact(f"transposed scales, block {k}", sf[:, k:k + 1].cpu().numpy(), rs)
+    del out, sf
+
+    # per-channel, in place: out [T, C], sf [T/128, C]
+    out = torch.empty((T, C), dtype=torch.uint8, device=dev)
+    sf = torch.empty((nb, C), dtype=torch.float32, device=dev)
+    assert tkq.tkq_per_channel_cast(ctypes.c_void_p(xb.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                    ctypes.c_void_p(sf.data_ptr()), T, C, 128, 0, 0, st) == 0
+    torch.cuda.synchronize()
+    for k in blocks:
+        ro, rs = oracle.per_channel_cast(keep[k], "e4m3", threads=THREADS)
+        parity.assert_bit_exact(f"in-place codes, block {k}",
+                                out[128 * k:128 * k + 128].cpu().numpy(), ro)
+        parity.assert_bit_exact(f"in-place scales, block {k}", sf[k:k + 1].cpu().numpy(), rs)
+    del out, sf
+
+    # per-block on the first T - 64 rows (the last block row holds 64 tokens)
+    Tb = T - 64
+    out = torch.empty((Tb, C), dtype=torch.uint8, device=dev)
+    sf = torch.empty((nb, C // 128), dtype=torch.float32, device=dev)
+    assert tkq.tkq_per_block_cast(ctypes.c_void_p(xb.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                  ctypes.c_void_p(sf.data_ptr()), Tb, C, 128, 0, st) == 0
+    torch.cuda.synchronize()
+    # cast back of the per-block result to bf16
+    y = torch.empty((Tb, C), dtype=torch.bfloat16, device=dev)
+    assert tkq.tkq_cast_back(ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(sf.data_ptr()),
+                             ctypes.c_void_p(y.data_ptr()), Tb, C, 128, 128, 0, tkq.OUT_BF16,
+                             st) == 0
+    torch.cuda.synchronize()
+    for k in blocks:
+        rows = keep[k][:max(0, min(128, Tb - 128 * k))]
+        ro, rs = oracle.per_block_cast(rows, "e4m3")
+        got = out[128 * k:128 * k + rows.shape[0]].cpu().numpy()
+        parity.assert_bit_exact(f"per-block codes, block {k}", got, ro)
+        parity.assert_bit_exact(f"per-block scales, block {k}", sf[k:k + 1].cpu().numpy(), rs)
+        ey = expected_cast_back(ro, rs, 128, 128, "e4m3", True)
+        gy = y[128 * k:128 * k + rows.shape[0]].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert_bits_equal_nan_aware(f"cast back, block {k}", gy, ey, True)
