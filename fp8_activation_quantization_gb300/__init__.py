@@ -14,6 +14,7 @@ tensor-level helpers follow the call shape of the TileKernels quant API
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -117,11 +118,11 @@ def tkq_read_device_status(clear: bool = False) -> int:
 
 
 def tkq_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
-    return load_library().tkq_selftest_wait_timeout(int(limit_ns), stream)
+    return (_lib or load_library()).tkq_selftest_wait_timeout(int(limit_ns), stream)
 
 
 def tkq_status_string(status: int) -> str:
-    return load_library().tkq_status_string(int(status)).decode()
+    return (_lib or load_library()).tkq_status_string(int(status)).decode()
 
 
 # ---------------------------------------------------------------------------
@@ -129,48 +130,48 @@ def tkq_status_string(status: int) -> str:
 # ---------------------------------------------------------------------------
 
 def tkq_per_token_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, stream=None) -> int:
-    return load_library().tkq_per_token_cast(x, out, sf, T, C, group, fmt, stream)
+    return (_lib or load_library()).tkq_per_token_cast(x, out, sf, T, C, group, fmt, stream)
 
 
 def tkq_swiglu_cast(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, stream=None) -> int:
-    return load_library().tkq_swiglu_cast(x, w, out, sf, T, H, group, fmt, stream)
+    return (_lib or load_library()).tkq_swiglu_cast(x, w, out, sf, T, H, group, fmt, stream)
 
 
 def tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
                       stream=None) -> int:
-    return load_library().tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group, fmt, stream)
+    return (_lib or load_library()).tkq_swiglu_cast_t(x, w, out, sf, out_t, sf_t, T, H, group, fmt, stream)
 
 
 def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
                              stream=None) -> int:
-    return load_library().tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
+    return (_lib or load_library()).tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group, fmt, stream)
 
 
 def tkq_per_token_cast_f32(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                            stream=None) -> int:
-    return load_library().tkq_per_token_cast_f32(x, out, sf, T, C, group, fmt, sf_flags, stream)
+    return (_lib or load_library()).tkq_per_token_cast_f32(x, out, sf, T, C, group, fmt, sf_flags, stream)
 
 
 def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                           clamp_value=0.0, clamp_count=None, stream=None) -> int:
-    return load_library().tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group, fmt, sf_flags,
+    return (_lib or load_library()).tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group, fmt, sf_flags,
                                                 clamp_value, clamp_count, stream)
 
 
 def tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
                             clamp_value=0.0, clamp_count=None, stream=None) -> int:
-    return load_library().tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group, fmt,
+    return (_lib or load_library()).tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group, fmt,
                                                   clamp_value, clamp_count, stream)
 
 
 def tkq_per_channel_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, transpose=0,
                          stream=None) -> int:
-    return load_library().tkq_per_channel_cast(x, out, sf, T, C, group, fmt, int(transpose),
+    return (_lib or load_library()).tkq_per_channel_cast(x, out, sf, T, C, group, fmt, int(transpose),
                                                stream)
 
 
 def tkq_per_block_cast(x, out, sf, T, C, block=GROUP, fmt=FMT_E4M3, stream=None) -> int:
-    return load_library().tkq_per_block_cast(x, out, sf, T, C, block, fmt, stream)
+    return (_lib or load_library()).tkq_per_block_cast(x, out, sf, T, C, block, fmt, stream)
 
 
 OUT_F32 = 0
@@ -179,7 +180,7 @@ OUT_BF16 = 1
 
 def tkq_cast_back(codes, sf, out, T, C, group_rows=1, group_cols=GROUP, fmt=FMT_E4M3,
                   out_dtype=OUT_F32, stream=None) -> int:
-    return load_library().tkq_cast_back(codes, sf, out, T, C, group_rows, group_cols, fmt,
+    return (_lib or load_library()).tkq_cast_back(codes, sf, out, T, C, group_rows, group_cols, fmt,
                                         out_dtype, stream)
 
 
@@ -189,22 +190,22 @@ SF_COL_MAJOR = 4
 
 
 def tkq_sf_bytes(T, groups_per_row, sf_flags=0) -> int:
-    return load_library().tkq_sf_bytes(T, groups_per_row, sf_flags)
+    return (_lib or load_library()).tkq_sf_bytes(T, groups_per_row, sf_flags)
 
 
 def tkq_per_token_cast_ex(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                           stream=None) -> int:
-    return load_library().tkq_per_token_cast_ex(x, out, sf, T, C, group, fmt, sf_flags, stream)
+    return (_lib or load_library()).tkq_per_token_cast_ex(x, out, sf, T, C, group, fmt, sf_flags, stream)
 
 
 def tkq_swiglu_cast_ex(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                        stream=None) -> int:
-    return load_library().tkq_swiglu_cast_ex(x, w, out, sf, T, H, group, fmt, sf_flags, stream)
+    return (_lib or load_library()).tkq_swiglu_cast_ex(x, w, out, sf, T, H, group, fmt, sf_flags, stream)
 
 
 def tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                                 stream=None) -> int:
-    return load_library().tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group, fmt,
+    return (_lib or load_library()).tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group, fmt,
                                                       sf_flags, stream)
 
 
@@ -249,12 +250,30 @@ def _check_input(x, name="x", allow_f32=False):
 
 
 def _stream_handle(dev):
+    """The current stream of `dev` as an int (ctypes passes it as void*).
+    torch's raw-stream query avoids building a Stream object per call; the
+    public call is used where that query does not exist."""
     import torch
-    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(dev.index if dev.index is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream(dev).cuda_stream
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+_NO_CONTEXT = contextlib.nullcontext()
+
+
+def _device_ctx(dev):
+    """The launch must happen on the tensors' device: switch only if it is not
+    the current one (entering torch.cuda.device costs more than the launch)."""
+    import torch
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return _NO_CONTEXT
+    return torch.cuda.device(dev)
 
 
 def _sf_flags(round_sf: bool, use_packed_ue8m0: bool, use_tma_aligned_col_major_sf: bool) -> int:
@@ -287,7 +306,7 @@ def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_s
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
         out_sf = sf_tensor(T, max(C // max(num_per_channels, 1), 0), flags, x.device)
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         call = tkq_per_token_cast_f32 if x.dtype == torch.float32 else tkq_per_token_cast_ex
         st = call(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f, flags,
                   _stream_handle(x.device))
@@ -337,7 +356,7 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
         out = torch.empty((T, H), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
         out_sf = sf_tensor(T, H // g, flags, x.device)
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         stream = _stream_handle(x.device)
         if not with_transpose:
             if clamp is None:
@@ -388,7 +407,7 @@ def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int 
         out = torch.empty((T, 2 * H), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
         out_sf = sf_tensor(T, 2 * H // g, flags, x.device)
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         st = tkq_swiglu_backward_cast_ex(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(out),
                                          _ptr(out_sf), T, H, num_per_channels, f, flags,
                                          _stream_handle(x.device))
@@ -412,7 +431,7 @@ def per_channel_cast(x, fmt="e4m3", num_per_channels: int = GROUP, transpose: bo
     if out_sf is None:
         out_sf = torch.empty((C, T // g) if transpose else (T // g, C), dtype=torch.float32,
                              device=x.device)
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         st = tkq_per_channel_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
                                   int(transpose), _stream_handle(x.device))
     if st:
@@ -432,7 +451,7 @@ def per_block_cast(x, fmt="e4m3", block_size: int = GROUP, out=None, out_sf=None
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
         out_sf = torch.empty(((T + b - 1) // b, C // b), dtype=torch.float32, device=x.device)
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         st = tkq_per_block_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, block_size, f,
                                 _stream_handle(x.device))
     if st:
@@ -471,7 +490,7 @@ def cast_back(x, sf, fmt=None, group_size=(1, GROUP), out_dtype=None, out=None):
     if out is None:
         out = torch.empty((T, C), dtype=out_dtype, device=x.device)
     code = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
-    with torch.cuda.device(x.device):
+    with _device_ctx(x.device):
         st = tkq_cast_back(_ptr(x), _ptr(sf), _ptr(out), T, C, gr, gc, f, code,
                            _stream_handle(x.device))
     if st:
