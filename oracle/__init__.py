@@ -175,11 +175,15 @@ def fp8_encode(v: float, fmt) -> int:
     return int(_load().ora_fp8_encode(float(np.float32(v)), _fmt(fmt)))
 
 
-def fp8_encode_array(v: np.ndarray, fmt) -> np.ndarray:
-    """Encode every binary32 value of ``v``."""
+def fp8_encode_array(v: np.ndarray, fmt, out: np.ndarray | None = None) -> np.ndarray:
+    """Encode every binary32 value of ``v`` (into ``out`` if given: uint8,
+    contiguous, the size of ``v``)."""
     lib = _load()
     flat = np.ascontiguousarray(v, dtype=np.float32).ravel()
-    out = np.empty(flat.shape, np.uint8)
+    if out is None:
+        out = np.empty(flat.shape, np.uint8)
+    elif out.dtype != np.uint8 or out.size != flat.size or not out.flags.c_contiguous:
+        raise ValueError("out must be a contiguous uint8 array of the input's size")
     _check(lib.ora_fp8_encode_array(_ptr(flat), flat.size, _fmt(fmt), _ptr(out)), "encode_array")
     return out.reshape(np.shape(v))
 

@@ -164,3 +164,30 @@ def test_concurrent_host_threads(cuda_device):
         t.join()
     assert not errors, errors
     assert tkq.tkq_read_device_status() == 0
+
+
+@pytest.mark.parametrize("sms", ["1", "3"])
+def test_tiny_persistent_grids_give_the_same_bytes(cuda_device, sms, monkeypatch):
+    """With the grid capped at a few SMs (TKQ_NUM_SMS), every persistent CTA
+    walks many tiles and its copy ring wraps many times; results must equal
+    the full-grid results byte for byte."""
+    dev = cuda_device
+    x = to_dev_bf16(synth.outlier_bf16(31, 1, 1000, 1024, zero_row_every=0), dev)
+    xs = to_dev_bf16(synth.swiglu_bf16(32, 2, 1024, 512, gate_std=2.0), dev)
+    codes = torch.from_numpy(synth.random_bytes(33, 3, 1000, 1024)).to(dev)
+    sfc = torch.from_numpy(synth.log_uniform_f32(34, 4, (1000, 8), -10.0, 2.0)).to(dev)
+
+    def run():
+        return [*tkq.per_token_cast(x), *tkq.swiglu_forward_and_per_token_cast(xs, with_transpose=True),
+                *tkq.swiglu_backward_and_per_token_cast(xs, xs[:, :512].contiguous()),
+                *tkq.per_block_cast(x), *tkq.per_channel_cast(xs, transpose=True),
+                tkq.cast_back(codes, sfc, fmt="e4m3", out_dtype=torch.bfloat16)]
+
+    ref = run()
+    torch.cuda.synchronize()
+    monkeypatch.setenv("TKQ_NUM_SMS", sms)
+    got = run()
+    torch.cuda.synchronize()
+    for i, (a, b) in enumerate(zip(got, ref)):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"output {i} differs"
+    assert tkq.tkq_read_device_status() == 0
