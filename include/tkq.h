@@ -153,8 +153,9 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
 int64_t tkq_sf_bytes(int64_t T, int64_t groups_per_row, unsigned sf_flags);
 
 /*
- * Per-token cast of an fp32 input ([P1] §2 operator table: the casts take fp32
- * as well as bf16 activations): x fp32 [T, C], row-major, 16-byte aligned;
+ * Per-token cast of an fp32 input ([P2] §3.2: the per-token cast kernel takes
+ * a BF16 or FP32 [num_tokens, hidden] matrix): x fp32 [T, C], row-major,
+ * 16-byte aligned;
  * otherwise tkq_per_token_cast_ex (codes of the exact quotient fl32(x / s),
  * bit-exact; sf in the layout sf_flags selects).
  */
