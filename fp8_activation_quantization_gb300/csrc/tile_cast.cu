@@ -249,6 +249,196 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Transposed per-channel cast with two independent consumer groups.
+//
+// With one lock-stepped group of 16 warps a tile's dependent chain (column
+// maxima, barrier, four warps forming scales, barrier, codes into the shared
+// tile, barrier, tile out) is exposed once per tile.  Here two groups of 8
+// warps take alternate half-width tiles (128 tokens x 64 channels) from one
+// 8-stage TMA ring, each with its own named barrier, column table and code
+// tile, so one group's chain overlaps the other's work.  A thread holds 16
+// tokens x 2 channels (warp w of a group: tokens 16w..16w+15; lane l:
+// channels 2l, 2l+1), i.e. one 16-byte run of codes per channel; the code tile
+// [channel][16-token unit] is XOR-swizzled by (channel / 2) & 7 so that both
+// the 16-byte writes (eight lanes: eight rows) and the 16-byte reads (eight
+// threads: one row) hit distinct bank groups.
+// ---------------------------------------------------------------------------
+constexpr int kCtGroupWarps = 8;
+constexpr int kCtGroupThreads = kCtGroupWarps * 32;
+constexpr int kCtGroups = 2;
+constexpr int kCtThreads = kCtGroups * kCtGroupThreads + 32;
+constexpr int kCtStages = 8;
+constexpr int kCtTileCols = 64;
+constexpr int kCtTileBytes = 128 * kCtTileCols * 2;
+
+struct CtGroupSmem {
+    uint4 codes[kCtTileCols][8];          // [channel][16-token unit], swizzled
+    float colmax[kCtGroupWarps][kCtTileCols];
+    float cs[kCtTileCols];
+    float cinv[kCtTileCols];
+};
+
+struct alignas(1024) CtSmem {
+    uint8_t stage[kCtStages][kCtTileBytes];
+    CtGroupSmem g[kCtGroups];
+    uint64_t full[kCtStages];
+    uint64_t empty[kCtStages];
+    int abort;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kCtThreads, 1)
+    channel_t_kernel(const __grid_constant__ CUtensorMap tmap, uint8_t* __restrict__ out,
+                     float* __restrict__ sf, int64_t T, int C, unsigned int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    CtSmem& sm = *reinterpret_cast<CtSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t{1023});
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t CB = static_cast<uint32_t>(C) / kCtTileCols;
+    const uint32_t TB = static_cast<uint32_t>(T >> 7);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kCtStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kCtGroupWarps);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer
+    if (warp == kCtGroups * kCtGroupWarps) {
+        if (lane == 0) {
+            uint32_t issued = 0;
+            RingPos<kCtStages> pos;
+            for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), ++issued) {
+                if (!mbar_wait_bounded(&sm.empty[pos.stage], pos.phase ^ 1u, &sm.abort, status)) {
+                    *static_cast<volatile int*>(&sm.abort) = 1;
+                    break;
+                }
+                uint64_t* full = &sm.full[pos.stage];
+                mbar_arrive_expect_tx(full, kCtTileBytes);
+                tma_load_2d(sm.stage[pos.stage], &tmap, static_cast<int>(tw.col * kCtTileCols),
+                            static_cast<int>(tw.row * 128), full);
+                pos.advance();
+            }
+            const uint32_t first = issued > kCtStages ? issued - kCtStages : 0;
+            for (uint32_t k = first; k < issued; ++k)
+                mbar_wait_bounded(&sm.full[k % kCtStages], (k / kCtStages) & 1u, nullptr, status);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------ consumer groups
+    const int grp = warp / kCtGroupWarps;
+    const int wg = warp - grp * kCtGroupWarps;
+    const int gt = threadIdx.x - grp * kCtGroupThreads;   // thread within the group
+    const int bar = 1 + grp;                             // the group's named barrier
+    CtGroupSmem& G = sm.g[grp];
+    uint32_t i = static_cast<uint32_t>(grp);            // CTA-local tile index
+    for (TileWalk tw(blockIdx.x + grp * gridDim.x, kCtGroups * gridDim.x, CB); tw.row < TB;
+         tw.next(), i += kCtGroups) {
+        const uint32_t s = i % kCtStages;
+        const uint32_t tb = tw.row;
+        const int64_t t0 = static_cast<int64_t>(tb) * 128;
+        const int c0 = static_cast<int>(tw.col) * kCtTileCols;
+
+        const bool ok = mbar_wait_bounded(&sm.full[s], (i / kCtStages) & 1u, &sm.abort, status);
+        float v[16][2];
+        {
+            const uint8_t* base = sm.stage[s] + (16 * wg) * (kCtTileCols * 2) + lane * 4;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const uint32_t q = ok ? *reinterpret_cast<const uint32_t*>(base + r * kCtTileCols * 2)
+                                      : 0u;
+                v[r][0] = bf16_lo(q);
+                v[r][1] = bf16_hi(q);
+            }
+        }
+        // column maxima over this thread's 16 tokens (two chains per column)
+        {
+            float2 cm;
+            float* c = &cm.x;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float a = fabsf(v[0][k]), b = fabsf(v[1][k]);
+#pragma unroll
+                for (int r = 2; r < 16; r += 2) {
+                    a = fmaxf(a, fabsf(v[r][k]));
+                    b = fmaxf(b, fabsf(v[r + 1][k]));
+                }
+                c[k] = fmaxf(a, b);
+            }
+            *reinterpret_cast<float2*>(&G.colmax[wg][lane * 2]) = cm;
+        }
+        if (named_bar_or(bar, kCtGroupThreads, !ok)) {
+            if (gt == 0) *static_cast<volatile int*>(&sm.abort) = 1;
+            break;
+        }
+        if (gt < kCtTileCols) {
+            float m = G.colmax[0][gt];
+#pragma unroll
+            for (int q = 1; q < kCtGroupWarps; ++q) m = fmaxf(m, G.colmax[q][gt]);
+            float s_c, inv_c;
+            group_scale<FMT>(m, s_c, inv_c);
+            G.cs[gt] = s_c;
+            G.cinv[gt] = inv_c;
+            st_stream(sf + static_cast<int64_t>(c0 + gt) * TB + tb, s_c);
+        }
+        named_bar_sync(bar, kCtGroupThreads);
+        {
+            const float2 cs2 = *reinterpret_cast<const float2*>(&G.cs[lane * 2]);
+            const float2 ci2 = *reinterpret_cast<const float2*>(&G.cinv[lane * 2]);
+            const float csv[2] = {cs2.x, cs2.y};
+            const float civ[2] = {ci2.x, ci2.y};
+            const int unit = wg ^ (lane & 7);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float col[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) col[r] = v[r][k];
+                const uint2 lo = quantize8<FMT>(col, csv[k], civ[k]);
+                const uint2 hi = quantize8<FMT>(col + 8, csv[k], civ[k]);
+                G.codes[lane * 2 + k][unit] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            }
+        }
+        // release the stage (its values are consumed) behind an async-proxy fence
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+
+        named_bar_sync(bar, kCtGroupThreads);   // the code tile is complete
+        uint4* out_t = reinterpret_cast<uint4*>(out);
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const int c = p * 32 + (gt >> 3);
+            const int u = gt & 7;
+            const uint4 q = G.codes[c][u ^ ((c >> 1) & 7)];
+            st_stream(out_t + ((static_cast<int64_t>(c0 + c) * T + t0) >> 4) + u, q);
+        }
+        // The next tile of this group writes colmax before its first barrier
+        // and the code tile only after its second, so these reads come first.
+    }
+}
+
+template <int FMT>
+cudaError_t launch_channel_t(const void* x, void* out, float* sf, int64_t T, int64_t C,
+                             cudaStream_t stream) {
+    CUtensorMap map;
+    if (!encode_bf16_2d(&map, x, C, T, kCtTileCols, 128)) return cudaErrorInvalidValue;
+    auto* k = &channel_t_kernel<FMT>;
+    const size_t smem = sizeof(CtSmem) + 1024;
+    const int64_t n_tiles = (T / 128) * (C / kCtTileCols);
+    const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
+                                     (n_tiles + 1) / 2);
+    k<<<grid, kCtThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
+                                            static_cast<int>(C), device_status_word());
+    return cudaGetLastError();
+}
+
 template <int FMT, int MODE>
 cudaError_t launch(const void* x, void* out, float* sf, int64_t T, int64_t C,
                    cudaStream_t stream) {
@@ -275,8 +465,10 @@ cudaError_t launch_fmt(int fmt, const void* x, void* out, float* sf, int64_t T, 
 
 cudaError_t launch_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
                                     int fmt, bool transpose, cudaStream_t stream) {
-    return transpose ? launch_fmt<kChannelT>(fmt, x, out, sf, T, C, stream)
-                     : launch_fmt<kChannel>(fmt, x, out, sf, T, C, stream);
+    if (!transpose) return launch_fmt<kChannel>(fmt, x, out, sf, T, C, stream);
+    if (T == 0) return cudaSuccess;
+    return fmt == kFmtE4M3 ? launch_channel_t<kFmtE4M3>(x, out, sf, T, C, stream)
+                           : launch_channel_t<kFmtE5M2>(x, out, sf, T, C, stream);
 }
 
 cudaError_t launch_per_block_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,
