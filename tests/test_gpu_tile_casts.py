@@ -326,3 +326,56 @@ def test_beyond_2_31_elements(cuda_device):
         ey = expected_cast_back(ro, rs, 128, 128, "e4m3", True)
         gy = y[128 * k:128 * k + rows.shape[0]].view(torch.int16).cpu().numpy().view(np.uint16)
         assert_bits_equal_nan_aware(f"cast back, block {k}", gy, ey, True)
+
+
+@pytest.mark.slow
+def test_repeated_launches_are_identical_for_every_kernel(cuda_device):
+    """60 launches of every other kernel on one input (full-size workloads):
+    each result equals the first bit for bit, which equals the oracle for the
+    exact casts.  A ring stage handed back to the TMA producer before its
+    readers are done, or a missing barrier between a group's table writes and
+    reads, shows up here as a rare differing group."""
+    dev = cuda_device
+    xc = synth.workload("per_channel")["x"]
+    xb = synth.workload("per_block")["x"]
+    xcd, xbd = to_dev_bf16(xc, dev), to_dev_bf16(xb, dev)
+    moe = synth.workload("swiglu_moe")
+    xs = to_dev_bf16(moe["x"], dev)
+    ws = torch.from_numpy(moe["w"]).to(dev)
+    bwd = synth.workload("swiglu_bwd", rows=16384)
+    xg, dy = to_dev_bf16(bwd["x"], dev), to_dev_bf16(bwd["dy"], dev)
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    ops = {
+        "per_channel": lambda: tkq.per_channel_cast(xcd),
+        "per_channel_t": lambda: tkq.per_channel_cast(xcd, transpose=True),
+        "per_block": lambda: tkq.per_block_cast(xbd),
+        "swiglu": lambda: tkq.swiglu_forward_and_per_token_cast(xs, topk_weights=ws),
+        "swiglu_clamp": lambda: tkq.swiglu_forward_and_per_token_cast(
+            xs, use_clamp=True, swiglu_clamp_value=1.5, clamp_count=cnt),
+        "swiglu_bwd": lambda: tkq.swiglu_backward_and_per_token_cast(xg, dy),
+    }
+    exact = {"per_channel_t": oracle.per_channel_cast(xc, "e4m3", transpose=True, threads=THREADS),
+             "per_block": oracle.per_block_cast(xb, "e4m3", threads=THREADS)}
+    for name, op in ops.items():
+        first = [t.clone() for t in op()]
+        torch.cuda.synchronize()
+        if name in exact:
+            for a, e in zip(first, exact[name]):
+                parity.assert_bit_exact(name, a.contiguous().view(torch.uint8).cpu().numpy(),
+                                        np.ascontiguousarray(e).view(np.uint8))
+        for _ in range(60):
+            cur = op()
+            torch.cuda.synchronize()
+            for a, b in zip(first, cur):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"{name} changed"
+        cb_first = tkq.cast_back(first[0], first[1],
+                                 group_size=(128, 128) if name == "per_block" else
+                                 ((128, 1) if name == "per_channel" else (1, 128)),
+                                 out_dtype=torch.bfloat16) if name in ("per_block", "per_channel") else None
+        if cb_first is not None:
+            for _ in range(20):
+                again = tkq.cast_back(first[0], first[1],
+                                      group_size=(128, 128) if name == "per_block" else (128, 1),
+                                      out_dtype=torch.bfloat16)
+                assert torch.equal(cb_first.view(torch.uint8), again.view(torch.uint8))
+    assert tkq.tkq_read_device_status() == 0
