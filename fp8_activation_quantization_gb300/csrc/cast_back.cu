@@ -113,7 +113,11 @@ __global__ void __launch_bounds__(kThreads, 3)
                 float y[16];
                 decode16<FMT>(q[k], y);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) y[i] = __fmul_rn(y[i], s[i]);
+                for (int i = 0; i < 16; i += 2) {
+                    const float2 p = mul2(make_float2(y[i], y[i + 1]), make_float2(s[i], s[i + 1]));
+                    y[i] = p.x;
+                    y[i + 1] = p.y;
+                }
                 if constexpr (BF16) {
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + t * C + c);
 #pragma unroll

@@ -282,9 +282,11 @@ __global__ void __launch_bounds__(kThreads, 3)
                 if (live) n_clamped += n;
             }
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                v[k] = swiglu(g[k], u[k]);
-                if constexpr (MT::kWeighted) v[k] = __fmul_rn(v[k], wt);
+            for (int k = 0; k < 16; k += 2) {
+                float2 y = swiglu2(make_float2(g[k], g[k + 1]), make_float2(u[k], u[k + 1]));
+                if constexpr (MT::kWeighted) y = mul2(y, make_float2(wt, wt));
+                v[k] = y.x;
+                v[k + 1] = y.y;
             }
             emit_group<FMT, false, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else {
@@ -293,12 +295,18 @@ __global__ void __launch_bounds__(kThreads, 3)
             load16(p + kBoxBytes, u);
             load16(p + 2 * kBoxBytes, d);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                swiglu_grad(g[k], u[k], d[k], dg[k], du[k]);
+            for (int k = 0; k < 16; k += 2) {
+                float2 a, b;
+                swiglu_grad2(make_float2(g[k], g[k + 1]), make_float2(u[k], u[k + 1]),
+                             make_float2(d[k], d[k + 1]), a, b);
                 if constexpr (MT::kWeighted) {
-                    dg[k] = __fmul_rn(dg[k], wt);
-                    du[k] = __fmul_rn(du[k], wt);
+                    a = mul2(a, make_float2(wt, wt));
+                    b = mul2(b, make_float2(wt, wt));
                 }
+                dg[k] = a.x;
+                dg[k + 1] = a.y;
+                du[k] = b.x;
+                du[k + 1] = b.y;
             }
             emit_group<FMT, false, SFX>(dg, live, o, sfp, j, sf, lay, row, cb);
             emit_group<FMT, false, SFX>(du, live, o + C_out / 8, sfp + CB, j, sf, lay, row,

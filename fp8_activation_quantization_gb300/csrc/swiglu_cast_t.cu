@@ -162,9 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    y[r][k] = swiglu(gv[k], uv[k]);
-                    if constexpr (WEIGHTED) y[r][k] = __fmul_rn(y[r][k], wt[r]);
+                for (int k = 0; k < 4; k += 2) {
+                    float2 p = swiglu2(make_float2(gv[k], gv[k + 1]), make_float2(uv[k], uv[k + 1]));
+                    if constexpr (WEIGHTED) p = mul2(p, make_float2(wt[r], wt[r]));
+                    y[r][k] = p.x;
+                    y[r][k + 1] = p.y;
                 }
             }
         }

@@ -156,9 +156,7 @@ __global__ void __launch_bounds__(kChThreads, 1)
         const float civ[4] = {ci4.x, ci4.y, ci4.z, ci4.w};
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            const uint32_t code = pack4<FMT>(
-                quotient(v[r][0], csv[0], civ[0]), quotient(v[r][1], csv[1], civ[1]),
-                quotient(v[r][2], csv[2], civ[2]), quotient(v[r][3], csv[3], civ[3]));
+            const uint32_t code = quantize4_each<FMT>(v[r], csv, civ);
             st_stream_u32(reinterpret_cast<uint32_t*>(out + (row0 + r) * C + c0) + lane, code);
         }
         // Release the stage once the values read from it are consumed (the

@@ -114,6 +114,59 @@ __device__ __forceinline__ float quotient(float y, float s, float inv) {
     return __fmaf_rn(-res, inv, q0);
 }
 
+
+// ---------------------------------------------------------------------------
+// Packed binary32 pairs: sm_100+ add / mul / fma .f32x2 perform two
+// independent IEEE operations per instruction, each rounded to nearest even
+// like the scalar one, so results are bit-identical to the scalar forms while
+// half as many instructions issue.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// quotient() of two elements with the packed pair instructions: the product
+// and the correction are packed, the residual stays scalar (it needs -y);
+// fma(res, -inv, q0) is the scalar fma(-res, inv, q0) exactly.  Bit-identical.
+__device__ __forceinline__ float2 quotient2(float2 y, float2 s, float2 inv) {
+    const float2 q0 = mul2(y, inv);
+    const float2 res = make_float2(__fmaf_rn(q0.x, s.x, -y.x), __fmaf_rn(q0.y, s.y, -y.y));
+    return fma2(res, make_float2(-inv.x, -inv.y), q0);
+}
+
 // ---------------------------------------------------------------------------
 // FP8 packing: cvt.rn.satfinite converts two binary32 values to two FP8 codes
 // with round-to-nearest-even and saturation to the largest finite value.  The
@@ -142,15 +195,30 @@ __device__ __forceinline__ uint32_t pack4(float a0, float a1, float a2, float a3
     return r;
 }
 
+// Codes of four values (exact quotients) with per-value scales, packed
+// little-endian.
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize4_each(const float* v, const float* s,
+                                                   const float* inv) {
+    const float2 a = quotient2(make_float2(v[0], v[1]), make_float2(s[0], s[1]),
+                               make_float2(inv[0], inv[1]));
+    const float2 b = quotient2(make_float2(v[2], v[3]), make_float2(s[2], s[3]),
+                               make_float2(inv[2], inv[3]));
+    return pack4<FMT>(a.x, a.y, b.x, b.y);
+}
+
 // Codes of eight values sharing one group scale, packed little-endian.
 template <int FMT>
 __device__ __forceinline__ uint2 quantize8(const float* v, float s, float inv) {
-    uint2 r;
-    r.x = pack4<FMT>(quotient(v[0], s, inv), quotient(v[1], s, inv), quotient(v[2], s, inv),
-                     quotient(v[3], s, inv));
-    r.y = pack4<FMT>(quotient(v[4], s, inv), quotient(v[5], s, inv), quotient(v[6], s, inv),
-                     quotient(v[7], s, inv));
-    return r;
+    const float2 s2 = make_float2(s, s), i2 = make_float2(inv, inv);
+    float q[8];
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const float2 r = quotient2(make_float2(v[k], v[k + 1]), s2, i2);
+        q[k] = r.x;
+        q[k + 1] = r.y;
+    }
+    return make_uint2(pack4<FMT>(q[0], q[1], q[2], q[3]), pack4<FMT>(q[4], q[5], q[6], q[7]));
 }
 
 __device__ __forceinline__ float absmax8(const float* v) {
@@ -187,6 +255,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return r;
 }
 
+// swiglu of two elements with the packed pair instructions (bit-identical).
+__device__ __forceinline__ float2 swiglu2(float2 g, float2 u) {
+    const float2 t = mul2(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    const float2 den = add2(make_float2(1.0f, 1.0f), make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+    return mul2(mul2(g, make_float2(rcp_approx(den.x), rcp_approx(den.y))), u);
+}
+
 __device__ __forceinline__ float swiglu(float g, float u) {
     const float e = ex2_approx(__fmul_rn(g, -1.4426950408889634f));
     const float den = __fadd_rn(1.0f, e);
@@ -210,6 +285,20 @@ __device__ __forceinline__ void swiglu_grad(float g, float u, float d, float& dg
     du = __fmul_rn(d, __fmul_rn(g, sig));
 }
 
+// swiglu_grad of two elements with the packed pair instructions (the clamp of
+// the exponent and the transcendental steps stay scalar).  Bit-identical.
+__device__ __forceinline__ void swiglu_grad2(float2 g, float2 u, float2 d, float2& dg,
+                                             float2& du) {
+    const float2 t = mul2(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+    const float2 e = make_float2(ex2_approx(fminf(t.x, 126.0f)), ex2_approx(fminf(t.y, 126.0f)));
+    const float2 den = add2(make_float2(1.0f, 1.0f), e);
+    const float2 sig = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+    const float2 one_minus_sig = mul2(e, sig);
+    const float2 dsilu = mul2(sig, fma2(g, one_minus_sig, make_float2(1.0f, 1.0f)));
+    dg = mul2(mul2(d, u), dsilu);
+    du = mul2(d, mul2(g, sig));
+}
+
 // Four bf16 packed in a uint2 -> four floats, element order preserved.
 __device__ __forceinline__ void unpack4(const uint2& q, float* v) {
     v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x);
@@ -219,8 +308,10 @@ __device__ __forceinline__ void unpack4(const uint2& q, float* v) {
 // Codes of four values sharing one group scale, packed little-endian.
 template <int FMT>
 __device__ __forceinline__ uint32_t quantize4(const float* v, float s, float inv) {
-    return pack4<FMT>(quotient(v[0], s, inv), quotient(v[1], s, inv), quotient(v[2], s, inv),
-                      quotient(v[3], s, inv));
+    const float2 s2 = make_float2(s, s), i2 = make_float2(inv, inv);
+    const float2 a = quotient2(make_float2(v[0], v[1]), s2, i2);
+    const float2 b = quotient2(make_float2(v[2], v[3]), s2, i2);
+    return pack4<FMT>(a.x, a.y, b.x, b.y);
 }
 
 // The SwiGLU kernels quantize y * inv, the product by the rounded reciprocal of
@@ -230,8 +321,10 @@ __device__ __forceinline__ uint32_t quantize4(const float* v, float s, float inv
 // there, while the plain cast keeps `quotient` to be bit-exact.
 template <int FMT>
 __device__ __forceinline__ uint32_t quantize4_mul(const float* v, float inv) {
-    return pack4<FMT>(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv), __fmul_rn(v[2], inv),
-                      __fmul_rn(v[3], inv));
+    const float2 i2 = make_float2(inv, inv);
+    const float2 a = mul2(make_float2(v[0], v[1]), i2);
+    const float2 b = mul2(make_float2(v[2], v[3]), i2);
+    return pack4<FMT>(a.x, a.y, b.x, b.y);
 }
 
 template <int FMT>
