@@ -13,16 +13,17 @@
 // GB300 design: persistent CTAs (3 per SM) stream "chunks" of 32 rows x one
 // 128-channel block.  Warp 8 is the producer: one lane loads each chunk with
 // one 2-D TMA box per operand (32 x 128 bf16 = 8 KB: x; or gate and up; or
-// gate, up and dy) into a shared ring of 64-72 KB (8 plain, 4 SwiGLU or 3
-// backward chunks in flight per CTA).  Rows past T are zero-filled by the TMA
+// gate, up and dy; 16 KB of fp32 x) into a shared ring of 64-72 KB (8 plain,
+// 4 SwiGLU or fp32, 3 backward chunks in flight per CTA).  Rows past T are zero-filled by the TMA
 // unit and never stored, so ragged T needs no special path.  Warps 0..7 are
 // consumers: warp w owns rows 4w..4w+3 of the chunk, eight lanes per row
 // (lane j holds elements [8j, 8j+8) and [64+8j, 64+8j+8), read as two
 // conflict-free 16-byte shared loads per operand), the group absmax is three
 // xor shuffles, and codes leave as 8-byte stores (eight lanes write one
-// 64-byte run).  The plain cast writes the codes of the exact binary32
-// quotient fl(x / s) (see `quotient`), so it is bit-exact; the SwiGLU casts
-// write the codes of y * fl(1 / s) as the page's kernel does.
+// 64-byte run).  The plain casts write the codes of the exact binary32
+// quotient fl(x / s) (`quotient` / `quotient2`), so they are bit-exact; the
+// SwiGLU casts write the codes of y * fl(1 / s) as the page's kernel does.
+// Elementwise fp32 steps run on packed pairs (tkq_device.cuh).
 // Every mbarrier wait is bounded (tkq_async.cuh).
 #include <cuda.h>
 

@@ -22,9 +22,9 @@
 // warp releases the stage to the producer; the column work runs from registers.
 //   * Row groups (1 x 128 channels = one warp row): a butterfly absmax across
 //     the 32 lanes that halves the live values at each xor step (9 shuffles
-//     for 8 rows); lanes 4r..4r+3 then hold row r, compute its scale once and
-//     shuffle scale and reciprocal back.  Codes leave as 4-byte stores, one
-//     128-byte run per warp store instruction.
+//     for 8 rows); lanes 4r..4r+3 then hold row r, one of them forms the
+//     row's scale and publishes its reciprocal through shared memory.  Codes
+//     leave as 4-byte stores, one 128-byte run per warp store instruction.
 //   * Column groups (128 tokens x 1 channel): per-thread maxima over 8 tokens,
 //     a 16 x 128 shared table reduced by 128 threads, scales broadcast through
 //     shared memory.  Codes are transposed through a 16 KB byte tile
