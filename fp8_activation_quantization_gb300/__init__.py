@@ -26,7 +26,7 @@ __all__ = [
     "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
     "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
-    "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32",
+    "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
 ]
 
 FMT_E4M3 = 0
@@ -100,6 +100,8 @@ def load_library():
         lib.tkq_swiglu_cast_t_clamp.restype = i
         lib.tkq_per_token_cast_f32.argtypes = [p, p, p, i64, i64, i, i, u, p]
         lib.tkq_per_token_cast_f32.restype = i
+        lib.tkq_swiglu_values.argtypes = [p, p, p, i64, i64, p]
+        lib.tkq_swiglu_values.restype = i
         _lib = lib
         return lib
 
@@ -150,6 +152,10 @@ def tkq_swiglu_backward_cast(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3,
 def tkq_per_token_cast_f32(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
                            stream=None) -> int:
     return (_lib or load_library()).tkq_per_token_cast_f32(x, out, sf, T, C, group, fmt, sf_flags, stream)
+
+
+def tkq_swiglu_values(x, w, y, T, H, stream=None) -> int:
+    return (_lib or load_library()).tkq_swiglu_values(x, w, y, T, H, stream)
 
 
 def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
@@ -496,3 +502,21 @@ def cast_back(x, sf, fmt=None, group_size=(1, GROUP), out_dtype=None, out=None):
     if st:
         raise TkqError(st, "tkq_cast_back")
     return out
+
+
+def swiglu_values(x, topk_weights=None):
+    """Diagnostic: the fp32 SwiGLU values [T, H] exactly as the SwiGLU casts
+    compute them before quantizing (x: bf16 [T, 2H] gate | up)."""
+    import torch
+    _check_input(x)
+    T, H2 = x.shape
+    if H2 % 2:
+        raise ValueError("x must have an even number of columns (gate | up)")
+    _check_weights(topk_weights, T, x)
+    y = torch.empty((T, H2 // 2), dtype=torch.float32, device=x.device)
+    with _device_ctx(x.device):
+        st = tkq_swiglu_values(_ptr(x), _ptr(topk_weights), _ptr(y), T, H2 // 2,
+                               _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_swiglu_values")
+    return y

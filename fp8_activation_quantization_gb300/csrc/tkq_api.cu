@@ -453,6 +453,21 @@ tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t 
                                                static_cast<cudaStream_t>(stream)));
 }
 
+tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T, int64_t H,
+                             tkq_stream_t stream) {
+    tkq_status st = check_common(T, H, 128, TKQ_FMT_E4M3);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !y) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(y, 16) || (w && !tkq::aligned(w, 4)))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * H * 4), ry = tkq::span(y, T * H * 4);
+    const auto rw = w ? tkq::span(w, T * 4) : tkq::Range{0, 0};
+    if (tkq::overlap(rx, ry) || tkq::overlap(rw, ry)) return TKQ_ERR_ALIAS;
+    return launch_status(
+        tkq::launch_swiglu_values(x, w, y, T, H, static_cast<cudaStream_t>(stream)));
+}
+
 tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
     if (!flags) return TKQ_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;

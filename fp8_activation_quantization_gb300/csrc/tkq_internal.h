@@ -35,6 +35,10 @@ int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks
 cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
                                   int fmt, unsigned sf_flags, cudaStream_t stream);
 
+// The fp32 SwiGLU values y [T, H] the SwiGLU casts quantize (diagnostic).
+cudaError_t launch_swiglu_values(const void* x, const float* w, float* y, int64_t T, int64_t H,
+                                 cudaStream_t stream);
+
 // The per-token cast of a row-major fp32 [T, C] matrix.
 cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
                                       int fmt, unsigned sf_flags, cudaStream_t stream);

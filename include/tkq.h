@@ -286,6 +286,18 @@ tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, flo
                                    int fmt, float clamp_value, uint64_t* clamp_count,
                                    tkq_stream_t stream);
 
+/*
+ * Diagnostic (not an operation of the source pages): the fp32 SwiGLU values
+ *   y[t, c] = silu(x[t, c]) * x[t, H + c] [* w[t]]
+ * computed exactly as tkq_swiglu_cast and tkq_swiglu_cast_t compute them
+ * before quantizing (the SM's ex2 / rcp, see tkq_swiglu_cast), written out so
+ * that their accuracy can be checked value by value.
+ *   x : bf16 [T, 2H];  w : fp32 [T] or NULL;  y : fp32 [T, H], 16-byte aligned
+ * T >= 0; H > 0, H % 128 == 0.
+ */
+tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T, int64_t H,
+                             tkq_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);
 
