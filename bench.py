@@ -51,12 +51,15 @@ KERNEL_OF = {
     "per_block": "per_block_cast",
     "cast_back": "cast_back",
     "swiglu_clamp": "swiglu_cast_clamp",
+    "swiglu_t_clamp": "swiglu_cast_t_clamp",
     "plain_f32": "per_token_cast_f32",
 }
 # bench workload -> seeded input set, where the names differ
-SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu"}
-# SwiGLU clamp bound of the swiglu_clamp workload (gate ~ N(0, 2^2): ~2.3 % of
-# the gates lie above it)
+SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu",
+            "swiglu_t_clamp": "swiglu_t"}
+# SwiGLU clamp bound of the clamped workloads (swiglu_clamp: gate ~ N(0, 2^2),
+# ~2.3 % of the gates lie above it; swiglu_t_clamp: gate and up ~ N(0, 1), about
+# one value in 10^4 is clamped; the clamp runs on every element either way)
 CLAMP_VALUE = 4.0
 KERNEL_SOURCES = {
     "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
@@ -68,6 +71,7 @@ KERNEL_SOURCES = {
     "per_block_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "cast_back": ["cast_back.cu", "tkq_device.cuh"],
     "swiglu_cast_clamp": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_cast_t_clamp": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_token_cast_f32": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
 }
 
@@ -93,7 +97,7 @@ def algorithmic_bytes(workload: str, T: int, C: int, weighted: bool) -> int:
     b = T * 2 * H * 2 + T * H + T * (H // 128) * 4
     if weighted:
         b += T * 4
-    if kern == "swiglu_cast_t":
+    if kern in ("swiglu_cast_t", "swiglu_cast_t_clamp"):
         b += T * H + H * (T // 128) * 4
     return b
 
@@ -296,6 +300,19 @@ class Problem:
             self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
                 i["x"], fmt, topk_weights=i.get("w"), with_transpose=True,
                 out=od[0].view(fp8), out_sf=od[1], out_t=od[2].view(fp8), out_sf_t=od[3])
+        elif kern == "swiglu_cast_t_clamp":
+            H = C // 2
+            self.count = E((1,), torch.int64).zero_()
+            self.outputs = [E((T, H)), E((T, H // 128), f32), E((H, T)), E((H, T // 128), f32)]
+            o = self.outputs
+            fn, args = tkq.tkq_swiglu_cast_t_clamp, [P(x), P(w), P(o[0]), P(o[1]), P(o[2]),
+                                                     P(o[3]), T, H, 128, fcode, CLAMP_VALUE,
+                                                     P(self.count)]
+            sf_pos = None
+            self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
+                i["x"], fmt, topk_weights=i.get("w"), with_transpose=True,
+                out=od[0].view(fp8), out_sf=od[1], out_t=od[2].view(fp8), out_sf_t=od[3],
+                use_clamp=True, swiglu_clamp_value=CLAMP_VALUE, clamp_count=self.count)
         elif kern in ("per_channel_cast", "per_channel_cast_t"):
             tr = kern.endswith("_t")
             self.outputs = [E((C, T) if tr else (T, C)),
@@ -493,6 +510,8 @@ def run_oracle(kern: str, d: dict, rows: int, fmt: str, threads: int = 1):
         return oracle.swiglu_cast(x, w, fmt, threads=threads, clamp=CLAMP_VALUE)
     if kern == "swiglu_backward_cast":
         return oracle.swiglu_backward_cast(x, d["dy"][:rows], w, fmt, threads=threads)
+    if kern == "swiglu_cast_t_clamp":
+        return oracle.swiglu_cast_t(x, w, fmt, threads=threads, clamp=CLAMP_VALUE)
     return oracle.swiglu_cast_t(x, w, fmt, threads=threads)
 
 
@@ -666,7 +685,7 @@ def other_workloads(dev, stream, peak, args):
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
                              ("per_channel_t", "e4m3", 0), ("per_block", "e4m3", 0),
                              ("cast_back", "e4m3", 0), ("swiglu_clamp", "e4m3", 0),
-                             ("plain_f32", "e4m3", 0)]:
+                             ("swiglu_t_clamp", "e4m3", 0), ("plain_f32", "e4m3", 0)]:
         prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
@@ -683,8 +702,11 @@ def other_workloads(dev, stream, peak, args):
 def _workload_desc(name):
     from fp8_activation_quantization_gb300 import synth
     d = synth.WORKLOADS[SYNTH_OF.get(name, name)][2]
-    return d.replace("per_channel_cast (+transpose)", "per_channel_cast + transpose") \
-        if name == "per_channel_t" else d
+    if name == "per_channel_t":
+        return d.replace("per_channel_cast (+transpose)", "per_channel_cast + transpose")
+    if name.endswith("_clamp"):
+        return d.replace("swiglu +", f"swiglu with clamp c = {CLAMP_VALUE:g} (count kept) +", 1)
+    return d
 
 
 # ---------------------------------------------------------------------------

@@ -23,7 +23,9 @@
 // 64-byte run).  The plain casts write the codes of the exact binary32
 // quotient fl(x / s) (`quotient` / `quotient2`), so they are bit-exact; the
 // SwiGLU casts write the codes of y * fl(1 / s) as the page's kernel does.
-// Elementwise fp32 steps run on packed pairs (tkq_device.cuh).
+// Elementwise fp32 steps run on packed pairs (tkq_device.cuh); a clamp bound
+// that is a bf16 value is applied, and its changes counted, on the packed bf16
+// input pairs before they are widened (same values, half the instructions).
 // Every mbarrier wait is bounded (tkq_async.cuh).
 #include <cuda.h>
 
@@ -163,11 +165,13 @@ __device__ __forceinline__ void load16_f32(const uint8_t* p, float* v) {
     *reinterpret_cast<float4*>(v + 12) = h[1];
 }
 
-// The SwiGLU clamp of one launch: bound c (> 0) and the counter that the
-// number of changed input values is added to (may be null).
+// The SwiGLU clamp of one launch: bound c (> 0), the counter that the number
+// of changed input values is added to (may be null), and c in both halves of
+// a bf16 pair when c is a bf16 value (else 0: the clamp then runs in fp32).
 struct Clamp {
     float value;
     unsigned long long* count;
+    uint32_t c2;
 };
 
 // tmap: x [T, C] (plain) or [T, 2H] (gate | up); tmap_dy: dy [T, H] (backward
@@ -269,18 +273,45 @@ __global__ void __launch_bounds__(kThreads, 3)
             emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else if constexpr (!MT::kBwd) {
             float g[16], u[16], v[16];
-            load16(p, g);
-            load16(p + kBoxBytes, u);
             if constexpr (MT::kClamp) {
-                const float c = clamp.value;
+                uint4 gq[2] = {*reinterpret_cast<const uint4*>(p),
+                               *reinterpret_cast<const uint4*>(p + 128)};
+                uint4 uq[2] = {*reinterpret_cast<const uint4*>(p + kBoxBytes),
+                               *reinterpret_cast<const uint4*>(p + kBoxBytes + 128)};
                 uint32_t n = 0;
+                if (clamp.c2) {
+                    // c is a bf16 value: clamp and count on the packed pairs
+                    const uint32_t c2 = clamp.c2;
+                    uint32_t n2 = 0;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    n += (g[k] > c) + (fabsf(u[k]) > c);
-                    g[k] = fminf(g[k], c);
-                    u[k] = fmaxf(fminf(u[k], c), -c);
+                    for (int h = 0; h < 2; ++h) {
+                        n2 += clamp_pairs_bf16(gq[h].x, uq[h].x, c2);
+                        n2 += clamp_pairs_bf16(gq[h].y, uq[h].y, c2);
+                        n2 += clamp_pairs_bf16(gq[h].z, uq[h].z, c2);
+                        n2 += clamp_pairs_bf16(gq[h].w, uq[h].w, c2);
+                    }
+                    n = (n2 & 0xFFFFu) + (n2 >> 16);
+                    unpack8(gq[0], g);
+                    unpack8(gq[1], g + 8);
+                    unpack8(uq[0], u);
+                    unpack8(uq[1], u + 8);
+                } else {
+                    unpack8(gq[0], g);
+                    unpack8(gq[1], g + 8);
+                    unpack8(uq[0], u);
+                    unpack8(uq[1], u + 8);
+                    const float c = clamp.value;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        n += (g[k] > c) + (fabsf(u[k]) > c);
+                        g[k] = fminf(g[k], c);
+                        u[k] = fmaxf(fminf(u[k], c), -c);
+                    }
                 }
                 if (live) n_clamped += n;
+            } else {
+                load16(p, g);
+                load16(p + kBoxBytes, u);
             }
 #pragma unroll
             for (int k = 0; k < 16; k += 2) {
@@ -376,7 +407,7 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, voi
 template <int MODE>
 cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, void* out,
                        void* sf, int64_t T, int64_t C_out, unsigned sf_flags,
-                       cudaStream_t stream, Clamp clamp = Clamp{0.0f, nullptr}) {
+                       cudaStream_t stream, Clamp clamp = Clamp{0.0f, nullptr, 0u}) {
     if (T == 0) return cudaSuccess;
     return fmt == kFmtE4M3
                ? launch<kFmtE4M3, MODE>(x, dy, w, out, sf, T, C_out, sf_flags, clamp, stream)
@@ -399,7 +430,7 @@ cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* s
                                int64_t H, int fmt, unsigned sf_flags, const float* clamp,
                                unsigned long long* clamp_count, cudaStream_t stream) {
     if (clamp) {
-        const Clamp c{*clamp, clamp_count};
+        const Clamp c{*clamp, clamp_count, bf16x2_bound(*clamp)};
         return w ? launch_fmt<kSwigluWeightedClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags,
                                                     stream, c)
                  : launch_fmt<kSwigluClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream, c);

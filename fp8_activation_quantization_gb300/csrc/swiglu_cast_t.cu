@@ -9,7 +9,8 @@
 // "per_channel_cast (+transpose / fused)").  Both outputs are quantized from the
 // same fp32 y.  With CLAMP the gate is clamped to <= c and the up projection to
 // [-c, c] before the SwiGLU, and the number of changed values is added to a
-// counter (one atomic per warp), as in §3.3 of the second page.
+// counter (one atomic per warp), as in §3.3 of the second page; a bound that is
+// a bf16 value is applied on the packed bf16 input pairs before widening.
 //
 // GB300 design: one persistent CTA per SM walks 128-token x 128-channel tiles
 // of y.  Warp 16 is the producer: one lane streams the gate and up tiles of the
@@ -70,7 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     swiglu_cast_t_kernel(const __grid_constant__ CUtensorMap tmap, const float* __restrict__ w,
                          uint8_t* __restrict__ out, float* __restrict__ sf,
                          uint4* __restrict__ out_t, float* __restrict__ sf_t, int64_t T, int H,
-                         float clamp, unsigned long long* __restrict__ clamp_count,
+                         float clamp, uint32_t clamp2,
+                         unsigned long long* __restrict__ clamp_count,
                          unsigned int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     SharedStorage& sm = *reinterpret_cast<SharedStorage*>(
@@ -142,6 +144,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- y = silu(g) * u [* w] for this thread's 8 x 4 block ----------
         float y[8][4];
         {
+            // clamp counts of this tile: per half of the packed-bf16 clamp, and
+            // of the fp32 clamp
+            [[maybe_unused]] uint32_t n2 = 0, n1 = 0;
             const uint8_t* g_base = sm.stage[s] + warp * 8 * 256 + lane * 8;
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -151,15 +156,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uq = *reinterpret_cast<const uint2*>(g_base + kTileBytes + r * 256);
                 }
                 float gv[4], uv[4];
-                unpack4(gq, gv);
-                unpack4(uq, uv);
                 if constexpr (CLAMP) {
+                    if (clamp2) {
+                        // c is a bf16 value: clamp and count on the packed pairs
+                        // (at most 4 per half and row: 32 per tile)
+                        n2 += clamp_pairs_bf16(gq.x, uq.x, clamp2);
+                        n2 += clamp_pairs_bf16(gq.y, uq.y, clamp2);
+                        unpack4(gq, gv);
+                        unpack4(uq, uv);
+                    } else {
+                        unpack4(gq, gv);
+                        unpack4(uq, uv);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        n_clamped += (gv[k] > clamp) + (fabsf(uv[k]) > clamp);
-                        gv[k] = fminf(gv[k], clamp);
-                        uv[k] = fmaxf(fminf(uv[k], clamp), -clamp);
+                        for (int k = 0; k < 4; ++k) {
+                            n1 += (gv[k] > clamp) + (fabsf(uv[k]) > clamp);
+                            gv[k] = fminf(gv[k], clamp);
+                            uv[k] = fmaxf(fminf(uv[k], clamp), -clamp);
+                        }
                     }
+                } else {
+                    unpack4(gq, gv);
+                    unpack4(uq, uv);
                 }
 #pragma unroll
                 for (int k = 0; k < 4; k += 2) {
@@ -169,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     y[r][k + 1] = p.y;
                 }
             }
+            if constexpr (CLAMP) n_clamped += (n2 & 0xFFFFu) + (n2 >> 16) + n1;
         }
 
         // ---- column maxima over this thread's 8 tokens -> shared table ----
@@ -314,7 +332,8 @@ cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* ou
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,
                                         static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H),
-                                        clamp, clamp_count, device_status_word());
+                                        clamp, CLAMP ? bf16x2_bound(clamp) : 0u, clamp_count,
+                                        device_status_word());
     return cudaGetLastError();
 }
 

@@ -9,6 +9,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace tkq {
@@ -266,6 +268,47 @@ __device__ __forceinline__ float swiglu(float g, float u) {
     const float e = ex2_approx(__fmul_rn(g, -1.4426950408889634f));
     const float den = __fadd_rn(1.0f, e);
     return __fmul_rn(__fmul_rn(g, rcp_approx(den)), u);
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU clamp (gate <= c, -c <= up <= c) on packed bf16 pairs
+// ---------------------------------------------------------------------------
+// When the bound c is itself a bf16 value the clamp can run on the raw input
+// pairs before they are widened, two elements per instruction: min / max
+// return one of their operands (the other one when an operand is NaN, as
+// fminf / fmaxf do), so they give exactly the values the fp32 clamp gives on
+// the exact widening; and an input differs from its clamped copy under the
+// ordered compare (false for NaN, as g > c and |u| > c are) exactly when it
+// lies beyond the bound.
+
+// c in both halves of a word, or 0 when c (finite, > 0) is not a bf16 value.
+__host__ __device__ inline uint32_t bf16x2_bound(float c) {
+    uint32_t b;
+    memcpy(&b, &c, sizeof b);
+    return (b & 0xFFFFu) ? 0u : (b >> 16) * 0x00010001u;
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) {
+    return *reinterpret_cast<const __nv_bfloat162*>(&w);
+}
+__device__ __forceinline__ uint32_t as_word(__nv_bfloat162 v) {
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Clamps the gate pair g and the up pair u in place (c2 = bf16x2_bound(c));
+// returns the number of changed values of each half in that half (0, 1 or 2).
+// The up clamp is one min.xorsign.abs: magnitude min(|u|, c), sign of u xor
+// sign of c (+), which is clamp(u, -c, c) for every u that is not NaN,
+// signed zeros and infinities included.
+__device__ __forceinline__ uint32_t clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint32_t c2) {
+    const __nv_bfloat162 gb = as_bf162(g), ub = as_bf162(u);
+    const __nv_bfloat162 gc = __hmin2(gb, as_bf162(c2));
+    uint32_t uw;
+    asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(uw) : "r"(u), "r"(c2));
+    const __nv_bfloat162 uc = as_bf162(uw);
+    g = as_word(gc);
+    u = uw;
+    return (__hne2_mask(gb, gc) & 0x00010001u) + (__hne2_mask(ub, uc) & 0x00010001u);
 }
 
 // Gradient of y = silu(g) * u with respect to g and u, scaled by the upstream

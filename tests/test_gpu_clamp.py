@@ -81,7 +81,9 @@ def run_clamp(x_bits, w, fmt, clamp, dev, transposed=False, count=None, sf_flags
             int(cnt.item()))
 
 
-@pytest.mark.parametrize("clamp", [0.5, 3.0])
+# Bounds that are bf16 values take the packed-bf16 clamp; 0.7 and 2.9 are not
+# bf16 values and take the fp32 clamp.
+@pytest.mark.parametrize("clamp", [0.5, 3.0, 0.7, 2.9])
 @pytest.mark.parametrize("weighted", [False, True])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("T,H", [(1, 128), (1031, 384)])
@@ -107,20 +109,21 @@ def test_clamped_swiglu_full_workload(cuda_device):
                                             q_rows(x, None, 4.0, e_sf), "e4m3")
 
 
+@pytest.mark.parametrize("clamp", [2.0, 1.3])
 @pytest.mark.parametrize("weighted", [False, True])
 @pytest.mark.parametrize("T,H", [(128, 128), (1024, 384)])
-def test_clamped_swiglu_cast_t(cuda_device, weighted, T, H):
+def test_clamped_swiglu_cast_t(cuda_device, clamp, weighted, T, H):
     x = synth.swiglu_bf16(73, T + H, T, H, gate_std=2.0)
     w = synth.routing_weights(74, T, T // 8) if weighted else None
-    o, s, ot, st, n = run_clamp(x, w, "e4m3", 2.0, cuda_device, transposed=True)
-    eo, es, eot, est, e_n = oracle.swiglu_cast_t(x, w, "e4m3", threads=THREADS, clamp=2.0)
+    o, s, ot, st, n = run_clamp(x, w, "e4m3", clamp, cuda_device, transposed=True)
+    eo, es, eot, est, e_n = oracle.swiglu_cast_t(x, w, "e4m3", threads=THREADS, clamp=clamp)
     assert n == e_n
     parity.assert_scales_close("sf", s, es)
-    parity.assert_codes_differ_only_at_ties("codes", o, eo, q_rows(x, w, 2.0, es), "e4m3")
+    parity.assert_codes_differ_only_at_ties("codes", o, eo, q_rows(x, w, clamp, es), "e4m3")
     parity.assert_scales_close("sf_t", st, est)
-    parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, w, 2.0, est), "e4m3")
+    parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, w, clamp, est), "e4m3")
     # the row outputs equal the clamped row cast's bit for bit
-    o2, s2, n2 = run_clamp(x, w, "e4m3", 2.0, cuda_device)
+    o2, s2, n2 = run_clamp(x, w, "e4m3", clamp, cuda_device)
     parity.assert_bit_exact("rows", o, o2)
     parity.assert_bit_exact("row scales", s, s2.view(np.float32).reshape(s.shape))
     assert n2 == n
@@ -172,3 +175,45 @@ def test_clamp_with_column_major_scales(cuda_device):
     cm = s1.view(np.float32).reshape(H // 128, T4)
     assert n0 == n1 and np.array_equal(c0, c1)
     assert np.array_equal(cm[:, :T], rm.T) and np.all(cm[:, T:] == 0)
+
+
+def _bf16_neighbours(c):
+    """bf16 bit patterns at and around the bound c (> 0): the largest bf16
+    value below c, c itself when it is a bf16 value, and the smallest above."""
+    b = int(np.float32(c).view(np.uint32))
+    lo = b >> 16
+    if b & 0xFFFF:
+        return [lo, lo + 1]
+    return [lo - 1, lo, lo + 1]
+
+
+# 2.0 and 448.0 are bf16 values (packed-bf16 clamp); 2.0 + 2^-20 and 0.3 are
+# not (fp32 clamp).  NaN inputs are outside the contract and not drawn.
+@pytest.mark.parametrize("clamp", [2.0, 448.0, 2.0 + 2.0 ** -20, 0.3])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_clamp_at_special_values(cuda_device, clamp, weighted):
+    """Gates and ups drawn from infinities, the largest finite bf16, signed
+    zeros, and the bf16 values at and next to +-c: the count is exact and the
+    outputs match the oracle (row and transposed casts)."""
+    near = _bf16_neighbours(clamp)
+    gates = np.array([0x7F80, 0x7F7F, 0x3F80, 0x0000, 0x8000, 0xC0A0, 0xC2C8]
+                     + near + [n | 0x8000 for n in near], np.uint16)
+    ups = np.array([0x7F80, 0xFF80, 0x7F7F, 0xFF7F, 0x0000, 0x8000, 0x3F00]
+                   + near + [n | 0x8000 for n in near], np.uint16)
+    rng = np.random.default_rng(int(clamp * 1000) + weighted)
+    T, H = 256, 256
+    x = np.concatenate([rng.choice(gates, (T, H)), rng.choice(ups, (T, H))], axis=1)
+    x = np.ascontiguousarray(x.astype(np.uint16))
+    w = synth.routing_weights(77, T, T // 8) if weighted else None
+    codes, sf_raw, n = run_clamp(x, w, "e4m3", clamp, cuda_device)
+    e_codes, e_sf, e_n = oracle.swiglu_cast(x, w, "e4m3", threads=THREADS, clamp=clamp)
+    assert n == e_n > 0
+    parity.assert_scales_close("sf", sf_raw.view(np.float32).reshape(T, H // 128), e_sf)
+    parity.assert_codes_differ_only_at_ties("codes", codes, e_codes, q_rows(x, w, clamp, e_sf),
+                                            "e4m3")
+    o, s, ot, st, n_t = run_clamp(x, w, "e4m3", clamp, cuda_device, transposed=True)
+    eo, es, eot, est, _ = oracle.swiglu_cast_t(x, w, "e4m3", threads=THREADS, clamp=clamp)
+    assert n_t == e_n
+    parity.assert_bit_exact("rows", o, codes)
+    parity.assert_scales_close("sf_t", st, est)
+    parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, w, clamp, est), "e4m3")
