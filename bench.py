@@ -680,6 +680,7 @@ def other_workloads(dev, stream, peak, args):
     out = {}
     for name, fmt, flags in [("plain_small", "e4m3", 0), ("plain_outlier", "e4m3", 0),
                              ("plain_outlier", "e5m2", 0), ("plain_outlier", "e4m3", 6),
+                             ("plain_outlier", "e4m3", 8),
                              ("swiglu", "e4m3", 0), ("swiglu_moe", "e4m3", 0),
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
@@ -690,7 +691,7 @@ def other_workloads(dev, stream, peak, args):
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
         gbs = prob.bytes / t / 1e9
-        key = f"{name}/{fmt}" + ("/ue8m0-col-major-sf" if flags == 6 else "")
+        key = f"{name}/{fmt}" + {0: "", 6: "/ue8m0-col-major-sf", 8: "/sf-inv"}[flags]
         out[key] = {"kernel": prob.kern, "us": round(t * 1e6, 2),
                                 "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                                 "rows_per_s": round(prob.T / t, 1), "bytes": prob.bytes}

@@ -193,6 +193,7 @@ def tkq_cast_back(codes, sf, out, T, C, group_rows=1, group_cols=GROUP, fmt=FMT_
 SF_ROUND_POW2 = 1
 SF_UE8M0_PACKED = 2
 SF_COL_MAJOR = 4
+Q_RECIPROCAL = 8   # plain casts: codes of x * fl32(1/s) instead of fl32(x/s)
 
 
 def tkq_sf_bytes(T, groups_per_row, sf_flags=0) -> int:
@@ -299,15 +300,18 @@ def _check_weights(topk_weights, T, x):
 
 def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_sf=None,
                    round_sf: bool = False, use_packed_ue8m0: bool = False,
-                   use_tma_aligned_col_major_sf: bool = False):
+                   use_tma_aligned_col_major_sf: bool = False, use_sf_inv: bool = False):
     """bf16 or fp32 [T, C] -> (FP8 codes [T, C], scales).  Scales are fp32
     [T, C/128] unless a scale-layout option is set (see ``sf_tensor`` for the
-    shapes)."""
+    shapes).  Codes are those of the exact quotient x / s, or with
+    ``use_sf_inv`` those of the product x * fl32(1 / s) (TKQ_Q_RECIPROCAL)."""
     import torch
     _check_input(x, allow_f32=True)
     f = _fmt_code(fmt)
     T, C = x.shape
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
+    if use_sf_inv:
+        flags |= Q_RECIPROCAL
     if out is None:
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:

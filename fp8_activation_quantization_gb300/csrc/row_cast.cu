@@ -71,11 +71,12 @@ struct alignas(1024) RowSmem {
 // Where the scales of a launch go (tkq_sf_layout flags; see tkq.h).
 struct SfLayout {
     unsigned flags;  // TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR
+                     // | TKQ_Q_RECIPROCAL
     int groups;      // groups per row (G)
     int words;       // ceil(G / 4), packed layouts
     int64_t rows4;   // T rounded up to a multiple of 4, column-major layouts
 };
-constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u;
+constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u, kQReciprocal = 8u;
 
 // Scale of group gj of `row` in the chosen layout.  Padding rows of the
 // column-major layouts (T <= row < rows4) get 0, and the unused bytes of a
@@ -103,7 +104,9 @@ __device__ __forceinline__ void store_scale(void* sf, const SfLayout& lay, int64
 // and the codes and scale stored for a live row.  EXACT selects the codes of
 // the exact quotient (plain cast) or of the product by the reciprocal scale.
 // SFX: the launch uses scale-layout options (power-of-two scales, packed
-// UE8M0, column-major); without it the scales are row-major fp32 at sfp.
+// UE8M0, column-major) or the reciprocal reading of the plain cast's codes
+// (products by fl32(1/s) instead of exact quotients); without it the scales
+// are row-major fp32 at sfp.
 template <int FMT, bool EXACT, bool SFX>
 __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, float* sfp,
                                            int j, void* sf, const SfLayout& lay, int64_t row,
@@ -116,6 +119,7 @@ __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, 
     group_scale<FMT>(m, sc, inv);
     bool exact_div = EXACT;
     if constexpr (SFX) {
+        if (lay.flags & kQReciprocal) exact_div = false;
         if (lay.flags & (kSfRoundPow2 | kSfPacked)) {
             // round the scale up to a power of two; y / s = y * 2^-k is then
             // exact, so the product needs no correction

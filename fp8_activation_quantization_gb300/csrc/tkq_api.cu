@@ -199,7 +199,8 @@ tkq_status check_common(int64_t T, int64_t C, int group, int fmt) {
 
 tkq_status launch_status(cudaError_t e) { return e == cudaSuccess ? TKQ_OK : TKQ_ERR_CUDA; }
 
-constexpr unsigned kSfAllFlags = TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR;
+constexpr unsigned kSfAllFlags =
+    TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR | TKQ_Q_RECIPROCAL;
 
 }  // namespace
 

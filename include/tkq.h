@@ -141,12 +141,23 @@ tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf
  * W = ceil(G/4), sf is
  *   fp32 [T, G] (no flags), fp32 [G, T4] (COL_MAJOR),
  *   int32 [T, W] (UE8M0_PACKED), int32 [W, T4] (UE8M0_PACKED | COL_MAJOR);
- * bytes of a row's last word beyond group G-1 are 0.  Unknown bits give
- * TKQ_ERR_FLAGS.
+ * bytes of a row's last word beyond group G-1 are 0.
+ * One more flag, which does not change the scales or their layout, selects
+ * the quotient reading of the plain per-token casts (tkq_per_token_cast_ex,
+ * tkq_per_token_cast_f32):
+ *   TKQ_Q_RECIPROCAL     codes of fl32(x * fl32(1 / s)), the product by the
+ *                        correctly rounded reciprocal of the scale ([P2] §3.2:
+ *                        the kernel multiplies by sf_inv), instead of the
+ *                        exact quotient fl32(x / s).  Bit-exact against the
+ *                        same reading of the definition.  With power-of-two
+ *                        scales the readings agree.  The SwiGLU casts always
+ *                        multiply this way, so there the flag changes nothing.
+ * Unknown bits give TKQ_ERR_FLAGS.
  */
 #define TKQ_SF_ROUND_POW2 1u
 #define TKQ_SF_UE8M0_PACKED 2u
 #define TKQ_SF_COL_MAJOR 4u
+#define TKQ_Q_RECIPROCAL 8u
 
 /* Size in bytes of the scale buffer for T rows of groups_per_row groups under
  * sf_flags, or -1 for invalid arguments. */

@@ -423,6 +423,8 @@ def swiglu_backward_cast(x_bits: np.ndarray, dy_bits: np.ndarray, w: np.ndarray 
 SF_ROUND_POW2 = 1
 SF_UE8M0_PACKED = 2
 SF_COL_MAJOR = 4
+# codes of fl32(v * fl32(1 / s)) instead of fl32(v / s); scales unchanged
+Q_RECIPROCAL = 8
 
 
 def pow2_ceil(s: float) -> np.float32:

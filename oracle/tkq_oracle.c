@@ -157,6 +157,19 @@ static void encode_group(const float* v, int64_t n, int64_t stride, float s, int
     }
 }
 
+/* The reciprocal-multiply reading: the code of each value is the code of the
+ * binary32 product v * fl32(1 / s) ("DeepSeek开源TileKernels：用Python写的GPU算子
+ * 逼近硬件性能上限" §3.2: the kernel multiplies by sf_inv; its computation is not
+ * shown, read here as the correctly rounded reciprocal). */
+static void encode_group_reciprocal(const float* v, int64_t n, float s, int fmt,
+                                    uint8_t* codes) {
+    const float inv = 1.0f / s;
+    for (int64_t i = 0; i < n; ++i) {
+        const float q = v[i] * inv;
+        codes[i] = ora_fp8_encode(q, fmt);
+    }
+}
+
 /* One group of n values at stride `stride` -> scale + codes. */
 static float cast_group(const float* v, int64_t n, int64_t stride, int fmt,
                         uint8_t* codes, int64_t code_stride) {
@@ -347,8 +360,9 @@ int64_t ora_sf_bytes(int64_t T, int64_t G, int flags) {
 int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, int fmt,
                          int flags, uint8_t* out, void* sf) {
     fp8_desc d;
-    if (get_desc(fmt, &d) || T < 0 || C < 0 || group <= 0 || C % group || (flags & ~7))
+    if (get_desc(fmt, &d) || T < 0 || C < 0 || group <= 0 || C % group || (flags & ~15))
         return -1;
+    const int reciprocal = (flags & ORA_Q_RECIPROCAL) != 0;
     const int packed = (flags & ORA_SF_UE8M0_PACKED) != 0;
     const int pow2 = packed || (flags & ORA_SF_ROUND_POW2);
     const int cm = (flags & ORA_SF_COL_MAJOR) != 0;
@@ -361,7 +375,10 @@ int ora_cast_rows_f32_ex(const float* y, int64_t T, int64_t C, int64_t group, in
             const float* v = y + t * C + j * group;
             float s = ora_group_scale(group_absmax(v, group, 1), fmt);
             if (pow2) s = ora_pow2_ceil(s);
-            encode_group(v, group, 1, s, fmt, out + t * C + j * group, 1);
+            if (reciprocal)
+                encode_group_reciprocal(v, group, s, fmt, out + t * C + j * group);
+            else
+                encode_group(v, group, 1, s, fmt, out + t * C + j * group, 1);
             if (packed) {
                 uint32_t bits;
                 memcpy(&bits, &s, sizeof bits);

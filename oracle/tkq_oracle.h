@@ -138,8 +138,16 @@ int ora_swiglu_cast_t_clamp(const uint16_t* x, const float* w, int64_t T, int64_
  * Layouts of sf (G groups per row, W = ceil(G / 4) words):
  *   default            fp32 [T, G]          ORA_SF_COL_MAJOR          fp32 [G, T4]
  *   ORA_SF_UE8M0_PACKED int32 [T, W]        UE8M0_PACKED|COL_MAJOR   int32 [W, T4]
- * Packed bytes of groups >= G in a row's last word are 0. */
-enum { ORA_SF_ROUND_POW2 = 1, ORA_SF_UE8M0_PACKED = 2, ORA_SF_COL_MAJOR = 4 };
+ * Packed bytes of groups >= G in a row's last word are 0.
+ * One more flag selects the quotient reading of the codes:
+ *   ORA_Q_RECIPROCAL    codes of fl32(v * fl32(1 / s)), the product by the
+ *                       correctly rounded reciprocal of the scale (the
+ *                       TileKernels kernel multiplies by sf_inv: [P2] §3.2),
+ *                       instead of the quotient fl32(v / s).  The scales and
+ *                       their layout are unchanged; with power-of-two scales
+ *                       the two readings agree. */
+enum { ORA_SF_ROUND_POW2 = 1, ORA_SF_UE8M0_PACKED = 2, ORA_SF_COL_MAJOR = 4,
+       ORA_Q_RECIPROCAL = 8 };
 
 /* Power of two >= s (s a positive normal binary32): 2^ceil(log2 s). */
 float ora_pow2_ceil(float s);

@@ -117,11 +117,13 @@ def test_sf_bytes(lib):
     assert lib.tkq_sf_bytes(13, 7, 2) == 13 * 2 * 4
     assert lib.tkq_sf_bytes(13, 7, 6) == 2 * 16 * 4
     assert lib.tkq_sf_bytes(13, 7, 1) == 13 * 7 * 4
-    assert lib.tkq_sf_bytes(13, 7, 8) == -1 and lib.tkq_sf_bytes(-1, 7, 0) == -1
+    # the reciprocal reading leaves the layout alone
+    assert lib.tkq_sf_bytes(13, 7, 8) == 13 * 7 * 4 and lib.tkq_sf_bytes(13, 7, 14) == 2 * 16 * 4
+    assert lib.tkq_sf_bytes(13, 7, 16) == -1 and lib.tkq_sf_bytes(-1, 7, 0) == -1
 
 
 @pytest.mark.parametrize("flags,sf_off,expected", [
-    (8, 0, 8),            # unknown flag bit
+    (16, 0, 8),           # unknown flag bit
     (4, 4, 5),            # column-major scales must be 16-byte aligned
     (6, 8, 5),            # packed column-major too
     (2, 2, 5),            # packed row-major: 4-byte aligned
@@ -133,7 +135,8 @@ def test_ex_validation(lib, flags, sf_off, expected):
 
 def test_ex_empty_batch_and_flags(lib):
     assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 6, None) == 0
-    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 9, None) == 8
+    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 9, None) == 0
+    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 17, None) == 8
     assert lib.tkq_swiglu_cast_ex(None, None, None, None, 0, 256, 128, 0, 16, None) == 8
     assert lib.tkq_swiglu_backward_cast_ex(None, None, None, None, None, 0, 256, 128, 0, 4,
                                            None) == 0
@@ -228,7 +231,7 @@ def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
     ((p(), p(1 << 20), p(2 << 20), 4, 200, 128, 0, 0), 2),             # C % 128
     ((p(), p(1 << 20), p(2 << 20), 4, 256, 64, 0, 0), 3),              # group
     ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 7, 0), 4),             # fmt
-    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 8), 8),             # flags
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 16), 8),            # flags
     ((p(4), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 0), 5),            # x misaligned
     ((p(), p(2048), p(2 << 20), 4, 256, 128, 0, 0), 7),                # out inside x (4 B/elem)
     ((None, None, None, 0, 256, 128, 0, 0), 0),                        # empty batch

@@ -406,7 +406,8 @@ def test_swiglu_backward_tensor_api(cuda_device):
 # scale-factor layouts
 # ---------------------------------------------------------------------------
 
-SF_FLAG_SETS = [0, 1, 2, 4, 5, 6]
+# 8 = TKQ_Q_RECIPROCAL: codes of the product by fl32(1/s) (scales unchanged)
+SF_FLAG_SETS = [0, 1, 2, 4, 5, 6, 8, 12, 14]
 
 
 def sf_rowmajor(raw: np.ndarray, T: int, G: int, flags: int) -> np.ndarray:
@@ -468,6 +469,48 @@ def test_plain_cast_sf_layouts_bit_exact(cuda_device, flags, fmt):
     parity.assert_bit_exact("scales (raw layout bytes)", raw, rs.view(np.uint8).ravel())
 
 
+def test_plain_cast_hand_groups_reciprocal(cuda_device):
+    """TKQ_Q_RECIPROCAL on the hand-worked groups: the two quotient-tie groups
+    give their hand-worked reciprocal codes (0xf3, 0xfb instead of 0xf2, 0xfa);
+    groups with a power-of-two scale keep the quotient's codes."""
+    spec = json.load(open(os.path.join(GOLDEN, "hand_groups.json")))
+    seen = 0
+    for case in spec["cases"]:
+        vals = np.full(128, case["fill"], np.float32)
+        for k, v in case["set"].items():
+            vals[int(k)] = np.float32(v)
+        x = synth.f32_to_bf16_bits(vals).reshape(1, 128)
+        out, raw, _ = run_ex("plain", x, 8, case["fmt"], cuda_device)
+        assert hex(int(raw.view(np.uint32)[0])) == case["scale_hex"], case["name"]
+        if "codes_reciprocal" in case:
+            want = case["codes_reciprocal"]
+            seen += 1
+        elif int(case["scale_hex"], 16) & 0x007FFFFF == 0:
+            want = case["codes"]
+        else:
+            continue
+        exp = np.full(128, int(case["code_fill"], 16), np.uint8)
+        for k, c in want.items():
+            exp[int(k)] = int(c, 16)
+        parity.assert_bit_exact(case["name"], out[0], exp)
+    assert seen == 2
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_plain_cast_reciprocal_full_workload(cuda_device, fmt):
+    """The full plain_outlier workload with TKQ_Q_RECIPROCAL, through the tensor
+    API (use_sf_inv): codes and scales bit-exact against the oracle's
+    reciprocal reading, and some codes differ from the quotient reading."""
+    x = synth.workload("plain_outlier")["x"]
+    xd = to_dev_bf16(x, cuda_device)
+    q, s = tkq.per_token_cast(xd, fmt, use_sf_inv=True)
+    ro, rs = oracle.per_token_cast_ex(x, fmt, 128, oracle.Q_RECIPROCAL, threads=THREADS)
+    parity.assert_bit_exact("codes", q.view(torch.uint8).cpu().numpy(), ro)
+    parity.assert_bit_exact("scales", s.cpu().numpy(), rs)
+    q2, _ = tkq.per_token_cast(xd, fmt)
+    assert not torch.equal(q.view(torch.uint8), q2.view(torch.uint8))
+
+
 def _pow2_boundary(s0: np.ndarray, tol=2e-6) -> np.ndarray:
     """Groups whose plain scale lies within tol (relative) of a power of two:
     a few ulp of SwiGLU error can move their rounded-up scale by one binade."""
@@ -476,7 +519,7 @@ def _pow2_boundary(s0: np.ndarray, tol=2e-6) -> np.ndarray:
 
 
 @pytest.mark.parametrize("kind", ["swiglu", "backward"])
-@pytest.mark.parametrize("flags", [1, 2, 4, 6])
+@pytest.mark.parametrize("flags", [1, 2, 4, 6, 8])
 def test_swiglu_sf_layouts(cuda_device, kind, flags):
     if kind == "swiglu":
         d = synth.workload("swiglu_moe", rows=1031)

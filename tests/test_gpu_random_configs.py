@@ -22,7 +22,7 @@ from tests.test_gpu_parity import to_dev_bf16
 pytestmark = pytest.mark.gpu
 
 THREADS = max(1, min(16, os.cpu_count() or 1))
-FLAGS = [0, 1, 2, 4, 5, 6, 7]
+FLAGS = [0, 1, 2, 4, 5, 6, 7, 8, 12, 15]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,7 +35,7 @@ def _library(cuda_device):
 
 def _opts(flags):
     return dict(round_sf=bool(flags & 1), use_packed_ue8m0=bool(flags & 2),
-                use_tma_aligned_col_major_sf=bool(flags & 4))
+                use_tma_aligned_col_major_sf=bool(flags & 4), use_sf_inv=bool(flags & 8))
 
 
 def _raw(t):

@@ -66,6 +66,9 @@ MUTANTS = [
     ("clamp: clamped ups not counted", "if (u > cv) { u = cv; ++n; }", "if (u > cv) { u = cv; }"),
     ("clamp: values at the bound counted", "if (g > cv) { g = cv; ++n; }",
      "if (g >= cv) { g = cv; ++n; }"),
+    ("reciprocal reading ignored", "            if (reciprocal)\n", "            if (0)\n"),
+    ("reciprocal reading multiplies by s", "const float q = v[i] * inv;",
+     "const float q = v[i] * s;"),
     ("cast back ignores the column group", "const float s = sf[(t / gr) * G + c / gc];",
      "const float s = sf[(t / gr) * G];"),
 ]
@@ -81,6 +84,7 @@ CHECKS = [
     (pins.test_swiglu_vs_binary64, {}),
     (pins.test_swiglu_backward_special_cases, {}),
     (pins.test_round_pow2_hand_group, {}),
+    (pins.test_reciprocal_reading_hand_groups, {}),
     (pins.test_swiglu_clamp_hand_values, {}),
     (pins.test_cast_back_hand_values_and_granularities, {}),
     (pins.test_per_channel_is_per_token_of_transpose, {"fmt": "e4m3"}),

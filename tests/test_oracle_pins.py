@@ -600,6 +600,65 @@ def test_round_pow2_hand_group():
     assert s.dtype == np.uint32 and s[0, 0] == 127 - 7   # one group: byte 0 only
 
 
+def test_reciprocal_reading_hand_groups():
+    """The reciprocal-multiply reading (codes of fl32(v * fl32(1 / s))): the two
+    quotient-tie groups give their hand-worked codes_reciprocal (one step away
+    from the quotient's codes); every group whose scale is a power of two,
+    where the product by the reciprocal is the exact quotient, keeps the
+    quotient's codes; the scales never change."""
+    spec = json.load(open(os.path.join(GOLDEN, "hand_groups.json")))
+    G = spec["group"]
+    seen = 0
+    for case in spec["cases"]:
+        vals = np.full(G, case["fill"], np.float32)
+        for k, v in case["set"].items():
+            vals[int(k)] = np.float32(v)
+        y = vals.reshape(1, G)
+        codes, sf = oracle.cast_rows_f32_ex(y, case["fmt"], G, oracle.Q_RECIPROCAL)
+        assert hex(int(sf.view(np.uint32)[0, 0])) == case["scale_hex"], case["name"]
+        scale_bits = int(case["scale_hex"], 16)
+        if "codes_reciprocal" in case:
+            want = case["codes_reciprocal"]
+            seen += 1
+        elif scale_bits & 0x007FFFFF == 0:
+            want = case["codes"]
+        else:
+            continue
+        exp = np.full(G, int(case["code_fill"], 16), np.uint8)
+        for k, c in want.items():
+            exp[int(k)] = int(c, 16)
+        bad = np.nonzero(codes[0] != exp)[0]
+        assert bad.size == 0, (case["name"], [(int(i), hex(codes[0, i]), hex(exp[i])) for i in bad])
+    assert seen == 2
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_reciprocal_reading_properties(fmt):
+    """On seeded data: with power-of-two scales both readings give the same
+    codes; otherwise a code differs from the quotient's by at most one FP8 step
+    (the product is within about one binary32 ulp of the quotient), and the
+    scales are those of the quotient reading."""
+    y = _layout_inputs(T=64, G=8, seed=71)
+    c_q, s_q = oracle.cast_rows_f32_ex(y, fmt, 128, 0)
+    c_r, s_r = oracle.cast_rows_f32_ex(y, fmt, 128, oracle.Q_RECIPROCAL)
+    assert np.array_equal(s_q, s_r)
+    # one step: adjacent codes of the same sign (the byte order of FP8 codes
+    # follows the magnitude within a sign)
+    same_sign = (c_q & 0x80) == (c_r & 0x80)
+    step = np.abs((c_q & 0x7F).astype(int) - (c_r & 0x7F).astype(int))
+    assert np.all(same_sign | ((c_q & 0x7F) == 0) & ((c_r & 0x7F) == 0))
+    assert step.max() <= 1
+    for flags in (oracle.SF_ROUND_POW2, oracle.SF_UE8M0_PACKED | oracle.SF_COL_MAJOR):
+        c1, s1 = oracle.cast_rows_f32_ex(y, fmt, 128, flags)
+        c2, s2 = oracle.cast_rows_f32_ex(y, fmt, 128, flags | oracle.Q_RECIPROCAL)
+        assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+
+
+def test_unknown_flag_is_rejected():
+    with pytest.raises(Exception):
+        oracle.cast_rows_f32_ex(np.zeros((1, 128), np.float32), "e4m3", 128, 16)
+
+
 def _layout_inputs(T=13, G=7, seed=67):
     rng = np.random.default_rng(seed)
     return (rng.standard_normal((T, G * 128)) * np.exp2(rng.integers(-6, 6, (T, G * 128))
