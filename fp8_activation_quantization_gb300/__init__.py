@@ -27,6 +27,7 @@ __all__ = [
     "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
     "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
+    "use_checked_library", "tkq_checked_build", "tkq_read_check_address",
 ]
 
 FMT_E4M3 = 0
@@ -36,8 +37,11 @@ _FMTS = {"e4m3": FMT_E4M3, "e5m2": FMT_E5M2}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libtkq.so")
-_lock = threading.Lock()
-_lib = None
+# the access-checked test build of the same sources (see include/tkq.h)
+_LIB_CHECKED_PATH = os.path.join(_HERE, "_lib", "libtkq_checked.so")
+_lock = threading.RLock()
+_lib = None          # the library every call of this module goes to
+_opened = {}         # path -> loaded library
 
 
 class TkqError(RuntimeError):
@@ -54,13 +58,35 @@ def load_library():
     """Load libtkq.so (built by ``__graft_entry__.build()``); raise if absent."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(_LIB_PATH):
+        if _lib is None:
+            _lib = _open(_LIB_PATH)
+        return _lib
+
+
+@contextlib.contextmanager
+def use_checked_library():
+    """Route this module's calls to the access-checked build libtkq_checked.so
+    (built by ``_build.build(checked=True)``) inside the ``with`` block."""
+    global _lib
+    with _lock:
+        prev = _lib
+        _lib = _open(_LIB_CHECKED_PATH)
+    try:
+        yield _lib
+    finally:
+        with _lock:
+            _lib = prev
+
+
+def _open(path):
+    with _lock:
+        if path in _opened:
+            return _opened[path]
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{_LIB_PATH} is missing: build the CUDA library first "
+                f"{path} is missing: build the CUDA library first "
                 "(python -c 'import __graft_entry__ as g; g.build()')")
-        lib = ctypes.CDLL(_LIB_PATH)
+        lib = ctypes.CDLL(path)
         p, i64, i = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.tkq_per_token_cast.argtypes = [p, p, p, i64, i64, i, i, p]
         lib.tkq_per_token_cast.restype = i
@@ -102,18 +128,38 @@ def load_library():
         lib.tkq_per_token_cast_f32.restype = i
         lib.tkq_swiglu_values.argtypes = [p, p, p, i64, i64, p]
         lib.tkq_swiglu_values.restype = i
-        _lib = lib
+        lib.tkq_checked_build.argtypes = []
+        lib.tkq_checked_build.restype = i
+        lib.tkq_read_check_address.argtypes = [ctypes.POINTER(ctypes.c_uint64), i]
+        lib.tkq_read_check_address.restype = i
+        _opened[path] = lib
         return lib
 
 
 DEVICE_TIMEOUT = 1
+DEVICE_OUT_OF_BOUNDS = 2
+
+
+def tkq_checked_build() -> bool:
+    return bool((_lib or load_library()).tkq_checked_build())
+
+
+def tkq_read_check_address(clear: bool = False) -> int:
+    """Synchronize the current device and return the first address an access
+    check refused (bit 63 set for a store; 0 if none, and always 0 in the
+    release build)."""
+    v = ctypes.c_uint64(0)
+    st = (_lib or load_library()).tkq_read_check_address(ctypes.byref(v), 1 if clear else 0)
+    if st:
+        raise TkqError(st, "tkq_read_check_address")
+    return int(v.value)
 
 
 def tkq_read_device_status(clear: bool = False) -> int:
     """Synchronize the current device and return its status word (bit
     DEVICE_TIMEOUT: a bounded wait inside a kernel gave up)."""
     v = ctypes.c_uint32(0)
-    st = load_library().tkq_read_device_status(ctypes.byref(v), 1 if clear else 0)
+    st = (_lib or load_library()).tkq_read_device_status(ctypes.byref(v), 1 if clear else 0)
     if st:
         raise TkqError(st, "tkq_read_device_status")
     return int(v.value)

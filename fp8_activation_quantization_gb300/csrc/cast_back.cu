@@ -102,11 +102,11 @@ __global__ void __launch_bounds__(kThreads, 3)
                     const float4* s4 = reinterpret_cast<const float4*>(srow + c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const float4 f = __ldg(s4 + i);
+                        const float4 f = ld_ro(s4 + i);
                         s[4 * i] = f.x; s[4 * i + 1] = f.y; s[4 * i + 2] = f.z; s[4 * i + 3] = f.w;
                     }
                 } else {
-                    const float one = __ldg(srow + c / GC);
+                    const float one = ld_ro(srow + c / GC);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) s[i] = one;
                 }
@@ -149,6 +149,7 @@ cudaError_t launch(const void* codes, const float* sf, void* out, int64_t T, int
     const int64_t unit_rows = static_cast<int64_t>(R) * kRowsPerThread;
     const int64_t n_units = (T + unit_rows - 1) / unit_rows;
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0, n_units);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kThreads, 0, stream>>>(static_cast<const uint8_t*>(codes), sf, out, T, C, R);
     return cudaGetLastError();
 }

@@ -90,13 +90,13 @@ __device__ __forceinline__ void store_scale(void* sf, const SfLayout& lay, int64
         const int64_t word = cm ? static_cast<int64_t>(gj >> 2) * lay.rows4 + row
                                 : row * lay.words + (gj >> 2);
         uint8_t* p = static_cast<uint8_t*>(sf) + word * 4;
-        p[gj & 3] = byte;
+        st_plain(p + (gj & 3), byte);
         if (gj == lay.groups - 1)
-            for (int k = (gj & 3) + 1; k < 4; ++k) p[k] = 0;
+            for (int k = (gj & 3) + 1; k < 4; ++k) st_plain(p + k, uint8_t{0});
     } else {
         const int64_t idx = cm ? static_cast<int64_t>(gj) * lay.rows4 + row
                                : row * lay.groups + gj;
-        static_cast<float*>(sf)[idx] = live ? sc : 0.0f;
+        st_plain(static_cast<float*>(sf) + idx, live ? sc : 0.0f);
     }
 }
 
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 
         float wt = 1.0f;
         if constexpr (MT::kWeighted) {
-            if (live) wt = __ldg(w + row);
+            if (live) wt = ld_ro(w + row);
         }
 
         // the warp leaves as a whole if any lane's wait gave up, so that no
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         unsigned long long t = n_clamped;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0 && t && clamp.count) atomicAdd(clamp.count, t);
+        if (lane == 0 && t && clamp.count) atomic_add_count(clamp.count, t);
     }
 }
 
@@ -375,6 +375,7 @@ cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& map_dy, const
     const size_t smem = sizeof(RowSmem<MODE>) + 1024;
     const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, lay, T,
                                         static_cast<int>(C_out), clamp, device_status_word());
     return cudaGetLastError();

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r) wt[r] = 1.0f;
         if constexpr (WEIGHTED) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r) wt[r] = __ldg(w + row0 + r);
+            for (int r = 0; r < 8; ++r) wt[r] = ld_ro(w + row0 + r);
         }
 
         const bool ok = mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status);
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long t = n_clamped;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if (lane == 0 && t && clamp_count) atomicAdd(clamp_count, t);
+        if (lane == 0 && t && clamp_count) atomic_add_count(clamp_count, t);
     }
 }
 
@@ -330,6 +330,7 @@ cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* ou
     const size_t smem = sizeof(SharedStorage) + 1024;
     const int64_t n_tiles = (T / 128) * (H / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,
                                         static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H),
                                         clamp, CLAMP ? bf16x2_bound(clamp) : 0u, clamp_count,

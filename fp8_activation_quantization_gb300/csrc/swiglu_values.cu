@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(kThreads)
         float g[8], u[8], r[8];
         unpack8(ld_stream(x + t * (2 * V) + v), g);
         unpack8(ld_stream(x + t * (2 * V) + V + v), u);
-        const float wt = WEIGHTED ? __ldg(w + t) : 1.0f;
+        const float wt = WEIGHTED ? ld_ro(w + t) : 1.0f;
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             float2 p = swiglu2(make_float2(g[k], g[k + 1]), make_float2(u[k], u[k + 1]));
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(kThreads)
             r[k] = p.x;
             r[k + 1] = p.y;
         }
-        y[2 * i] = make_float4(r[0], r[1], r[2], r[3]);
-        y[2 * i + 1] = make_float4(r[4], r[5], r[6], r[7]);
+        st_plain(y + 2 * i, make_float4(r[0], r[1], r[2], r[3]));
+        st_plain(y + 2 * i + 1, make_float4(r[4], r[5], r[6], r[7]));
     }
 }
 
@@ -54,6 +54,7 @@ cudaError_t launch_swiglu_values(const void* x, const float* w, float* y, int64_
     auto* k = w ? &swiglu_values_kernel<true> : &swiglu_values_kernel<false>;
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0,
                                      (n + kThreads - 1) / kThreads);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(x), w, reinterpret_cast<float4*>(y),
                                      T, H);
     return cudaGetLastError();

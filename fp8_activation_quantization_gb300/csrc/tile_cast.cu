@@ -178,6 +178,7 @@ cudaError_t launch_channel(const void* x, void* out, float* sf, int64_t T, int64
     const size_t smem = sizeof(ChSmem) + 1024;
     const int64_t n_tiles = (T / 128) * (C / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kChThreads, smem, n_tiles);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kChThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
                                           static_cast<int>(C), device_status_word());
     return cudaGetLastError();
@@ -480,6 +481,7 @@ cudaError_t launch_block(const void* x, void* out, float* sf, int64_t T, int64_t
     const int64_t n_tiles = ((T + 127) / 128) * (C / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
                                      (n_tiles + 1) / 2);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kCtThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
                                           static_cast<int>(C), device_status_word());
     return cudaGetLastError();
@@ -495,6 +497,7 @@ cudaError_t launch_channel_t(const void* x, void* out, float* sf, int64_t T, int
     const int64_t n_tiles = (T / 128) * (C / kCtTileCols);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
                                      (n_tiles + 1) / 2);
+    if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kCtThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
                                             static_cast<int>(C), device_status_word());
     return cudaGetLastError();

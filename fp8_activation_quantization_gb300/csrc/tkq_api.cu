@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <functional>
+#include <initializer_list>
 #include <mutex>
 #include <unordered_map>
 
@@ -20,6 +21,8 @@
 // into it (tkq::kDeviceTimeout when a bounded wait gave up); the host reads and
 // clears it with tkq_read_device_status.
 __device__ unsigned int g_tkq_device_status;
+// First address an access check refused (checked build; bit 63: a store).
+__device__ unsigned long long g_tkq_bad_address;
 
 namespace tkq {
 
@@ -27,6 +30,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];  // 0 = not yet queried
 std::atomic<unsigned int*> g_status_ptr[kMaxDevices];
+std::atomic<unsigned long long*> g_bad_ptr[kMaxDevices];
 
 // One CTA waits on an mbarrier that nothing ever arrives on, so its bounded
 // wait must give up after limit_ns and record a timeout in the status word.
@@ -134,7 +138,57 @@ unsigned int* device_status_word() {
     return static_cast<unsigned int*>(p);
 }
 
+CheckTable& host_check_table() {
+    thread_local CheckTable table{};
+    return table;
+}
+
 namespace {
+unsigned long long* bad_address_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+    if (dev < kMaxDevices) {
+        unsigned long long* p = g_bad_ptr[dev].load(std::memory_order_acquire);
+        if (p) return p;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tkq_bad_address) != cudaSuccess) return nullptr;
+    if (dev < kMaxDevices)
+        g_bad_ptr[dev].store(static_cast<unsigned long long*>(p), std::memory_order_release);
+    return static_cast<unsigned long long*>(p);
+}
+
+// The buffers of the call about to launch, for the checked build's access
+// checks (a no-op otherwise): inputs may be read, outputs read and written.
+// Empty ranges (an absent optional buffer) are skipped.  The environment
+// variable TKQ_CHECK_WITHHOLD=n (checked build only) leaves the last n bytes of
+// every output out of the table, so that the kernels' stores there are refused
+// and reported: the test of the checks themselves, with no access outside any
+// allocation.
+void register_call(std::initializer_list<Range> inputs, std::initializer_list<Range> outputs) {
+#ifdef TKQ_CHECKED
+    CheckTable& t = host_check_table();
+    t = CheckTable{};
+    uint64_t withhold = 0;
+    if (const char* env = std::getenv("TKQ_CHECK_WITHHOLD")) withhold = std::strtoull(env, nullptr, 10);
+    auto add = [&t](uintptr_t lo, uintptr_t hi, bool out) {
+        if (hi <= lo || t.n >= kCheckMax) return;
+        t.lo[t.n] = lo;
+        t.hi[t.n] = hi;
+        if (out) t.writable |= 1u << t.n;
+        ++t.n;
+    };
+    for (const Range& r : inputs) add(r.lo, r.hi, false);
+    for (const Range& r : outputs)
+        add(r.lo, r.hi - r.lo > withhold ? r.hi - withhold : r.lo, true);
+    t.status = device_status_word();
+    t.bad = bad_address_word();
+#else
+    (void)inputs;
+    (void)outputs;
+#endif
+}
+
 // Per (kernel, device, threads, smem): resident blocks per SM.  The first
 // launch on a device raises the kernel's dynamic shared-memory limit and asks
 // the occupancy calculator; later launches reuse the answer, which keeps both
@@ -236,6 +290,7 @@ tkq_status tkq_per_token_cast_ex(const void* x, void* out, void* sf, int64_t T, 
     const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
                rs = tkq::span(sf, tkq_sf_bytes(T, C / group, sf_flags));
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx}, {ro, rs});
     return launch_status(tkq::launch_per_token_cast(x, out, sf, T, C, fmt, sf_flags,
                                                     static_cast<cudaStream_t>(stream)));
 }
@@ -252,6 +307,7 @@ tkq_status tkq_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T
     const auto rx = tkq::span(x, T * C * 4), ro = tkq::span(out, T * C),
                rs = tkq::span(sf, tkq_sf_bytes(T, C / group, sf_flags));
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx}, {ro, rs});
     return launch_status(tkq::launch_per_token_cast_f32(x, out, sf, T, C, fmt, sf_flags,
                                                         static_cast<cudaStream_t>(stream)));
 }
@@ -295,6 +351,8 @@ tkq_status swiglu_cast_impl(const void* x, const float* w, void* out, void* sf, 
         const tkq::Range others[4] = {rx, ro, rs, rw};
         if ((st = check_clamp(*clamp, clamp_count, others, 4)) != TKQ_OK) return st;
     }
+    const auto rc = clamp && clamp_count ? tkq::span(clamp_count, 8) : tkq::Range{0, 0};
+    tkq::register_call({rx, rw}, {ro, rs, rc});
     return launch_status(tkq::launch_swiglu_cast(
         x, w, out, sf, T, H, fmt, sf_flags, clamp,
         reinterpret_cast<unsigned long long*>(clamp_count), static_cast<cudaStream_t>(stream)));
@@ -338,6 +396,7 @@ tkq_status tkq_swiglu_backward_cast_ex(const void* x, const void* dy, const floa
     if (tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
     for (const auto& in : inputs)
         if (tkq::overlap(in, ro) || tkq::overlap(in, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({inputs[0], inputs[1], inputs[2]}, {ro, rs});
     return launch_status(tkq::launch_swiglu_backward_cast(x, dy, w, out, sf, T, H, fmt, sf_flags,
                                                           static_cast<cudaStream_t>(stream)));
 }
@@ -376,6 +435,8 @@ tkq_status swiglu_cast_t_impl(const void* x, const float* w, void* out, float* s
         const tkq::Range others[6] = {r[0], r[1], r[2], r[3], r[4], rw};
         if ((st = check_clamp(*clamp, clamp_count, others, 6)) != TKQ_OK) return st;
     }
+    const auto rc = clamp && clamp_count ? tkq::span(clamp_count, 8) : tkq::Range{0, 0};
+    tkq::register_call({r[0], rw}, {r[1], r[2], r[3], r[4], rc});
     return launch_status(tkq::launch_swiglu_cast_t(
         x, w, out, sf, out_t, sf_t, T, H, fmt, clamp,
         reinterpret_cast<unsigned long long*>(clamp_count), static_cast<cudaStream_t>(stream)));
@@ -409,6 +470,7 @@ tkq_status tkq_per_channel_cast(const void* x, void* out, float* sf, int64_t T, 
     const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
                rs = tkq::span(sf, (T / group) * C * 4);
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx}, {ro, rs});
     return launch_status(tkq::launch_per_channel_cast(x, out, sf, T, C, fmt, transpose != 0,
                                                       static_cast<cudaStream_t>(stream)));
 }
@@ -424,6 +486,7 @@ tkq_status tkq_per_block_cast(const void* x, void* out, float* sf, int64_t T, in
     const auto rx = tkq::span(x, T * C * 2), ro = tkq::span(out, T * C),
                rs = tkq::span(sf, (T + block - 1) / block * (C / block) * 4);
     if (tkq::overlap(rx, ro) || tkq::overlap(rx, rs) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx}, {ro, rs});
     return launch_status(
         tkq::launch_per_block_cast(x, out, sf, T, C, fmt, static_cast<cudaStream_t>(stream)));
 }
@@ -446,9 +509,10 @@ tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t 
         return TKQ_ERR_ALIGN;
     const int64_t out_bytes = T * C * (out_dtype == TKQ_OUT_F32 ? 4 : 2);
     const int64_t sf_bytes = (T + group_rows - 1) / group_rows * (C / group_cols) * 4;
-    const auto ro = tkq::span(out, out_bytes);
-    if (tkq::overlap(ro, tkq::span(codes, T * C)) || tkq::overlap(ro, tkq::span(sf, sf_bytes)))
-        return TKQ_ERR_ALIAS;
+    const auto ro = tkq::span(out, out_bytes), rq = tkq::span(codes, T * C),
+               rs = tkq::span(sf, sf_bytes);
+    if (tkq::overlap(ro, rq) || tkq::overlap(ro, rs)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rq, rs}, {ro});
     return launch_status(tkq::launch_cast_back(codes, sf, out, T, C, group_rows, group_cols, fmt,
                                                out_dtype == TKQ_OUT_BF16,
                                                static_cast<cudaStream_t>(stream)));
@@ -465,6 +529,7 @@ tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T,
     const auto rx = tkq::span(x, T * H * 4), ry = tkq::span(y, T * H * 4);
     const auto rw = w ? tkq::span(w, T * 4) : tkq::Range{0, 0};
     if (tkq::overlap(rx, ry) || tkq::overlap(rw, ry)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx, rw}, {ry});
     return launch_status(
         tkq::launch_swiglu_values(x, w, y, T, H, static_cast<cudaStream_t>(stream)));
 }
@@ -510,5 +575,27 @@ const char* tkq_status_string(int status) {
 }
 
 int tkq_version(void) { return 100; }
+
+int tkq_checked_build(void) {
+#ifdef TKQ_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+tkq_status tkq_read_check_address(uint64_t* addr, int clear) {
+    if (!addr) return TKQ_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;
+    unsigned long long v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tkq_bad_address, sizeof v) != cudaSuccess) return TKQ_ERR_CUDA;
+    if (clear) {
+        const unsigned long long zero = 0;
+        if (cudaMemcpyToSymbol(g_tkq_bad_address, &zero, sizeof zero) != cudaSuccess)
+            return TKQ_ERR_CUDA;
+    }
+    *addr = v;
+    return TKQ_OK;
+}
 
 }  // extern "C"

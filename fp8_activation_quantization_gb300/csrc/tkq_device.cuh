@@ -13,6 +13,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "tkq_internal.h"
+
 namespace tkq {
 
 constexpr int kFmtE4M3 = 0;
@@ -32,39 +34,103 @@ struct FmtTraits<kFmtE5M2> {
 };
 
 // ---------------------------------------------------------------------------
+// access checking (checked build only)
+// ---------------------------------------------------------------------------
+// Built with -DTKQ_CHECKED, every global load and store of the kernels (all of
+// them go through the helpers below; TMA loads are bounded by their tensor
+// maps) first checks that the bytes it touches lie inside one of the buffers
+// of the current call: its inputs for a load, its outputs for a store.  The
+// ABI layer registers those buffers per call and each launcher copies the
+// table to its translation unit's copy on the launch stream before the launch.
+// An access outside them is skipped (no fault), sets kDeviceOutOfBounds in the
+// device status word and records the first such address (bit 63 set for a
+// store).  It stands in for a memory checker; the checked library is a test
+// build, one launch at a time (the table is shared by a translation unit's
+// launches).  In the release build the checks compile away.
+#ifdef TKQ_CHECKED
+static __device__ CheckTable g_check;  // this translation unit's copy
+
+inline cudaError_t upload_checks(cudaStream_t s) {
+    return cudaMemcpyToSymbolAsync(g_check, &host_check_table(), sizeof(CheckTable), 0,
+                                   cudaMemcpyHostToDevice, s);
+}
+#else
+inline cudaError_t upload_checks(cudaStream_t) { return cudaSuccess; }
+#endif
+
+__device__ __forceinline__ bool access_ok(const void* p, unsigned bytes, bool write) {
+#ifdef TKQ_CHECKED
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    for (int k = 0; k < g_check.n; ++k)
+        if (a >= g_check.lo[k] && a + bytes <= g_check.hi[k] &&
+            (!write || ((g_check.writable >> k) & 1u)))
+            return true;
+    if (g_check.status) atomicOr(g_check.status, kDeviceOutOfBounds);
+    if (g_check.bad) atomicCAS(g_check.bad, 0ull, a | (write ? (1ull << 63) : 0ull));
+    return false;
+#else
+    (void)p;
+    (void)bytes;
+    (void)write;
+    return true;
+#endif
+}
+
+// ---------------------------------------------------------------------------
 // memory access
 // ---------------------------------------------------------------------------
 
 // 16-byte streaming load of read-only input: not kept in L1 (each byte is read
 // once by this kernel).
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-    uint4 r;
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (!access_ok(p, 16, false)) return r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
     return r;
 }
 
-__device__ __forceinline__ float ld_stream_f32(const float* p) {
-    float r;
-    asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(r) : "l"(p));
-    return r;
+// Read-only loads through the non-coherent path (small per-row operands).
+__device__ __forceinline__ float ld_ro(const float* p) {
+    return access_ok(p, 4, false) ? __ldg(p) : 0.0f;
+}
+__device__ __forceinline__ float4 ld_ro(const float4* p) {
+    return access_ok(p, 16, false) ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Streaming stores (.cs: the output is not read again by this kernel).
 __device__ __forceinline__ void st_stream(uint2* p, uint2 v) {
+    if (!access_ok(p, 8, true)) return;
     asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
+    if (!access_ok(p, 16, true)) return;
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
 }
 __device__ __forceinline__ void st_stream_u32(uint32_t* p, uint32_t v) {
+    if (!access_ok(p, 4, true)) return;
     asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_stream(float* p, float v) {
+    if (!access_ok(p, 4, true)) return;
     asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// Plain stores and the counter update, checked the same way.
+__device__ __forceinline__ void st_plain(uint8_t* p, uint8_t v) {
+    if (access_ok(p, 1, true)) *p = v;
+}
+__device__ __forceinline__ void st_plain(float* p, float v) {
+    if (access_ok(p, 4, true)) *p = v;
+}
+__device__ __forceinline__ void st_plain(float4* p, float4 v) {
+    if (access_ok(p, 16, true)) *p = v;
+}
+__device__ __forceinline__ void atomic_add_count(unsigned long long* p, unsigned long long v) {
+    if (access_ok(p, 8, true)) atomicAdd(p, v);
 }
 
 // ---------------------------------------------------------------------------

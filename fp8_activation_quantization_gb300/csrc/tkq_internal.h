@@ -28,6 +28,23 @@ int num_sms();
 // device with cudaGetSymbolAddress.
 unsigned int* device_status_word();
 
+// Access checking of the checked build (-DTKQ_CHECKED; see tkq_device.cuh):
+// the buffers of the current call, inputs and outputs, as address ranges.
+constexpr uint32_t kDeviceOutOfBounds = 2u;  // status-word bit: an access was refused
+constexpr int kCheckMax = 8;
+
+struct CheckTable {
+    unsigned long long lo[kCheckMax], hi[kCheckMax];  // [lo, hi) per buffer
+    unsigned writable;                                // bit k: buffer k is an output
+    int n;
+    unsigned int* status;     // the library's device status word
+    unsigned long long* bad;  // first refused address (bit 63: a store)
+};
+
+// The calling host thread's table for its current call (filled by the ABI
+// layer, copied to the device by each launcher).  Checked build only.
+CheckTable& host_check_table();
+
 // Persistent grid: min(blocks needed, SMs x resident blocks per SM).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
 

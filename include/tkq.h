@@ -309,6 +309,26 @@ tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, flo
 tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T, int64_t H,
                              tkq_stream_t stream);
 
+/*
+ * Access checking (not from the source pages; the stand-in for a memory
+ * checker).  The same sources built with -DTKQ_CHECKED give libtkq_checked.so,
+ * a test build in which every global load and store of the kernels is first
+ * checked against the buffers of the current call (loads: its inputs and
+ * outputs; stores: its outputs, sized as documented for each call).  An access
+ * outside them is skipped, sets TKQ_DEVICE_OUT_OF_BOUNDS in the device status
+ * word (tkq_read_device_status) and records the first such address, read with
+ * tkq_read_check_address (bit 63 set for a store).  The checked build keeps one
+ * table per kernel source file, so its calls must not run concurrently.  In
+ * the release build no access is checked: the status bit is never set and the
+ * address reads 0.
+ */
+#define TKQ_DEVICE_OUT_OF_BOUNDS 2u
+/* 1 in the checked build, 0 in the release build. */
+int tkq_checked_build(void);
+/* Synchronizes the current device, then returns (and with clear != 0 resets)
+ * the first refused address.  Errors: TKQ_ERR_NULL, TKQ_ERR_CUDA. */
+tkq_status tkq_read_check_address(uint64_t* addr, int clear);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* tkq_status_string(int status);
 

@@ -39,6 +39,19 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libtkq.so does not export {name}"
 
 
+def test_checked_build_exports_every_declared_symbol(lib):
+    """The access-checked test build compiles from the same sources, exports the
+    same ABI and says which build it is; the release build says it is not."""
+    from fp8_activation_quantization_gb300 import _build
+    path = _build.build(checked=True)
+    checked = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(checked, name), f"libtkq_checked.so does not export {name}"
+    assert checked.tkq_checked_build() == 1
+    assert lib.tkq_checked_build() == 0
+    assert lib.tkq_read_check_address(None, 0) == 1           # NULL out-pointer
+
+
 def test_library_is_built_for_sm_103a():
     from fp8_activation_quantization_gb300 import _build
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
