@@ -1,0 +1,86 @@
+"""Many launches of every kernel and option set on mid-size inputs, each
+result compared on the GPU with the first, byte for byte.  An intermittent
+race (a ring stage handed back before its readers are done, a missing barrier
+between a table's writes and reads) shows up as a rare differing launch; the
+full-grid and few-SM runs exercise short and long ring walks."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_activation_quantization_gb300 as tkq
+from fp8_activation_quantization_gb300 import synth
+from tests.test_gpu_parity import to_dev_bf16
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+RUNS = 1500
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    tkq.load_library()
+    yield
+
+
+def _ops(dev):
+    x = to_dev_bf16(synth.outlier_bf16(1, 1, 4099, 4096, zero_row_every=0), dev)
+    xs = to_dev_bf16(synth.swiglu_bf16(2, 2, 4096, 2048, gate_std=2.0), dev)
+    w = torch.from_numpy(synth.routing_weights(3, 3, 512)).to(dev)
+    dy = to_dev_bf16(synth.normal_bf16(4, 4, 4096, 2048), dev)
+    xf = torch.from_numpy(synth.log_uniform_f32(7, 7, (2051, 4096), -6.0, 6.0)).to(dev)
+    codes = torch.from_numpy(synth.random_bytes(5, 5, 4096, 4096)).to(dev)
+    sfc = torch.from_numpy(synth.log_uniform_f32(6, 6, (4096, 32), -10.0, 2.0)).to(dev)
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def clamped(**kw):
+        def run():
+            cnt.zero_()
+            return (*tkq.swiglu_forward_and_per_token_cast(xs, use_clamp=True, clamp_count=cnt,
+                                                           **kw), cnt)
+        return run
+
+    return {
+        "plain": lambda: tkq.per_token_cast(x),
+        "plain ue8m0 col-major": lambda: tkq.per_token_cast(
+            x, use_packed_ue8m0=True, use_tma_aligned_col_major_sf=True),
+        "plain e5m2 sf_inv": lambda: tkq.per_token_cast(x, "e5m2", use_sf_inv=True),
+        "plain fp32": lambda: tkq.per_token_cast(xf),
+        "swiglu weighted": lambda: tkq.swiglu_forward_and_per_token_cast(xs, topk_weights=w),
+        "swiglu clamp": clamped(topk_weights=w, swiglu_clamp_value=2.0),
+        "swiglu_t weighted": lambda: tkq.swiglu_forward_and_per_token_cast(
+            xs, topk_weights=w, with_transpose=True),
+        "swiglu_t clamp": clamped(with_transpose=True, swiglu_clamp_value=2.9),
+        "backward weighted": lambda: tkq.swiglu_backward_and_per_token_cast(xs, dy, topk_weights=w),
+        "per_channel": lambda: tkq.per_channel_cast(xs),
+        "per_channel_t": lambda: tkq.per_channel_cast(xs, transpose=True),
+        "per_block": lambda: tkq.per_block_cast(x),
+        "cast_back bf16": lambda: (tkq.cast_back(codes, sfc, fmt="e4m3", out_dtype=torch.bfloat16),),
+        "cast_back fp32 blocks": lambda: (tkq.cast_back(codes, sfc[:32, :32].contiguous(),
+                                                        fmt="e5m2", group_size=(128, 128)),),
+    }
+
+
+def _same(a, b):
+    return torch.equal(a.contiguous().view(torch.uint8), b.contiguous().view(torch.uint8))
+
+
+@pytest.mark.parametrize("sms", [None, "7"])
+def test_many_launches_give_identical_bytes(cuda_device, sms, monkeypatch):
+    if sms is not None:
+        monkeypatch.setenv("TKQ_NUM_SMS", sms)
+    runs = RUNS if sms is None else RUNS // 5
+    differing = {}
+    for name, op in _ops(cuda_device).items():
+        ref = [t.clone() for t in op()]
+        bad = 0
+        for _ in range(runs):
+            if not all(_same(a, b) for a, b in zip(op(), ref)):
+                bad += 1
+        if bad:
+            differing[name] = bad
+    assert not differing, f"launches differing from the first: {differing} of {runs} each"
+    assert tkq.tkq_read_device_status() == 0
