@@ -291,10 +291,11 @@ def test_swiglu_t_shapes(cuda_device, T, H, weighted, fmt):
 
 
 @pytest.mark.slow
-def test_swiglu_t_full_workload_sampled(cuda_device):
-    """The full [131072, 4096] workload in one launch; 48 token blocks of 128
-    rows are checked against the oracle (row and column outputs), and every row
-    output against the SwiGLU cast kernel bit for bit."""
+def test_swiglu_t_full_workload(cuda_device):
+    """The full [131072, 4096] workload in the launch the benchmark times:
+    every row and column output against the oracle (all 2 x 268 M codes and
+    their scales), and every row output against the SwiGLU cast kernel bit
+    for bit."""
     dev = cuda_device
     x = synth.workload("swiglu_t")["x"]
     T, H2 = x.shape
@@ -315,18 +316,13 @@ def test_swiglu_t_full_workload_sampled(cuda_device):
     torch.cuda.synchronize()
     assert tkq.tkq_read_device_status() == 0, "a bounded wait gave up"
     assert torch.equal(out, out2) and torch.equal(sf.view(torch.int32), sf2.view(torch.int32))
-    blocks = np.unique(np.concatenate([[0, T // 128 - 1],
-                                       np.random.default_rng(3).integers(0, T // 128, 46)]))
-    rows = np.concatenate([np.arange(b * 128, b * 128 + 128) for b in blocks])
-    ro, rs, rot, rst = oracle.swiglu_cast_t(np.ascontiguousarray(x[rows]), None, "e4m3",
-                                            threads=THREADS)
-    ridx = torch.from_numpy(rows).to(dev)
-    parity.assert_scales_close("row scales", sf.index_select(0, ridx).cpu().numpy(), rs)
-    parity.assert_codes_close("row codes", out.index_select(0, ridx).cpu().numpy(), ro)
-    got_t = out_t.index_select(1, ridx).cpu().numpy()
-    got_st = sf_t.index_select(1, torch.from_numpy(blocks).to(dev)).cpu().numpy()
-    parity.assert_scales_close("column scales", got_st, rst)
-    parity.assert_codes_close("column codes", got_t, rot)
+    del out2, sf2, xd
+    ro, rs, rot, rst = oracle.swiglu_cast_t(x, None, "e4m3", threads=THREADS)
+    parity.assert_scales_close("row scales", sf.cpu().numpy(), rs)
+    parity.assert_codes_close("row codes", out.cpu().numpy(), ro)
+    del ro, rs
+    parity.assert_scales_close("column scales", sf_t.cpu().numpy(), rst)
+    parity.assert_codes_close("column codes", out_t.cpu().numpy(), rot)
 
 
 # ---------------------------------------------------------------------------
