@@ -126,3 +126,34 @@ def test_casts_quantize_these_values(cuda_device, weighted):
     parity.assert_bit_exact("column scales", st.cpu().numpy(), e_st)
     parity.assert_codes_differ_only_at_ties("column codes", qt.view(torch.uint8).cpu().numpy(), e_qt,
                                             y.T / np.repeat(e_st, 128, axis=1), "e4m3")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["swiglu_moe", "swiglu_t"])
+def test_full_workloads_quantize_these_values(cuda_device, name):
+    """At the full sizes of the weighted SwiGLU workload and of the transposed
+    workload (the benchmark's step): every row scale, and for the transposed
+    cast every column scale, equals bit for bit the oracle's scale rule applied
+    to the kernels' own y; every code equals the oracle's code of that y except
+    at FP8 ties."""
+    d = synth.workload(name)
+    x, w = d["x"], d.get("w")
+    xd = to_dev_bf16(x, cuda_device)
+    wd = None if w is None else torch.from_numpy(w).to(cuda_device)
+    y = tkq.swiglu_values(xd, wd).cpu().numpy()
+    if name == "swiglu_t":
+        q, s, qt, st = tkq.swiglu_forward_and_per_token_cast(xd, with_transpose=True)
+    else:
+        q, s = tkq.swiglu_forward_and_per_token_cast(xd, topk_weights=wd)
+    del xd
+    e_q, e_s = oracle.cast_rows_f32(y, "e4m3")
+    parity.assert_bit_exact("row scales", s.cpu().numpy(), e_s)
+    parity.assert_codes_differ_only_at_ties("row codes", q.view(torch.uint8).cpu().numpy(), e_q,
+                                            y / np.repeat(e_s, 128, axis=1), "e4m3")
+    del e_q, e_s, q, s
+    if name == "swiglu_t":
+        e_qt, e_st = oracle.cast_cols_f32(y, "e4m3")
+        parity.assert_bit_exact("column scales", st.cpu().numpy(), e_st)
+        parity.assert_codes_differ_only_at_ties(
+            "column codes", qt.view(torch.uint8).cpu().numpy(), e_qt,
+            y.T / np.repeat(e_st, 128, axis=1), "e4m3")
