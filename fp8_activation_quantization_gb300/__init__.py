@@ -28,6 +28,7 @@ __all__ = [
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
     "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
     "use_checked_library", "tkq_checked_build", "tkq_read_check_address",
+    "tkq_swiglu_backward_values", "swiglu_backward_values",
 ]
 
 FMT_E4M3 = 0
@@ -128,6 +129,8 @@ def _open(path):
         lib.tkq_per_token_cast_f32.restype = i
         lib.tkq_swiglu_values.argtypes = [p, p, p, i64, i64, p]
         lib.tkq_swiglu_values.restype = i
+        lib.tkq_swiglu_backward_values.argtypes = [p, p, p, p, i64, i64, p]
+        lib.tkq_swiglu_backward_values.restype = i
         lib.tkq_checked_build.argtypes = []
         lib.tkq_checked_build.restype = i
         lib.tkq_read_check_address.argtypes = [ctypes.POINTER(ctypes.c_uint64), i]
@@ -202,6 +205,10 @@ def tkq_per_token_cast_f32(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags
 
 def tkq_swiglu_values(x, w, y, T, H, stream=None) -> int:
     return (_lib or load_library()).tkq_swiglu_values(x, w, y, T, H, stream)
+
+
+def tkq_swiglu_backward_values(x, dy, w, y, T, H, stream=None) -> int:
+    return (_lib or load_library()).tkq_swiglu_backward_values(x, dy, w, y, T, H, stream)
 
 
 def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
@@ -569,4 +576,25 @@ def swiglu_values(x, topk_weights=None):
                                _stream_handle(x.device))
     if st:
         raise TkqError(st, "tkq_swiglu_values")
+    return y
+
+
+def swiglu_backward_values(x, dy, topk_weights=None):
+    """Diagnostic: the fp32 gradients [dg | du] ([T, 2H]) exactly as the SwiGLU
+    backward cast computes them before quantizing (x: bf16 [T, 2H] gate | up,
+    dy: bf16 [T, H])."""
+    import torch
+    _check_input(x)
+    _check_input(dy, "dy")
+    T, H2 = x.shape
+    H = H2 // 2
+    if H2 % 2 or tuple(dy.shape) != (T, H) or dy.device != x.device:
+        raise ValueError("dy must be [T, H] for x [T, 2H], on the same device")
+    _check_weights(topk_weights, T, x)
+    y = torch.empty((T, H2), dtype=torch.float32, device=x.device)
+    with _device_ctx(x.device):
+        st = tkq_swiglu_backward_values(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(y), T, H,
+                                        _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_swiglu_backward_values")
     return y

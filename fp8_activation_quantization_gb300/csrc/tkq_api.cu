@@ -534,6 +534,24 @@ tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T,
         tkq::launch_swiglu_values(x, w, y, T, H, static_cast<cudaStream_t>(stream)));
 }
 
+tkq_status tkq_swiglu_backward_values(const void* x, const void* dy, const float* w, float* y,
+                                      int64_t T, int64_t H, tkq_stream_t stream) {
+    tkq_status st = check_common(T, H, 128, TKQ_FMT_E4M3);
+    if (st != TKQ_OK) return st;
+    if (T == 0) return TKQ_OK;
+    if (!x || !dy || !y) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(dy, 16) || !tkq::aligned(y, 16) ||
+        (w && !tkq::aligned(w, 4)))
+        return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, T * H * 4), rd = tkq::span(dy, T * H * 2),
+               ry = tkq::span(y, T * H * 8);
+    const auto rw = w ? tkq::span(w, T * 4) : tkq::Range{0, 0};
+    if (tkq::overlap(rx, ry) || tkq::overlap(rd, ry) || tkq::overlap(rw, ry)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx, rd, rw}, {ry});
+    return launch_status(tkq::launch_swiglu_backward_values(x, dy, w, y, T, H,
+                                                            static_cast<cudaStream_t>(stream)));
+}
+
 tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
     if (!flags) return TKQ_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;

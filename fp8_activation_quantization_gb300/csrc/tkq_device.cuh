@@ -330,12 +330,6 @@ __device__ __forceinline__ float2 swiglu2(float2 g, float2 u) {
     return mul2(mul2(g, make_float2(rcp_approx(den.x), rcp_approx(den.y))), u);
 }
 
-__device__ __forceinline__ float swiglu(float g, float u) {
-    const float e = ex2_approx(__fmul_rn(g, -1.4426950408889634f));
-    const float den = __fadd_rn(1.0f, e);
-    return __fmul_rn(__fmul_rn(g, rcp_approx(den)), u);
-}
-
 // ---------------------------------------------------------------------------
 // SwiGLU clamp (gate <= c, -c <= up <= c) on packed bf16 pairs
 // ---------------------------------------------------------------------------
@@ -379,30 +373,25 @@ __device__ __forceinline__ uint32_t clamp_pairs_bf16(uint32_t& g, uint32_t& u, u
 
 // Gradient of y = silu(g) * u with respect to g and u, scaled by the upstream
 // gradient d (the derivative of the SwiGLU of the same page; it gives no
-// formula, this is the textbook one):
+// formula, this is the textbook one), for two elements at a time with the
+// packed pair instructions (the transcendental steps and the bound below stay
+// scalar):
 //   sigma = 1 / (1 + e), e = exp(-g);  1 - sigma = e * sigma (no cancellation)
 //   dg = d * u * sigma * (1 + g * (1 - sigma)),  du = d * g * sigma.
-// The exponent is clamped at 2^126 so that e * sigma stays finite for very
-// negative g (where sigma, silu and both gradients are ~0 anyway).
-__device__ __forceinline__ void swiglu_grad(float g, float u, float d, float& dg, float& du) {
-    const float t = fminf(__fmul_rn(g, -1.4426950408889634f), 126.0f);
-    const float e = ex2_approx(t);
-    const float sig = rcp_approx(__fadd_rn(1.0f, e));
-    const float one_minus_sig = __fmul_rn(e, sig);
-    const float dsilu = __fmul_rn(sig, __fmaf_rn(g, one_minus_sig, 1.0f));
-    dg = __fmul_rn(__fmul_rn(d, u), dsilu);
-    du = __fmul_rn(d, __fmul_rn(g, sig));
-}
-
-// swiglu_grad of two elements with the packed pair instructions (the clamp of
-// the exponent and the transcendental steps stay scalar).  Bit-identical.
+// e * sigma is bounded by 1.  Where e overflows (g < -88.7), sigma = 0 and
+// e * sigma = inf * 0 is NaN, which fminf turns into 1; both gradients are
+// then exactly 0, which is what sigma -> 0 makes them.  (Clamping the exponent
+// instead would leave sigma at its smallest normal value, so that dg grew like
+// 2^-126 * g for very negative g.)  Elsewhere the bound changes at most a
+// product that rounded above 1.
 __device__ __forceinline__ void swiglu_grad2(float2 g, float2 u, float2 d, float2& dg,
                                              float2& du) {
     const float2 t = mul2(g, make_float2(-1.4426950408889634f, -1.4426950408889634f));
-    const float2 e = make_float2(ex2_approx(fminf(t.x, 126.0f)), ex2_approx(fminf(t.y, 126.0f)));
+    const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
     const float2 den = add2(make_float2(1.0f, 1.0f), e);
     const float2 sig = make_float2(rcp_approx(den.x), rcp_approx(den.y));
-    const float2 one_minus_sig = mul2(e, sig);
+    const float2 es = mul2(e, sig);
+    const float2 one_minus_sig = make_float2(fminf(es.x, 1.0f), fminf(es.y, 1.0f));
     const float2 dsilu = mul2(sig, fma2(g, one_minus_sig, make_float2(1.0f, 1.0f)));
     dg = mul2(mul2(d, u), dsilu);
     du = mul2(d, mul2(g, sig));

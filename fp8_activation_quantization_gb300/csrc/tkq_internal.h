@@ -56,6 +56,11 @@ cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T,
 cudaError_t launch_swiglu_values(const void* x, const float* w, float* y, int64_t T, int64_t H,
                                  cudaStream_t stream);
 
+// The fp32 gradients [dg | du] ([T, 2H]) the SwiGLU backward cast quantizes
+// (diagnostic).
+cudaError_t launch_swiglu_backward_values(const void* x, const void* dy, const float* w, float* y,
+                                          int64_t T, int64_t H, cudaStream_t stream);
+
 // The per-token cast of a row-major fp32 [T, C] matrix.
 cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
                                       int fmt, unsigned sf_flags, cudaStream_t stream);

@@ -310,6 +310,18 @@ tkq_status tkq_swiglu_values(const void* x, const float* w, float* y, int64_t T,
                              tkq_stream_t stream);
 
 /*
+ * Diagnostic (not an operation of the source pages): the fp32 gradients the
+ * SwiGLU backward cast quantizes, computed exactly as tkq_swiglu_backward_cast
+ * computes them (the SM's ex2 / rcp, the weight product), written out:
+ *   y[t, c] = dg,  y[t, H + c] = du   (formulas of tkq_swiglu_backward_cast)
+ *   x : bf16 [T, 2H];  dy : bf16 [T, H];  w : fp32 [T] or NULL;
+ *   y : fp32 [T, 2H], 16-byte aligned, overlapping none of the inputs
+ * T >= 0; H > 0, H % 128 == 0.
+ */
+tkq_status tkq_swiglu_backward_values(const void* x, const void* dy, const float* w, float* y,
+                                      int64_t T, int64_t H, tkq_stream_t stream);
+
+/*
  * Access checking (not from the source pages; the stand-in for a memory
  * checker).  The same sources built with -DTKQ_CHECKED give libtkq_checked.so,
  * a test build in which every global load and store of the kernels is first

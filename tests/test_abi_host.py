@@ -251,3 +251,28 @@ def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
 ])
 def test_per_token_cast_f32_validation(lib, args, expected):
     assert lib.tkq_per_token_cast_f32(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((None, None, p(1 << 24), 4, 128), 1),                 # NULL x
+    ((p(), None, p(1 << 24), 4, 100), 2),                  # H % 128
+    ((p(4), None, p(1 << 24), 4, 128), 5),                 # x misaligned
+    ((p(), p(2), p(1 << 24), 4, 128), 5),                  # w misaligned
+    ((p(), None, p(1024), 4, 128), 7),                     # y inside x (2048 bytes)
+    ((None, None, None, 0, 128), 0),                       # empty batch
+])
+def test_swiglu_values_validation(lib, args, expected):
+    assert lib.tkq_swiglu_values(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((p(), None, None, p(1 << 24), 4, 128), 1),             # NULL dy
+    ((p(), p(1 << 20), None, p(1 << 24), 4, 200), 2),       # H % 128
+    ((p(), p((1 << 20) + 8), None, p(1 << 24), 4, 128), 5),  # dy misaligned
+    ((p(), p(1 << 20), None, p((1 << 24) + 4), 4, 128), 5),  # y misaligned
+    ((p(), p(1 << 20), None, p((1 << 20) + 512), 4, 128), 7),  # y overlaps dy (1024 bytes)
+    ((p(), p(1 << 20), p(1 << 22), p((1 << 22) - 4096 + 16), 4, 128), 7),  # w inside y
+    ((None, None, None, None, 0, 128), 0),                  # empty batch
+])
+def test_swiglu_backward_values_validation(lib, args, expected):
+    assert lib.tkq_swiglu_backward_values(*args, None) == expected

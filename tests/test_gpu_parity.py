@@ -373,14 +373,19 @@ def test_swiglu_backward_ragged(cuda_device, T, H, weighted, fmt):
 
 
 def test_swiglu_backward_extreme_gates(cuda_device):
-    """Gates from -120 to 120 (exp(-g) overflows binary32 below -88): the
-    gradients must stay finite and match the oracle."""
+    """Gates from -120 to 120 (exp(-g) overflows binary32 below -88) and of
+    magnitude up to 1e38: the gradients must stay finite and match the oracle
+    (sigma -> 0 makes both exactly 0 for very negative gates; an exponent
+    clamped at 126 would leave dg = d u 2^-126 (1 + g) there, which the codes
+    of rows holding gates near -1e38 show)."""
     T, H = 256, 256
     rng = np.random.default_rng(8)
-    g = np.linspace(-120, 120, T * H).astype(np.float32).reshape(T, H)
+    n = T * H // 2
+    big = np.logspace(2.0, 38.0, n // 2) * np.where(np.arange(n // 2) % 2, 1.0, -1.0)
+    g = np.concatenate([np.linspace(-120, 120, n), big, -big]).astype(np.float32).reshape(T, H)
     u = rng.standard_normal((T, H)).astype(np.float32)
     x = np.concatenate([synth.f32_to_bf16_bits(g), synth.f32_to_bf16_bits(u)], axis=1)
-    dy = synth.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    dy = synth.f32_to_bf16_bits(rng.uniform(-1.0, 1.0, (T, H)).astype(np.float32))
     out, sf = run_swiglu_bwd(x, dy, None, "e4m3", cuda_device)
     ro, rs = oracle.swiglu_backward_cast(x, dy, None, "e4m3")
     assert np.all(np.isfinite(sf))
