@@ -1,11 +1,19 @@
 """The oracle's FP8 encoder on every one of the 2^32 binary32 bit patterns,
-against torch's float8 conversion (a library routine, round to nearest even)
-with the saturation rule applied on top: where torch gives a finite code the
-oracle gives the same; where a finite input overflows (torch: NaN for e4m3fn,
-inf for e5m2) the oracle gives the largest finite code of that sign; an
-infinite input gives the largest finite code of its sign; a NaN gives the NaN
-code 0x7F (either sign bit accepted).  Split over threads (ctypes and torch
-release the GIL); every thread reuses its buffers."""
+against two references:
+1. torch's float8 conversion (a library routine, round to nearest even) with
+   the saturation rule applied on top: where torch gives a finite code the
+   oracle gives the same; where a finite input overflows (torch: NaN for
+   e4m3fn, inf for e5m2) the oracle gives the largest finite code of that
+   sign; an infinite input gives the largest finite code of its sign; a NaN
+   gives the NaN code 0x7F (either sign bit accepted);
+2. a brute-force nearest-value search: the finite codes of each format are
+   decoded by torch (their magnitudes increase with the code), and |v| is
+   placed among the midpoints between consecutive magnitudes; the nearer
+   magnitude wins, an exact midpoint goes to the even code (even last mantissa
+   bit), anything above the largest finite magnitude saturates to it, and the
+   sign bit is copied.
+Split over threads (ctypes, torch and numpy release the GIL); every thread
+reuses its buffers."""
 import os
 import threading
 from concurrent.futures import ThreadPoolExecutor
@@ -21,6 +29,41 @@ MAXCODE = {"e4m3": 0x7E, "e5m2": 0x7B}
 TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 _BASE = np.arange(CHUNK, dtype=np.uint32)
 _local = threading.local()
+
+
+def _magnitudes(fmt):
+    """Decoded magnitudes of the non-negative finite codes 0 .. MAXCODE."""
+    codes = torch.arange(MAXCODE[fmt] + 1, dtype=torch.uint8)
+    return codes.view(TORCH[fmt]).to(torch.float64).numpy()
+
+
+MAGS = {f: _magnitudes(f) for f in MAXCODE}
+
+
+def _midpoints(fmt):
+    """Binary32 bit patterns of the midpoints between consecutive magnitudes
+    (every such midpoint is exactly a binary32 value)."""
+    m = MAGS[fmt]
+    mid = (m[:-1] + m[1:]) / 2.0
+    assert np.array_equal(mid.astype(np.float32).astype(np.float64), mid)
+    return mid.astype(np.float32).view(np.uint32)
+
+
+MIDS = {f: _midpoints(f) for f in MAXCODE}
+
+
+def _nearest_codes(bits, fmt):
+    """The brute-force encoder (reference 2) for non-NaN bit patterns.  Positive
+    binary32 patterns order like their values, so the number of midpoints below
+    |v| is the index of the nearest magnitude; |v| equal to a midpoint is a tie
+    between codes k and k + 1, which goes to the even one; beyond the largest
+    magnitude every midpoint is below, which saturates."""
+    mids = MIDS[fmt]
+    mag = bits & np.uint32(0x7FFFFFFF)
+    k = np.searchsorted(mids, mag)
+    tie = mids[np.minimum(k, mids.size - 1)] == mag
+    code = k + (tie & (k % 2 == 1))
+    return code.astype(np.uint8) | ((bits >> np.uint32(24)).astype(np.uint8) & np.uint8(0x80))
 
 
 def _buffers(fmt):
@@ -49,6 +92,12 @@ def _check_chunk(start, fmt):
     if bad.any():
         i = int(np.flatnonzero(bad)[0])
         return f"{fmt}: bits {int(bits[i]):#010x} -> {int(got[i]):#04x}, expected {int(exp[i]):#04x}"
+    near = _nearest_codes(bits, fmt)
+    bad = ~nan_in & (got != near)
+    if bad.any():
+        i = int(np.flatnonzero(bad)[0])
+        return (f"{fmt}: bits {int(bits[i]):#010x} -> {int(got[i]):#04x}, nearest-value search "
+                f"{int(near[i]):#04x}")
     return None
 
 
