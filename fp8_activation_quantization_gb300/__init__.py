@@ -28,7 +28,7 @@ __all__ = [
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
     "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
     "use_checked_library", "tkq_checked_build", "tkq_read_check_address",
-    "tkq_swiglu_backward_values", "swiglu_backward_values",
+    "tkq_swiglu_backward_values", "swiglu_backward_values", "tkq_fp8_encode", "fp8_encode",
 ]
 
 FMT_E4M3 = 0
@@ -131,6 +131,8 @@ def _open(path):
         lib.tkq_swiglu_values.restype = i
         lib.tkq_swiglu_backward_values.argtypes = [p, p, p, p, i64, i64, p]
         lib.tkq_swiglu_backward_values.restype = i
+        lib.tkq_fp8_encode.argtypes = [p, p, i64, i, p]
+        lib.tkq_fp8_encode.restype = i
         lib.tkq_checked_build.argtypes = []
         lib.tkq_checked_build.restype = i
         lib.tkq_read_check_address.argtypes = [ctypes.POINTER(ctypes.c_uint64), i]
@@ -205,6 +207,10 @@ def tkq_per_token_cast_f32(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, sf_flags
 
 def tkq_swiglu_values(x, w, y, T, H, stream=None) -> int:
     return (_lib or load_library()).tkq_swiglu_values(x, w, y, T, H, stream)
+
+
+def tkq_fp8_encode(x, out, n, fmt=FMT_E4M3, stream=None) -> int:
+    return (_lib or load_library()).tkq_fp8_encode(x, out, n, fmt, stream)
 
 
 def tkq_swiglu_backward_values(x, dy, w, y, T, H, stream=None) -> int:
@@ -598,3 +604,18 @@ def swiglu_backward_values(x, dy, topk_weights=None):
     if st:
         raise TkqError(st, "tkq_swiglu_backward_values")
     return y
+
+
+def fp8_encode(x, fmt="e4m3"):
+    """Diagnostic: the FP8 codes (uint8, same shape) of an fp32 CUDA tensor,
+    unscaled, by the conversion every cast ends with."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous fp32 CUDA tensor")
+    f = _fmt_code(fmt)
+    out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    with _device_ctx(x.device):
+        st = tkq_fp8_encode(_ptr(x), _ptr(out), x.numel(), f, _stream_handle(x.device))
+    if st:
+        raise TkqError(st, "tkq_fp8_encode")
+    return out

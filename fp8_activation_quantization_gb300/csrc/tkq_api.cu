@@ -552,6 +552,19 @@ tkq_status tkq_swiglu_backward_values(const void* x, const void* dy, const float
                                                             static_cast<cudaStream_t>(stream)));
 }
 
+tkq_status tkq_fp8_encode(const float* x, void* out, int64_t n, int fmt, tkq_stream_t stream) {
+    if (n < 0 || n % 4) return TKQ_ERR_SHAPE;
+    if (fmt != TKQ_FMT_E4M3 && fmt != TKQ_FMT_E5M2) return TKQ_ERR_FMT;
+    if (n == 0) return TKQ_OK;
+    if (!x || !out) return TKQ_ERR_NULL;
+    if (!tkq::aligned(x, 16) || !tkq::aligned(out, 4)) return TKQ_ERR_ALIGN;
+    const auto rx = tkq::span(x, n * 4), ro = tkq::span(out, n);
+    if (tkq::overlap(rx, ro)) return TKQ_ERR_ALIAS;
+    tkq::register_call({rx}, {ro});
+    return launch_status(
+        tkq::launch_fp8_encode(x, out, n, fmt, static_cast<cudaStream_t>(stream)));
+}
+
 tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
     if (!flags) return TKQ_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return TKQ_ERR_CUDA;

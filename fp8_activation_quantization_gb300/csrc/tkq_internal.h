@@ -61,6 +61,10 @@ cudaError_t launch_swiglu_values(const void* x, const float* w, float* y, int64_
 cudaError_t launch_swiglu_backward_values(const void* x, const void* dy, const float* w, float* y,
                                           int64_t T, int64_t H, cudaStream_t stream);
 
+// FP8 codes of n fp32 values, unscaled (diagnostic; n % 4 == 0).
+cudaError_t launch_fp8_encode(const float* x, void* out, int64_t n, int fmt,
+                              cudaStream_t stream);
+
 // The per-token cast of a row-major fp32 [T, C] matrix.
 cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
                                       int fmt, unsigned sf_flags, cudaStream_t stream);

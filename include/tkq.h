@@ -322,6 +322,16 @@ tkq_status tkq_swiglu_backward_values(const void* x, const void* dy, const float
                                       int64_t T, int64_t H, tkq_stream_t stream);
 
 /*
+ * Diagnostic (not an operation of the source pages): the FP8 codes of n fp32
+ * values, unscaled, by the conversion every cast ends with (saturating
+ * round-to-nearest-even, cvt.rn.satfinite; NaN gives a NaN code).  Lets the
+ * hardware conversion be compared with the format definition on any value.
+ *   x : fp32 [n], 16-byte aligned;  out : FP8 codes [n], 4-byte aligned
+ * n >= 0, n % 4 == 0 (else TKQ_ERR_SHAPE); fmt as for the casts.
+ */
+tkq_status tkq_fp8_encode(const float* x, void* out, int64_t n, int fmt, tkq_stream_t stream);
+
+/*
  * Access checking (not from the source pages; the stand-in for a memory
  * checker).  The same sources built with -DTKQ_CHECKED give libtkq_checked.so,
  * a test build in which every global load and store of the kernels is first

@@ -276,3 +276,17 @@ def test_swiglu_values_validation(lib, args, expected):
 ])
 def test_swiglu_backward_values_validation(lib, args, expected):
     assert lib.tkq_swiglu_backward_values(*args, None) == expected
+
+
+@pytest.mark.parametrize("args,expected", [
+    ((p(), p(1 << 24), 6, 0), 2),             # n % 4
+    ((p(), p(1 << 24), -4, 0), 2),            # n < 0
+    ((p(), p(1 << 24), 16, 3), 4),            # fmt
+    ((None, p(1 << 24), 16, 0), 1),           # NULL x
+    ((p(8), p(1 << 24), 16, 0), 5),           # x misaligned
+    ((p(), p(2), 16, 0), 5),                  # out misaligned
+    ((p(), p(32), 16, 0), 7),                 # out inside x (64 bytes)
+    ((None, None, 0, 1), 0),                  # empty
+])
+def test_fp8_encode_validation(lib, args, expected):
+    assert lib.tkq_fp8_encode(*args, None) == expected

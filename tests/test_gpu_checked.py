@@ -109,6 +109,9 @@ def _cases(dev):
             cases.append((f"cast_back {T}x{C} groups {group} {dt}",
                           lambda q=codes, s=sf, g=group, dt=dt: (tkq.cast_back(
                               q, s, fmt="e4m3", group_size=g, out_dtype=dt),)))
+    for n, fmt in [(4, "e4m3"), (1028, "e5m2")]:
+        xv = _dev_f32(np.random.default_rng(n).standard_normal(n) * 300.0, dev)
+        cases.append((f"fp8_encode {n} {fmt}", lambda x=xv, f=fmt: (tkq.fp8_encode(x, f),)))
     for T, H, weighted in [(3, 128, False), (129, 256, True)]:
         x = to_dev_bf16(synth.swiglu_bf16(T + 6, H, T, H), dev)
         w = _dev_f32(synth.routing_weights(T, 6, -(-T // 8))[:T], dev) if weighted else None
