@@ -14,15 +14,17 @@
 // 128-channel block.  Warp 8 is the producer: one lane loads each chunk with
 // one 2-D TMA box per operand (32 x 128 bf16 = 8 KB: x; or gate and up; or
 // gate, up and dy; 16 KB of fp32 x) into a shared ring of 64-72 KB (8 plain,
-// 4 SwiGLU or fp32, 3 backward chunks in flight per CTA).  Rows past T are zero-filled by the TMA
-// unit and never stored, so ragged T needs no special path.  Warps 0..7 are
+// 4 SwiGLU or fp32, 3 backward chunks in flight per CTA).  Rows past T are
+// zero-filled by the TMA unit and never stored, so ragged T needs no special
+// path.  Warps 0..7 are
 // consumers: warp w owns rows 4w..4w+3 of the chunk, eight lanes per row
 // (lane j holds elements [8j, 8j+8) and [64+8j, 64+8j+8), read as two
 // conflict-free 16-byte shared loads per operand), the group absmax is three
 // xor shuffles, and codes leave as 8-byte stores (eight lanes write one
 // 64-byte run).  The plain casts write the codes of the exact binary32
-// quotient fl(x / s) (`quotient` / `quotient2`), so they are bit-exact; the
-// SwiGLU casts write the codes of y * fl(1 / s) as the page's kernel does.
+// quotient fl(x / s) (`quotient` / `quotient2`), so they are bit-exact, or
+// with TKQ_Q_RECIPROCAL those of x * fl(1 / s); the SwiGLU casts write the
+// codes of y * fl(1 / s) as the page's kernel does.
 // Elementwise fp32 steps run on packed pairs (tkq_device.cuh); a clamp bound
 // that is a bf16 value is applied, and its changes counted, on the packed bf16
 // input pairs before they are widened (same values, half the instructions).
@@ -404,7 +406,8 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, voi
     lay.rows4 = (T + 3) / 4 * 4;
     float* sff = static_cast<float*>(sf);
     return sf_flags
-               ? launch_mode<FMT, MODE, true>(map, map_dy, w, out, sff, lay, T, C_out, clamp, stream)
+               ? launch_mode<FMT, MODE, true>(map, map_dy, w, out, sff, lay, T, C_out, clamp,
+                                              stream)
                : launch_mode<FMT, MODE, false>(map, map_dy, w, out, sff, lay, T, C_out, clamp,
                                                stream);
 }

@@ -180,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int k = 0; k < 4; k += 2) {
-                    float2 p = swiglu2(make_float2(gv[k], gv[k + 1]), make_float2(uv[k], uv[k + 1]));
+                    float2 p =
+                        swiglu2(make_float2(gv[k], gv[k + 1]), make_float2(uv[k], uv[k + 1]));
                     if constexpr (WEIGHTED) p = mul2(p, make_float2(wt[r], wt[r]));
                     y[r][k] = p.x;
                     y[r][k + 1] = p.y;
@@ -243,7 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             float rinv[8];
-            *reinterpret_cast<float4*>(rinv) = *reinterpret_cast<const float4*>(&sm.rowinv[warp][0]);
+            *reinterpret_cast<float4*>(rinv) =
+                *reinterpret_cast<const float4*>(&sm.rowinv[warp][0]);
             *reinterpret_cast<float4*>(rinv + 4) =
                 *reinterpret_cast<const float4*>(&sm.rowinv[warp][4]);
 #pragma unroll

@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(kCtThreads, 1)
             const uint8_t* base = sm.stage[s] + (16 * wg) * (kCtTileCols * 2) + lane * 4;
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
-                const uint32_t q = ok ? *reinterpret_cast<const uint32_t*>(base + r * kCtTileCols * 2)
-                                      : 0u;
+                const uint32_t q =
+                    ok ? *reinterpret_cast<const uint32_t*>(base + r * kCtTileCols * 2) : 0u;
                 v[r][0] = bf16_lo(q);
                 v[r][1] = bf16_hi(q);
             }

@@ -170,7 +170,8 @@ void register_call(std::initializer_list<Range> inputs, std::initializer_list<Ra
     CheckTable& t = host_check_table();
     t = CheckTable{};
     uint64_t withhold = 0;
-    if (const char* env = std::getenv("TKQ_CHECK_WITHHOLD")) withhold = std::strtoull(env, nullptr, 10);
+    if (const char* env = std::getenv("TKQ_CHECK_WITHHOLD"))
+        withhold = std::strtoull(env, nullptr, 10);
     auto add = [&t](uintptr_t lo, uintptr_t hi, bool out) {
         if (hi <= lo || t.n >= kCheckMax) return;
         t.lo[t.n] = lo;
