@@ -193,13 +193,14 @@ def _bf16_neighbours(c):
 @pytest.mark.parametrize("weighted", [False, True])
 def test_clamp_at_special_values(cuda_device, clamp, weighted):
     """Gates and ups drawn from infinities, the largest finite bf16, signed
-    zeros, and the bf16 values at and next to +-c: the count is exact and the
-    outputs match the oracle (row and transposed casts)."""
+    zeros, bf16 subnormals, and the bf16 values at and next to +-c: the count
+    is exact and the outputs match the oracle (row and transposed casts)."""
     near = _bf16_neighbours(clamp)
+    subnormals = [0x0001, 0x8001, 0x007F, 0x807F]        # must pass the clamp unchanged
     gates = np.array([0x7F80, 0x7F7F, 0x3F80, 0x0000, 0x8000, 0xC0A0, 0xC2C8]
-                     + near + [n | 0x8000 for n in near], np.uint16)
+                     + subnormals + near + [n | 0x8000 for n in near], np.uint16)
     ups = np.array([0x7F80, 0xFF80, 0x7F7F, 0xFF7F, 0x0000, 0x8000, 0x3F00]
-                   + near + [n | 0x8000 for n in near], np.uint16)
+                   + subnormals + near + [n | 0x8000 for n in near], np.uint16)
     rng = np.random.default_rng(int(clamp * 1000) + weighted)
     T, H = 256, 256
     x = np.concatenate([rng.choice(gates, (T, H)), rng.choice(ups, (T, H))], axis=1)
