@@ -37,10 +37,13 @@
  *   group), TKQ_ERR_GROUP (group != 128), TKQ_ERR_FMT (unknown format),
  *   TKQ_ERR_ALIGN (x, out, out_t not 16-byte aligned, or sf, sf_t, w not
  *   4-byte aligned), TKQ_ERR_ALIAS (an output overlaps an input or another
- *   output).  T == 0 is an empty batch: TKQ_OK, nothing is launched and the
- *   pointers may be NULL.
+ *   output), TKQ_ERR_FLAGS (unknown option bits), TKQ_ERR_VALUE (an invalid
+ *   scalar argument: a clamp bound that is not finite and positive).
+ *   T == 0 is an empty batch: TKQ_OK, nothing is launched and the pointers
+ *   may be NULL.
  * - A failed launch returns TKQ_ERR_CUDA (cudaGetLastError after the launch).
- * - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ * - Inputs must be finite; NaN or Inf inputs give unspecified codes, and so
+ *   does a SwiGLU value or gradient that overflows binary32.
  * - Calls on the same buffers from different streams must be ordered by the
  *   caller.
  */
@@ -101,6 +104,7 @@ tkq_status tkq_per_token_cast(const void* x, void* out, float* sf,
  * those of y times the rounded reciprocal of s (as the TileKernels kernel
  * multiplies by sf_inv, [P2] §3.2): they are not bit-pinned to a CPU
  * evaluation (parity: scales within 1e-6 relative, codes within one FP8 step).
+ * tkq_swiglu_values returns the fp32 y itself.
  */
 tkq_status tkq_swiglu_cast(const void* x, const float* w, void* out, float* sf,
                            int64_t T, int64_t H, int group, int fmt,
