@@ -618,16 +618,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded, generated on the host; see config.workload)",
-        "config": {
-            "workload": _workload_desc(args.workload),
-            "T": prob.T, "cols": prob.C, "fmt": args.fmt, "group": 128,
-            "weighted": prob.weighted,
-            "algorithmic_bytes_per_step": prob.bytes,
-            "l2": "L2 flushed (read of a 512 MB buffer) before every timed launch; "
-                  "value = summed per-launch event times"
-            if small else "inputs larger than L2 (no flush between steps)",
-            "parallelism": f"replicas x{ws} (rows independent, no collective)",
-        },
+        "config": workload_config(args.workload, args.fmt, ws),
         "pct_of_peak": round(100.0 * gbs / ws / peak, 2),
         "rows_per_s": round(rows_per_s, 1),
         "gpu_launches": args.steps,
@@ -714,6 +705,25 @@ def other_workloads(dev, stream, peak, args):
     return out
 
 
+def workload_config(workload: str, fmt: str, ws: int) -> dict:
+    """The `config` object of the JSON line: the same for both arms."""
+    from fp8_activation_quantization_gb300 import synth
+    syn = SYNTH_OF.get(workload, workload)
+    T, C, _ = synth.WORKLOADS[syn]
+    weighted = "w" in synth.workload(syn, rows=1)
+    nbytes = algorithmic_bytes(workload, T, C, weighted)
+    return {
+        "workload": _workload_desc(workload),
+        "T": T, "cols": C, "fmt": fmt, "group": 128,
+        "weighted": weighted,
+        "algorithmic_bytes_per_step": nbytes,
+        "l2": "L2 flushed (read of a 512 MB buffer) before every timed launch; "
+              "value = summed per-launch event times"
+        if nbytes < SMALL_BYTES else "inputs larger than L2 (no flush between steps)",
+        "parallelism": f"replicas x{ws} (rows independent, no collective)",
+    }
+
+
 def _workload_desc(name):
     from fp8_activation_quantization_gb300 import synth
     d = synth.WORKLOADS[SYNTH_OF.get(name, name)][2]
@@ -769,8 +779,7 @@ def run_reference(args):
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded, generated on the host; see config.workload)",
-        "config": {"workload": _workload_desc(args.workload), "T": T_full, "cols": C,
-                   "fmt": args.fmt, "group": 128},
+        "config": workload_config(args.workload, args.fmt, ws),
         "rows_per_s": round(r * args.steps / dt, 1),
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {r} rows of the workload per step, row blocks split "

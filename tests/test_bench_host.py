@@ -84,3 +84,18 @@ def test_profiled_traffic_needs_the_current_sources(tmp_path, monkeypatch):
     (csrc / bench.KERNEL_SOURCES[kern][0]).write_text("// changed\n")
     assert bench.profiled_traffic(kern, workload) is None
     assert bench.profiled_traffic(kern, "no_such_workload") is None
+
+
+def test_both_arms_describe_the_same_config():
+    """The config object comes from one function for both arms; it matches the
+    workload tables and the byte count."""
+    for name in bench.KERNEL_OF:
+        cfg = bench.workload_config(name, "e4m3", 1)
+        T, C, _ = synth.WORKLOADS[bench.SYNTH_OF.get(name, name)]
+        assert (cfg["T"], cfg["cols"]) == (T, C)
+        assert cfg["algorithmic_bytes_per_step"] == bench.algorithmic_bytes(name, T, C,
+                                                                            cfg["weighted"])
+    assert bench.workload_config("swiglu_moe", "e4m3", 1)["weighted"]
+    assert not bench.workload_config("swiglu_t", "e4m3", 1)["weighted"]
+    assert "larger than L2" in bench.workload_config("swiglu_t", "e4m3", 1)["l2"]
+    assert "flushed" in bench.workload_config("plain_outlier", "e4m3", 1)["l2"]
