@@ -60,10 +60,10 @@ def _nearest_codes(bits, fmt):
     magnitude every midpoint is below, which saturates."""
     mids = MIDS[fmt]
     mag = bits & np.uint32(0x7FFFFFFF)
-    k = np.searchsorted(mids, mag)
-    tie = mids[np.minimum(k, mids.size - 1)] == mag
-    code = k + (tie & (k % 2 == 1))
-    return code.astype(np.uint8) | ((bits >> np.uint32(24)).astype(np.uint8) & np.uint8(0x80))
+    k = np.searchsorted(mids, mag).astype(np.uint8)          # at most MAXCODE
+    tie = mids[np.minimum(k, np.uint8(mids.size - 1))] == mag
+    code = k + (tie & ((k & np.uint8(1)) == 1)).astype(np.uint8)
+    return code | ((bits >> np.uint32(24)).astype(np.uint8) & np.uint8(0x80))
 
 
 def _buffers(fmt):
