@@ -306,7 +306,7 @@ class Problem:
             self.outputs = [E((T, H)), E((T, H // 128), f32), E((H, T)), E((H, T // 128), f32)]
             o = self.outputs
             fn, args = tkq.tkq_swiglu_cast_t_clamp, [P(x), P(w), P(o[0]), P(o[1]), P(o[2]),
-                                                     P(o[3]), T, H, 128, fcode, CLAMP_VALUE,
+                                                     P(o[3]), T, H, 128, fcode, 0, CLAMP_VALUE,
                                                      P(self.count)]
             sf_pos = None
             self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(

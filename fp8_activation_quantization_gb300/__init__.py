@@ -26,7 +26,7 @@ __all__ = [
     "tkq_read_device_status", "tkq_selftest_wait_timeout", "FMT_E4M3", "FMT_E5M2", "GROUP",
     "tkq_per_channel_cast", "tkq_per_block_cast", "tkq_cast_back", "per_channel_cast",
     "per_block_cast", "cast_back", "OUT_F32", "OUT_BF16", "tkq_swiglu_cast_clamp",
-    "tkq_swiglu_cast_t_clamp", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
+    "tkq_swiglu_cast_t_clamp", "tkq_swiglu_cast_t_ex", "tkq_per_token_cast_f32", "tkq_swiglu_values", "swiglu_values",
     "use_checked_library", "tkq_checked_build", "tkq_read_check_address",
     "tkq_swiglu_backward_values", "swiglu_backward_values", "tkq_fp8_encode", "fp8_encode",
 ]
@@ -123,8 +123,10 @@ def _open(path):
         f32 = ctypes.c_float
         lib.tkq_swiglu_cast_clamp.argtypes = [p, p, p, p, i64, i64, i, i, u, f32, p, p]
         lib.tkq_swiglu_cast_clamp.restype = i
-        lib.tkq_swiglu_cast_t_clamp.argtypes = [p, p, p, p, p, p, i64, i64, i, i, f32, p, p]
+        lib.tkq_swiglu_cast_t_clamp.argtypes = [p, p, p, p, p, p, i64, i64, i, i, u, f32, p, p]
         lib.tkq_swiglu_cast_t_clamp.restype = i
+        lib.tkq_swiglu_cast_t_ex.argtypes = [p, p, p, p, p, p, i64, i64, i, i, u, p]
+        lib.tkq_swiglu_cast_t_ex.restype = i
         lib.tkq_per_token_cast_f32.argtypes = [p, p, p, i64, i64, i, i, u, p]
         lib.tkq_per_token_cast_f32.restype = i
         lib.tkq_swiglu_values.argtypes = [p, p, p, i64, i64, p]
@@ -224,9 +226,16 @@ def tkq_swiglu_cast_clamp(x, w, out, sf, T, H, group=GROUP, fmt=FMT_E4M3, sf_fla
 
 
 def tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3,
-                            clamp_value=0.0, clamp_count=None, stream=None) -> int:
-    return (_lib or load_library()).tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group, fmt,
-                                                  clamp_value, clamp_count, stream)
+                            sf_flags=0, clamp_value=0.0, clamp_count=None, stream=None) -> int:
+    return (_lib or load_library()).tkq_swiglu_cast_t_clamp(x, w, out, sf, out_t, sf_t, T, H, group,
+                                                            fmt, sf_flags, clamp_value, clamp_count,
+                                                            stream)
+
+
+def tkq_swiglu_cast_t_ex(x, w, out, sf, out_t, sf_t, T, H, group=GROUP, fmt=FMT_E4M3, sf_flags=0,
+                         stream=None) -> int:
+    return (_lib or load_library()).tkq_swiglu_cast_t_ex(x, w, out, sf, out_t, sf_t, T, H, group,
+                                                         fmt, sf_flags, stream)
 
 
 def tkq_per_channel_cast(x, out, sf, T, C, group=GROUP, fmt=FMT_E4M3, transpose=0,
@@ -394,7 +403,8 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
     """bf16 [T, 2H] (gate | up) -> (codes [T, H], scales [T, H/128]) and, with
     ``with_transpose``, also (codes_t [H, T], scales_t [H, T/128]).
     ``topk_weights``: optional fp32 [T] routing weight per row.  The scale-layout
-    options apply to the row scales of the cast without transpose.
+    options apply to the row scales and, with ``with_transpose``, to the column
+    scales as an [H, T/128] matrix (see ``sf_tensor`` for the shapes).
     ``use_clamp``: clamp the gate to <= swiglu_clamp_value and the up projection
     to [-swiglu_clamp_value, swiglu_clamp_value] before the SwiGLU; the number of
     changed values is added to ``clamp_count`` (a zeroed int64 CUDA tensor of one
@@ -419,8 +429,6 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
     g = max(num_per_channels, 1)
     _check_weights(topk_weights, T, x)
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
-    if flags and with_transpose:
-        raise ValueError("scale-layout options are not available with with_transpose")
     if out is None:
         out = torch.empty((T, H), dtype=_fp8_dtype(f), device=x.device)
     if out_sf is None:
@@ -441,14 +449,15 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
         if out_t is None:
             out_t = torch.empty((H, T), dtype=_fp8_dtype(f), device=x.device)
         if out_sf_t is None:
-            out_sf_t = torch.empty((H, T // g), dtype=torch.float32, device=x.device)
+            out_sf_t = sf_tensor(H, T // g, flags, x.device)
         if clamp is None:
-            st = tkq_swiglu_cast_t(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
-                                   _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f, stream)
+            st = tkq_swiglu_cast_t_ex(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
+                                      _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f,
+                                      flags, stream)
         else:
             st = tkq_swiglu_cast_t_clamp(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
                                          _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f,
-                                         clamp, _ptr(clamp_count), stream)
+                                         flags, clamp, _ptr(clamp_count), stream)
         if st:
             raise TkqError(st, "tkq_swiglu_cast_t")
         return out, out_sf, out_t, out_sf_t

@@ -70,38 +70,6 @@ struct alignas(1024) RowSmem {
     int abort;
 };
 
-// Where the scales of a launch go (tkq_sf_layout flags; see tkq.h).
-struct SfLayout {
-    unsigned flags;  // TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR
-                     // | TKQ_Q_RECIPROCAL
-    int groups;      // groups per row (G)
-    int words;       // ceil(G / 4), packed layouts
-    int64_t rows4;   // T rounded up to a multiple of 4, column-major layouts
-};
-constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u, kQReciprocal = 8u;
-
-// Scale of group gj of `row` in the chosen layout.  Padding rows of the
-// column-major layouts (T <= row < rows4) get 0, and the unused bytes of a
-// row's last packed word are zeroed by the lane of its last group.
-__device__ __forceinline__ void store_scale(void* sf, const SfLayout& lay, int64_t row,
-                                            bool live, int gj, float sc) {
-    const bool cm = lay.flags & kSfColMajor;
-    if (!live && !(cm && row < lay.rows4)) return;
-    if (lay.flags & kSfPacked) {
-        const uint8_t byte = live ? static_cast<uint8_t>(__float_as_uint(sc) >> 23) : 0;
-        const int64_t word = cm ? static_cast<int64_t>(gj >> 2) * lay.rows4 + row
-                                : row * lay.words + (gj >> 2);
-        uint8_t* p = static_cast<uint8_t*>(sf) + word * 4;
-        st_plain(p + (gj & 3), byte);
-        if (gj == lay.groups - 1)
-            for (int k = (gj & 3) + 1; k < 4; ++k) st_plain(p + k, uint8_t{0});
-    } else {
-        const int64_t idx = cm ? static_cast<int64_t>(gj) * lay.rows4 + row
-                               : row * lay.groups + gj;
-        st_plain(static_cast<float*>(sf) + idx, live ? sc : 0.0f);
-    }
-}
-
 // absmax of one 1x128 group held by eight lanes (16 values each), its scale,
 // and the codes and scale stored for a live row.  EXACT selects the codes of
 // the exact quotient (plain cast) or of the product by the reciprocal scale.
@@ -123,12 +91,8 @@ __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, 
     if constexpr (SFX) {
         if (lay.flags & kQReciprocal) exact_div = false;
         if (lay.flags & (kSfRoundPow2 | kSfPacked)) {
-            // round the scale up to a power of two; y / s = y * 2^-k is then
-            // exact, so the product needs no correction
-            uint32_t b = __float_as_uint(sc);
-            if (b & 0x007FFFFFu) b = (b & 0x7F800000u) + 0x00800000u;
-            sc = __uint_as_float(b);
-            inv = __uint_as_float((254u << 23) - b);
+            // y / s = y * 2^-k is then exact, so the product needs no correction
+            pow2_scale(sc, inv);
             exact_div = false;
         }
     }

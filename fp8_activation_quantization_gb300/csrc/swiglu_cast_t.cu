@@ -66,12 +66,15 @@ struct alignas(1024) SharedStorage {
     int abort;
 };
 
-template <int FMT, bool WEIGHTED, bool CLAMP>
+// SFX: the launch uses scale-layout options (lay_r for the row scales
+// [T, H/128], lay_c for the column scales [H, T/128]); without it both are
+// row-major fp32 as documented for tkq_swiglu_cast_t.
+template <int FMT, bool WEIGHTED, bool CLAMP, bool SFX>
 __global__ void __launch_bounds__(kThreads, 1)
     swiglu_cast_t_kernel(const __grid_constant__ CUtensorMap tmap, const float* __restrict__ w,
                          uint8_t* __restrict__ out, float* __restrict__ sf,
                          uint4* __restrict__ out_t, float* __restrict__ sf_t, int64_t T, int H,
-                         float clamp, uint32_t clamp2,
+                         SfLayout lay_r, SfLayout lay_c, float clamp, uint32_t clamp2,
                          unsigned long long* __restrict__ clamp_count,
                          unsigned int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
@@ -238,8 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // one of them publishes the row's reciprocal scale to the warp
             float s_own, inv_own;
             group_scale<FMT>(c, s_own, inv_own);
+            if constexpr (SFX) {
+                if (lay_r.flags & (kSfRoundPow2 | kSfPacked)) pow2_scale(s_own, inv_own);
+            }
             if ((lane & 3) == 0) {
-                st_stream(sf + (row0 + (lane >> 2)) * CB + cb, s_own);
+                if constexpr (SFX)
+                    store_scale(sf, lay_r, row0 + (lane >> 2), true, cb, s_own);
+                else
+                    st_stream(sf + (row0 + (lane >> 2)) * CB + cb, s_own);
                 sm.rowinv[warp][lane >> 2] = inv_own;
             }
             __syncwarp();
@@ -277,8 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 1; q < kConsumerWarps; ++q) m = fmaxf(m, sm.colmax[q][ct]);
             float s_c, inv_c;
             group_scale<FMT>(m, s_c, inv_c);
+            if constexpr (SFX) {
+                if (lay_c.flags & (kSfRoundPow2 | kSfPacked)) pow2_scale(s_c, inv_c);
+            }
             sm.cinv[ct] = inv_c;
-            st_stream(sf_t + static_cast<int64_t>(c0 + ct) * TB + tb, s_c);
+            if constexpr (SFX)
+                store_scale(sf_t, lay_c, c0 + ct, true, static_cast<int>(tb), s_c);
+            else
+                st_stream(sf_t + static_cast<int64_t>(c0 + ct) * TB + tb, s_c);
         }
         named_bar_sync(kBarConsumers, kConsumers);
 
@@ -320,54 +335,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int FMT, bool WEIGHTED, bool CLAMP>
+template <int FMT, bool WEIGHTED, bool CLAMP, bool SFX>
 cudaError_t launch(const void* x, const float* w, void* out, float* sf, void* out_t,
-                   float* sf_t, int64_t T, int64_t H, float clamp,
-                   unsigned long long* clamp_count, cudaStream_t stream) {
+                   float* sf_t, int64_t T, int64_t H, const SfLayout& lay_r,
+                   const SfLayout& lay_c, float clamp, unsigned long long* clamp_count,
+                   cudaStream_t stream) {
     // x as a bf16 [T, 2H] matrix (gate | up), read in 128 x 128 boxes
     CUtensorMap map;
     if (!encode_bf16_2d(&map, x, 2 * H, T, 128, 128)) return cudaErrorInvalidValue;
 
-    auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED, CLAMP>;
+    auto* k = &swiglu_cast_t_kernel<FMT, WEIGHTED, CLAMP, SFX>;
     const size_t smem = sizeof(SharedStorage) + 1024;
     const int64_t n_tiles = (T / 128) * (H / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_tiles);
     if (const cudaError_t e = upload_checks(stream)) return e;
     k<<<grid, kThreads, smem, stream>>>(map, w, static_cast<uint8_t*>(out), sf,
                                         static_cast<uint4*>(out_t), sf_t, T, static_cast<int>(H),
-                                        clamp, CLAMP ? bf16x2_bound(clamp) : 0u, clamp_count,
-                                        device_status_word());
+                                        lay_r, lay_c, clamp, CLAMP ? bf16x2_bound(clamp) : 0u,
+                                        clamp_count, device_status_word());
     return cudaGetLastError();
 }
 
-}  // namespace
+// The layout of a [rows, groups] scale matrix under sf_flags.
+SfLayout layout_of(unsigned sf_flags, int64_t rows, int64_t groups) {
+    SfLayout lay;
+    lay.flags = sf_flags;
+    lay.groups = static_cast<int>(groups);
+    lay.words = static_cast<int>((groups + 3) / 4);
+    lay.rows4 = (rows + 3) / 4 * 4;
+    return lay;
+}
 
-namespace {
 template <int FMT, bool CLAMP>
 cudaError_t launch_w(const void* x, const float* w, void* out, float* sf, void* out_t,
-                     float* sf_t, int64_t T, int64_t H, float clamp,
+                     float* sf_t, int64_t T, int64_t H, unsigned sf_flags, float clamp,
                      unsigned long long* clamp_count, cudaStream_t stream) {
-    return w ? launch<FMT, true, CLAMP>(x, w, out, sf, out_t, sf_t, T, H, clamp, clamp_count,
-                                        stream)
-             : launch<FMT, false, CLAMP>(x, w, out, sf, out_t, sf_t, T, H, clamp, clamp_count,
-                                         stream);
+    const SfLayout lr = layout_of(sf_flags, T, H / 128), lc = layout_of(sf_flags, H, T / 128);
+    if (sf_flags)
+        return w ? launch<FMT, true, CLAMP, true>(x, w, out, sf, out_t, sf_t, T, H, lr, lc, clamp,
+                                                  clamp_count, stream)
+                 : launch<FMT, false, CLAMP, true>(x, w, out, sf, out_t, sf_t, T, H, lr, lc,
+                                                   clamp, clamp_count, stream);
+    return w ? launch<FMT, true, CLAMP, false>(x, w, out, sf, out_t, sf_t, T, H, lr, lc, clamp,
+                                               clamp_count, stream)
+             : launch<FMT, false, CLAMP, false>(x, w, out, sf, out_t, sf_t, T, H, lr, lc, clamp,
+                                                clamp_count, stream);
 }
+
 }  // namespace
 
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
-                                 const float* clamp, unsigned long long* clamp_count,
-                                 cudaStream_t stream) {
+                                 unsigned sf_flags, const float* clamp,
+                                 unsigned long long* clamp_count, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const float c = clamp ? *clamp : 0.0f;
     if (fmt == kFmtE4M3)
-        return clamp ? launch_w<kFmtE4M3, true>(x, w, out, sf, out_t, sf_t, T, H, c, clamp_count,
-                                                stream)
-                     : launch_w<kFmtE4M3, false>(x, w, out, sf, out_t, sf_t, T, H, c, nullptr,
-                                                 stream);
-    return clamp ? launch_w<kFmtE5M2, true>(x, w, out, sf, out_t, sf_t, T, H, c, clamp_count,
-                                            stream)
-                 : launch_w<kFmtE5M2, false>(x, w, out, sf, out_t, sf_t, T, H, c, nullptr, stream);
+        return clamp ? launch_w<kFmtE4M3, true>(x, w, out, sf, out_t, sf_t, T, H, sf_flags, c,
+                                                clamp_count, stream)
+                     : launch_w<kFmtE4M3, false>(x, w, out, sf, out_t, sf_t, T, H, sf_flags, c,
+                                                 nullptr, stream);
+    return clamp ? launch_w<kFmtE5M2, true>(x, w, out, sf, out_t, sf_t, T, H, sf_flags, c,
+                                            clamp_count, stream)
+                 : launch_w<kFmtE5M2, false>(x, w, out, sf, out_t, sf_t, T, H, sf_flags, c,
+                                             nullptr, stream);
 }
 
 }  // namespace tkq

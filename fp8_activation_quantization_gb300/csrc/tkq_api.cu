@@ -409,23 +409,28 @@ tkq_status tkq_swiglu_backward_cast(const void* x, const void* dy, const float* 
 }
 
 namespace {
-tkq_status swiglu_cast_t_impl(const void* x, const float* w, void* out, float* sf, void* out_t,
-                              float* sf_t, int64_t T, int64_t H, int group, int fmt,
-                              const float* clamp, uint64_t* clamp_count, tkq_stream_t stream) {
+tkq_status swiglu_cast_t_impl(const void* x, const float* w, void* out, void* sf, void* out_t,
+                              void* sf_t, int64_t T, int64_t H, int group, int fmt,
+                              unsigned sf_flags, const float* clamp, uint64_t* clamp_count,
+                              tkq_stream_t stream) {
     tkq_status st = check_common(T, H, group, fmt);
     if (st != TKQ_OK) return st;
     if (T % group) return TKQ_ERR_SHAPE;
+    if (sf_flags & ~kSfAllFlags) return TKQ_ERR_FLAGS;
     if (clamp && !(*clamp > 0.0f && *clamp < INFINITY)) return TKQ_ERR_VALUE;
     if (T == 0) return TKQ_OK;
     // TMA box coordinates are 32-bit
     if (H > (int64_t{1} << 30) || T > INT32_MAX) return TKQ_ERR_SHAPE;
     if (!x || !out || !sf || !out_t || !sf_t) return TKQ_ERR_NULL;
     if (!tkq::aligned(x, 16) || !tkq::aligned(out, 16) || !tkq::aligned(out_t, 16) ||
-        !tkq::aligned(sf, 4) || !tkq::aligned(sf_t, 4) || (w && !tkq::aligned(w, 4)))
+        (w && !tkq::aligned(w, 4)))
         return TKQ_ERR_ALIGN;
+    if ((st = check_sf(sf, sf_flags)) != TKQ_OK || (st = check_sf(sf_t, sf_flags)) != TKQ_OK)
+        return st;
     const tkq::Range r[5] = {tkq::span(x, T * H * 4), tkq::span(out, T * H),
-                             tkq::span(sf, T * (H / group) * 4), tkq::span(out_t, T * H),
-                             tkq::span(sf_t, H * (T / group) * 4)};
+                             tkq::span(sf, tkq_sf_bytes(T, H / group, sf_flags)),
+                             tkq::span(out_t, T * H),
+                             tkq::span(sf_t, tkq_sf_bytes(H, T / group, sf_flags))};
     for (int i = 0; i < 5; ++i)
         for (int k = i + 1; k < 5; ++k)
             if (tkq::overlap(r[i], r[k])) return TKQ_ERR_ALIAS;
@@ -439,24 +444,32 @@ tkq_status swiglu_cast_t_impl(const void* x, const float* w, void* out, float* s
     const auto rc = clamp && clamp_count ? tkq::span(clamp_count, 8) : tkq::Range{0, 0};
     tkq::register_call({r[0], rw}, {r[1], r[2], r[3], r[4], rc});
     return launch_status(tkq::launch_swiglu_cast_t(
-        x, w, out, sf, out_t, sf_t, T, H, fmt, clamp,
-        reinterpret_cast<unsigned long long*>(clamp_count), static_cast<cudaStream_t>(stream)));
+        x, w, out, static_cast<float*>(sf), out_t, static_cast<float*>(sf_t), T, H, fmt, sf_flags,
+        clamp, reinterpret_cast<unsigned long long*>(clamp_count),
+        static_cast<cudaStream_t>(stream)));
 }
 }  // namespace
 
 tkq_status tkq_swiglu_cast_t(const void* x, const float* w, void* out, float* sf, void* out_t,
                              float* sf_t, int64_t T, int64_t H, int group, int fmt,
                              tkq_stream_t stream) {
-    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, nullptr, nullptr,
-                              stream);
+    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, 0u, nullptr,
+                              nullptr, stream);
 }
 
-tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, float* sf,
-                                   void* out_t, float* sf_t, int64_t T, int64_t H, int group,
-                                   int fmt, float clamp_value, uint64_t* clamp_count,
-                                   tkq_stream_t stream) {
-    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, &clamp_value,
-                              clamp_count, stream);
+tkq_status tkq_swiglu_cast_t_ex(const void* x, const float* w, void* out, void* sf, void* out_t,
+                                void* sf_t, int64_t T, int64_t H, int group, int fmt,
+                                unsigned sf_flags, tkq_stream_t stream) {
+    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, sf_flags, nullptr,
+                              nullptr, stream);
+}
+
+tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, void* sf,
+                                   void* out_t, void* sf_t, int64_t T, int64_t H, int group,
+                                   int fmt, unsigned sf_flags, float clamp_value,
+                                   uint64_t* clamp_count, tkq_stream_t stream) {
+    return swiglu_cast_t_impl(x, w, out, sf, out_t, sf_t, T, H, group, fmt, sf_flags,
+                              &clamp_value, clamp_count, stream);
 }
 
 tkq_status tkq_per_channel_cast(const void* x, void* out, float* sf, int64_t T, int64_t C,

@@ -184,6 +184,53 @@ __device__ __forceinline__ float quotient(float y, float s, float inv) {
 
 
 // ---------------------------------------------------------------------------
+// scale-factor layouts (the TKQ_SF_* flags of tkq.h)
+// ---------------------------------------------------------------------------
+
+// Where the scales of a launch go: a [rows, groups] matrix of scales in the
+// layout the flags select.
+struct SfLayout {
+    unsigned flags;  // TKQ_SF_ROUND_POW2 | TKQ_SF_UE8M0_PACKED | TKQ_SF_COL_MAJOR
+                     // | TKQ_Q_RECIPROCAL
+    int groups;      // groups per row (G)
+    int words;       // ceil(G / 4), packed layouts
+    int64_t rows4;   // rows rounded up to a multiple of 4, column-major layouts
+};
+constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u, kQReciprocal = 8u;
+
+// The scale rounded up to a power of two, s = 2^ceil(log2 s) (the mantissa
+// bits dropped and the exponent raised when any were set), and its reciprocal,
+// exact: 2^-k has the biased exponent 254 minus that of 2^k.
+__device__ __forceinline__ void pow2_scale(float& s, float& inv) {
+    uint32_t b = __float_as_uint(s);
+    if (b & 0x007FFFFFu) b = (b & 0x7F800000u) + 0x00800000u;
+    s = __uint_as_float(b);
+    inv = __uint_as_float((254u << 23) - b);
+}
+
+// Scale of group gj of `row` in the chosen layout.  Padding rows of the
+// column-major layouts (rows <= row < rows4) get 0, and the unused bytes of a
+// row's last packed word are zeroed by the lane of its last group.
+__device__ __forceinline__ void store_scale(void* sf, const SfLayout& lay, int64_t row,
+                                            bool live, int gj, float sc) {
+    const bool cm = lay.flags & kSfColMajor;
+    if (!live && !(cm && row < lay.rows4)) return;
+    if (lay.flags & kSfPacked) {
+        const uint8_t byte = live ? static_cast<uint8_t>(__float_as_uint(sc) >> 23) : 0;
+        const int64_t word = cm ? static_cast<int64_t>(gj >> 2) * lay.rows4 + row
+                                : row * lay.words + (gj >> 2);
+        uint8_t* p = static_cast<uint8_t*>(sf) + word * 4;
+        st_plain(p + (gj & 3), byte);
+        if (gj == lay.groups - 1)
+            for (int k = (gj & 3) + 1; k < 4; ++k) st_plain(p + k, uint8_t{0});
+    } else {
+        const int64_t idx = cm ? static_cast<int64_t>(gj) * lay.rows4 + row
+                               : row * lay.groups + gj;
+        st_plain(static_cast<float*>(sf) + idx, live ? sc : 0.0f);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Packed binary32 pairs: sm_100+ add / mul / fma .f32x2 perform two
 // independent IEEE operations per instruction, each rounded to nearest even
 // like the scalar one, so results are bit-identical to the scalar forms while

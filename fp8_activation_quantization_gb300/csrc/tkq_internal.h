@@ -79,10 +79,12 @@ cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const flo
                                         void* sf, int64_t T, int64_t H, int fmt,
                                         unsigned sf_flags, cudaStream_t stream);
 
+// sf_flags: TKQ_SF_* layout of both the row scales [T, H/128] and the column
+// scales [H, T/128] (0 = row-major fp32).
 cudaError_t launch_swiglu_cast_t(const void* x, const float* w, void* out, float* sf,
                                  void* out_t, float* sf_t, int64_t T, int64_t H, int fmt,
-                                 const float* clamp, unsigned long long* clamp_count,
-                                 cudaStream_t stream);
+                                 unsigned sf_flags, const float* clamp,
+                                 unsigned long long* clamp_count, cudaStream_t stream);
 
 // Per-channel cast (128-token groups; T % 128 == 0): codes [T, C] with sf
 // [T/128, C], or codes [C, T] with sf [C, T/128] when transpose.

@@ -179,7 +179,11 @@ tkq_status tkq_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T
 
 /* tkq_per_token_cast, tkq_swiglu_cast and tkq_swiglu_backward_cast with a
  * scale-factor layout (sf_flags above; sf sized by tkq_sf_bytes).  With
- * sf_flags == 0 they are the calls above. */
+ * sf_flags == 0 they are the calls above.  tkq_swiglu_cast_t_ex applies the
+ * same layout to both of its scale outputs: sf as a [T, H/128] matrix (sized
+ * tkq_sf_bytes(T, H/128, sf_flags)) and sf_t as an [H, T/128] matrix (sized
+ * tkq_sf_bytes(H, T/128, sf_flags)); the codes of both copies are those of
+ * the product by the reciprocal of the (possibly power-of-two) scale. */
 tkq_status tkq_per_token_cast_ex(const void* x, void* out, void* sf, int64_t T, int64_t C,
                                  int group, int fmt, unsigned sf_flags, tkq_stream_t stream);
 tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf, int64_t T,
@@ -188,6 +192,9 @@ tkq_status tkq_swiglu_cast_ex(const void* x, const float* w, void* out, void* sf
 tkq_status tkq_swiglu_backward_cast_ex(const void* x, const void* dy, const float* w, void* out,
                                        void* sf, int64_t T, int64_t H, int group, int fmt,
                                        unsigned sf_flags, tkq_stream_t stream);
+tkq_status tkq_swiglu_cast_t_ex(const void* x, const float* w, void* out, void* sf, void* out_t,
+                                void* sf_t, int64_t T, int64_t H, int group, int fmt,
+                                unsigned sf_flags, tkq_stream_t stream);
 
 /*
  * Device status word.  The pipelined kernels (every cast above) wait on
@@ -288,7 +295,7 @@ tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t 
  * equal to c is unchanged) is ADDED to *clamp_count: the caller zeroes the
  * counter, and consecutive calls accumulate (the page counts clamps with a sum
  * reducer and an atomic add; counting each changed value is this library's
- * reading).  Otherwise these are tkq_swiglu_cast_ex and tkq_swiglu_cast_t.
+ * reading).  Otherwise these are tkq_swiglu_cast_ex and tkq_swiglu_cast_t_ex.
  *   clamp_value : c, finite and > 0, else TKQ_ERR_VALUE
  *   clamp_count : DEVICE pointer to one uint64 (8-byte aligned, overlapping
  *                 no other buffer of the call), or NULL for no count.
@@ -296,10 +303,10 @@ tkq_status tkq_cast_back(const void* codes, const float* sf, void* out, int64_t 
 tkq_status tkq_swiglu_cast_clamp(const void* x, const float* w, void* out, void* sf, int64_t T,
                                  int64_t H, int group, int fmt, unsigned sf_flags,
                                  float clamp_value, uint64_t* clamp_count, tkq_stream_t stream);
-tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, float* sf,
-                                   void* out_t, float* sf_t, int64_t T, int64_t H, int group,
-                                   int fmt, float clamp_value, uint64_t* clamp_count,
-                                   tkq_stream_t stream);
+tkq_status tkq_swiglu_cast_t_clamp(const void* x, const float* w, void* out, void* sf,
+                                   void* out_t, void* sf_t, int64_t T, int64_t H, int group,
+                                   int fmt, unsigned sf_flags, float clamp_value,
+                                   uint64_t* clamp_count, tkq_stream_t stream);
 
 /*
  * Diagnostic (not an operation of the source pages): the fp32 SwiGLU values

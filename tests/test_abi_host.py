@@ -228,7 +228,7 @@ def test_swiglu_clamp_validation(lib, clamp, count_off, expected):
     count = p((4 << 20) + count_off)
     args = (p(), None, p(3 << 20), p(5 << 20), T, H, 128, 0, 0, clamp, count, None)
     assert lib.tkq_swiglu_cast_clamp(*args) == expected
-    args_t = (p(), None, p(3 << 20), p(5 << 20), p(6 << 20), p(7 << 20), T, H, 128, 0, clamp,
+    args_t = (p(), None, p(3 << 20), p(5 << 20), p(6 << 20), p(7 << 20), T, H, 128, 0, 0, clamp,
               count, None)
     assert lib.tkq_swiglu_cast_t_clamp(*args_t) == expected
 
@@ -290,3 +290,16 @@ def test_swiglu_backward_values_validation(lib, args, expected):
 ])
 def test_fp8_encode_validation(lib, args, expected):
     assert lib.tkq_fp8_encode(*args, None) == expected
+
+
+@pytest.mark.parametrize("flags,sf_t_addr,expected", [
+    (16, 7 << 20, 8),                      # unknown flag bit
+    (4, (7 << 20) + 4, 5),                 # column-major sf_t must be 16-byte aligned
+    (0, (7 << 20) + 4, 0),                 # empty batch: valid flags return OK, no launch
+    (6, (5 << 20) + 16, 7),                # sf_t inside sf (both sized by their layouts)
+])
+def test_swiglu_cast_t_ex_validation(lib, flags, sf_t_addr, expected):
+    T, H = (0 if expected == 0 else 256), 256
+    args = (p(), None, p(3 << 20), p(5 << 20), p(6 << 20), p(sf_t_addr), T, H, 128, 0, flags,
+            None)
+    assert lib.tkq_swiglu_cast_t_ex(*args) == expected

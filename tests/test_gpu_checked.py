@@ -77,7 +77,8 @@ def _cases(dev):
         x = to_dev_bf16(synth.swiglu_bf16(T + 1, H, T, H, gate_std=2.0), dev)
         w = _dev_f32(synth.routing_weights(T, 4, T // 8), dev) if weighted else None
         cnt = torch.zeros(1, dtype=torch.int64, device=dev)
-        kw = dict(topk_weights=w, with_transpose=True)
+        kw = dict(topk_weights=w, with_transpose=True,
+                  use_packed_ue8m0=bool(T == 384), use_tma_aligned_col_major_sf=bool(T >= 256))
         if clamp is not None:
             kw.update(use_clamp=True, swiglu_clamp_value=clamp, clamp_count=cnt)
 

@@ -71,7 +71,8 @@ def run_clamp(x_bits, w, fmt, clamp, dev, transposed=False, count=None, sf_flags
     out_t = Guarded(T * H, dev)
     sf_t = Guarded(H * (T // 128) * 4, dev)
     st = tkq.tkq_swiglu_cast_t_clamp(ctypes.c_void_p(xd.data_ptr()), wp, out.ptr, sf.ptr,
-                                     out_t.ptr, sf_t.ptr, T, H, 128, f, clamp, cp, stream_of(dev))
+                                     out_t.ptr, sf_t.ptr, T, H, 128, f, 0, clamp, cp,
+                                     stream_of(dev))
     assert st == 0, tkq.tkq_status_string(st)
     torch.cuda.synchronize()
     for g, n in ((out, "out"), (sf, "sf"), (out_t, "out_t"), (sf_t, "sf_t")):

@@ -54,6 +54,8 @@ def _ops(dev):
         "swiglu_t weighted": lambda: tkq.swiglu_forward_and_per_token_cast(
             xs, topk_weights=w, with_transpose=True),
         "swiglu_t clamp": clamped(with_transpose=True, swiglu_clamp_value=2.9),
+        "swiglu_t ue8m0 col-major": lambda: tkq.swiglu_forward_and_per_token_cast(
+            xs, with_transpose=True, use_packed_ue8m0=True, use_tma_aligned_col_major_sf=True),
         "backward weighted": lambda: tkq.swiglu_backward_and_per_token_cast(xs, dy, topk_weights=w),
         "per_channel": lambda: tkq.per_channel_cast(xs),
         "per_channel_t": lambda: tkq.per_channel_cast(xs, transpose=True),

@@ -13,7 +13,9 @@ where y is then 0; the codes there are a signed zero either way).
 
 Then the casts are shown to quantize exactly these values: the SwiGLU cast's
 scales equal bit for bit the oracle's scale rule applied to the diagnostic y,
-and its codes equal the oracle's codes of that y except at FP8 ties.
+and its codes equal the oracle's codes of that y except at FP8 ties (and bit
+for bit the codes of the oracle's reciprocal-multiply reading, the product by
+fl32(1 / s) that the kernels compute), with and without scale layouts.
 """
 from __future__ import annotations
 
@@ -120,12 +122,18 @@ def test_casts_quantize_these_values(cuda_device, weighted):
     parity.assert_bit_exact("scales", s.cpu().numpy(), e_s)
     parity.assert_codes_differ_only_at_ties("codes", q.view(torch.uint8).cpu().numpy(), e_q,
                                             y / np.repeat(e_s, 128, axis=1), "e4m3")
+    # the codes are exactly the reciprocal-multiply reading of y
+    e_qr, _ = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.Q_RECIPROCAL)
+    parity.assert_bit_exact("codes (reciprocal reading)", q.view(torch.uint8).cpu().numpy(), e_qr)
     # the transposed kernel quantizes the same y as well
     q2, s2, qt, st = tkq.swiglu_forward_and_per_token_cast(xd, topk_weights=wd, with_transpose=True)
     e_qt, e_st = oracle.cast_cols_f32(y, "e4m3")
     parity.assert_bit_exact("column scales", st.cpu().numpy(), e_st)
     parity.assert_codes_differ_only_at_ties("column codes", qt.view(torch.uint8).cpu().numpy(), e_qt,
                                             y.T / np.repeat(e_st, 128, axis=1), "e4m3")
+    e_qtr, _ = oracle.cast_rows_f32_ex(np.ascontiguousarray(y.T), "e4m3", 128, oracle.Q_RECIPROCAL)
+    parity.assert_bit_exact("column codes (reciprocal reading)",
+                            qt.view(torch.uint8).cpu().numpy(), e_qtr)
 
 
 @pytest.mark.slow
@@ -135,7 +143,8 @@ def test_full_workloads_quantize_these_values(cuda_device, name):
     workload (the benchmark's step): every row scale, and for the transposed
     cast every column scale, equals bit for bit the oracle's scale rule applied
     to the kernels' own y; every code equals the oracle's code of that y except
-    at FP8 ties."""
+    at FP8 ties, and equals bit for bit the code of its reciprocal-multiply
+    reading (the product by fl32(1 / s), which is what the kernels compute)."""
     d = synth.workload(name)
     x, w = d["x"], d.get("w")
     xd = to_dev_bf16(x, cuda_device)
@@ -150,10 +159,53 @@ def test_full_workloads_quantize_these_values(cuda_device, name):
     parity.assert_bit_exact("row scales", s.cpu().numpy(), e_s)
     parity.assert_codes_differ_only_at_ties("row codes", q.view(torch.uint8).cpu().numpy(), e_q,
                                             y / np.repeat(e_s, 128, axis=1), "e4m3")
-    del e_q, e_s, q, s
+    e_qr, _ = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.Q_RECIPROCAL, threads=16)
+    parity.assert_bit_exact("row codes (reciprocal reading)", q.view(torch.uint8).cpu().numpy(),
+                            e_qr)
+    del e_q, e_s, e_qr, q, s
     if name == "swiglu_t":
         e_qt, e_st = oracle.cast_cols_f32(y, "e4m3")
         parity.assert_bit_exact("column scales", st.cpu().numpy(), e_st)
         parity.assert_codes_differ_only_at_ties(
             "column codes", qt.view(torch.uint8).cpu().numpy(), e_qt,
             y.T / np.repeat(e_st, 128, axis=1), "e4m3")
+        del e_qt
+        e_qtr, _ = oracle.cast_rows_f32_ex(np.ascontiguousarray(y.T), "e4m3", 128,
+                                           oracle.Q_RECIPROCAL, threads=16)
+        parity.assert_bit_exact("column codes (reciprocal reading)",
+                                qt.view(torch.uint8).cpu().numpy(), e_qtr)
+
+
+def _raw(t):
+    return np.ascontiguousarray(t.contiguous().view(torch.uint8).cpu().numpy()).ravel()
+
+
+@pytest.mark.parametrize("flags,fmt", [(1, "e4m3"), (2, "e4m3"), (4, "e4m3"), (6, "e5m2"),
+                                       (7, "e4m3"), (8, "e5m2")])
+def test_transposed_cast_layouts_quantize_these_values(cuda_device, flags, fmt):
+    """The transposed cast with a scale layout: its row codes and scales, and
+    its column codes and scales (an [H, T/128] matrix in the same layout),
+    equal bit for bit the oracle's reciprocal-multiply reading of the kernels'
+    own y in that layout (rows of y, rows of y transposed); the row outputs
+    equal the row cast's with the same flags.  T = 384 and H = 640 leave
+    partly used packed words on both scale matrices."""
+    T, H = 384, 640
+    x = synth.swiglu_bf16(61, 3, T, H, gate_std=2.0)
+    w = synth.routing_weights(62, 4, T // 8)
+    xd = to_dev_bf16(x, cuda_device)
+    wd = torch.from_numpy(w).to(cuda_device)
+    opts = dict(round_sf=bool(flags & 1), use_packed_ue8m0=bool(flags & 2),
+                use_tma_aligned_col_major_sf=bool(flags & 4))
+    y = tkq.swiglu_values(xd, wd).cpu().numpy()
+    q, s, qt, st = tkq.swiglu_forward_and_per_token_cast(xd, fmt, topk_weights=wd,
+                                                         with_transpose=True, **opts)
+    e_q, e_s = oracle.cast_rows_f32_ex(y, fmt, 128, flags | oracle.Q_RECIPROCAL)
+    e_qt, e_st = oracle.cast_rows_f32_ex(np.ascontiguousarray(y.T), fmt, 128,
+                                         flags | oracle.Q_RECIPROCAL)
+    parity.assert_bit_exact("row codes", q.view(torch.uint8).cpu().numpy(), e_q)
+    parity.assert_bit_exact("row scales (layout bytes)", _raw(s), e_s.view(np.uint8).ravel())
+    parity.assert_bit_exact("column codes", qt.view(torch.uint8).cpu().numpy(), e_qt)
+    parity.assert_bit_exact("column scales (layout bytes)", _raw(st), e_st.view(np.uint8).ravel())
+    q2, s2 = tkq.swiglu_forward_and_per_token_cast(xd, fmt, topk_weights=wd, **opts)
+    assert torch.equal(q.view(torch.uint8), q2.view(torch.uint8))
+    assert np.array_equal(_raw(s), _raw(s2))

@@ -140,7 +140,8 @@ def test_random_values_within_the_bound(cuda_device):
 
 def _cast_matches_values(x, dy, w, dev, fmt="e4m3"):
     """The backward cast's scales = the oracle's scale rule on the diagnostic
-    values (bit for bit); its codes = the oracle's codes of them except at ties."""
+    values (bit for bit); its codes = the oracle's codes of them except at ties,
+    and bit for bit those of the reciprocal-multiply reading."""
     xd, dyd = to_dev_bf16(x, dev), to_dev_bf16(dy, dev)
     wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(dev)
     y = tkq.swiglu_backward_values(xd, dyd, wd).cpu().numpy()
@@ -149,6 +150,8 @@ def _cast_matches_values(x, dy, w, dev, fmt="e4m3"):
     parity.assert_bit_exact("scales", s.cpu().numpy(), e_s)
     parity.assert_codes_differ_only_at_ties("codes", q.view(torch.uint8).cpu().numpy(), e_q,
                                             y / np.repeat(e_s, 128, axis=1), fmt)
+    e_qr, _ = oracle.cast_rows_f32_ex(y, fmt, 128, oracle.Q_RECIPROCAL, threads=16)
+    parity.assert_bit_exact("codes (reciprocal reading)", q.view(torch.uint8).cpu().numpy(), e_qr)
 
 
 @pytest.mark.parametrize("T,H,weighted,fmt", [(1, 128, False, "e4m3"), (129, 384, True, "e4m3"),
