@@ -249,6 +249,7 @@ class Problem:
         E = lambda shape, dt=u8: torch.empty(shape, dtype=dt, device=dev)
         opt = dict(round_sf=bool(sf_flags & 1), use_packed_ue8m0=bool(sf_flags & 2),
                    use_tma_aligned_col_major_sf=bool(sf_flags & 4))
+        sf_done = False   # a branch that handles sf_flags itself
         if kern == "per_token_cast":
             self.outputs = [E((T, C)), E((T, C // 128), f32)]
             fn, args = tkq.tkq_per_token_cast, [P(x), P(self.outputs[0]), None, T, C, 128, fcode]
@@ -292,14 +293,25 @@ class Problem:
                 out_sf=od[1], **opt)
         elif kern == "swiglu_cast_t":
             H = C // 2
-            self.outputs = [E((T, H)), E((T, H // 128), f32), E((H, T)), E((H, T // 128), f32)]
+            if sf_flags:
+                # both scale outputs in the layout the flags select
+                self.outputs = [E((T, H)), E((tkq.tkq_sf_bytes(T, H // 128, sf_flags),)),
+                                E((H, T)), E((tkq.tkq_sf_bytes(H, T // 128, sf_flags),))]
+            else:
+                self.outputs = [E((T, H)), E((T, H // 128), f32), E((H, T)),
+                                E((H, T // 128), f32)]
             o = self.outputs
-            fn, args = tkq.tkq_swiglu_cast_t, [P(x), P(w), P(o[0]), P(o[1]), P(o[2]), P(o[3]),
-                                               T, H, 128, fcode]
+            args = [P(x), P(w), P(o[0]), P(o[1]), P(o[2]), P(o[3]), T, H, 128, fcode]
+            if sf_flags:
+                fn = tkq.tkq_swiglu_cast_t_ex
+                args.append(sf_flags)
+            else:
+                fn = tkq.tkq_swiglu_cast_t
             sf_pos = None
+            sf_done = True
             self.api = lambda i, od: tkq.swiglu_forward_and_per_token_cast(
                 i["x"], fmt, topk_weights=i.get("w"), with_transpose=True,
-                out=od[0].view(fp8), out_sf=od[1], out_t=od[2].view(fp8), out_sf_t=od[3])
+                out=od[0].view(fp8), out_sf=od[1], out_t=od[2].view(fp8), out_sf_t=od[3], **opt)
         elif kern == "swiglu_cast_t_clamp":
             H = C // 2
             self.count = E((1,), torch.int64).zero_()
@@ -354,8 +366,8 @@ class Problem:
                       "swiglu_cast": tkq.tkq_swiglu_cast_ex,
                       "swiglu_backward_cast": tkq.tkq_swiglu_backward_cast_ex}[kern]
             args[sf_pos] = P(self.outputs[1])
-        elif sf_flags:
-            raise ValueError("scale-layout options apply to the row casts only")
+        elif sf_flags and not sf_done:
+            raise ValueError("scale-layout options apply to the row and transposed casts only")
         self._fn, self._args = fn, tuple(args)
 
     def launch(self, stream):
@@ -688,6 +700,7 @@ def other_workloads(dev, stream, peak, args):
                              ("plain_outlier", "e4m3", 8),
                              ("swiglu", "e4m3", 0), ("swiglu_moe", "e4m3", 0),
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
+                             ("swiglu_t", "e4m3", 6),
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
                              ("per_channel_t", "e4m3", 0), ("per_block", "e4m3", 0),
                              ("cast_back", "e4m3", 0), ("swiglu_clamp", "e4m3", 0),
