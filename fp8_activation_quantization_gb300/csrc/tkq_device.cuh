@@ -42,8 +42,9 @@ struct FmtTraits<kFmtE5M2> {
 // of the current call: its inputs for a load, its outputs for a store.  The
 // ABI layer registers those buffers per call and each launcher copies the
 // table to its translation unit's copy on the launch stream before the launch.
-// An access outside them is skipped (no fault), sets kDeviceOutOfBounds in the
-// device status word and records the first such address (bit 63 set for a
+// An access not wholly inside them is skipped (no fault), sets
+// kDeviceOutOfBounds in the device status word and records the first byte of
+// the first such access that lies outside the buffers (bit 63 set for a
 // store).  It stands in for a memory checker; the checked library is a test
 // build, one launch at a time (the table is shared by a translation unit's
 // launches).  In the release build the checks compile away.
@@ -61,12 +62,15 @@ inline cudaError_t upload_checks(cudaStream_t) { return cudaSuccess; }
 __device__ __forceinline__ bool access_ok(const void* p, unsigned bytes, bool write) {
 #ifdef TKQ_CHECKED
     const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    unsigned long long first_out = a;   // first byte of the access outside the buffers
     for (int k = 0; k < g_check.n; ++k)
-        if (a >= g_check.lo[k] && a + bytes <= g_check.hi[k] &&
-            (!write || ((g_check.writable >> k) & 1u)))
-            return true;
+        if (a >= g_check.lo[k] && a < g_check.hi[k] &&
+            (!write || ((g_check.writable >> k) & 1u))) {
+            if (a + bytes <= g_check.hi[k]) return true;
+            first_out = g_check.hi[k];
+        }
     if (g_check.status) atomicOr(g_check.status, kDeviceOutOfBounds);
-    if (g_check.bad) atomicCAS(g_check.bad, 0ull, a | (write ? (1ull << 63) : 0ull));
+    if (g_check.bad) atomicCAS(g_check.bad, 0ull, first_out | (write ? (1ull << 63) : 0ull));
     return false;
 #else
     (void)p;

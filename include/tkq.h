@@ -348,8 +348,9 @@ tkq_status tkq_fp8_encode(const float* x, void* out, int64_t n, int fmt, tkq_str
  * a test build in which every global load and store of the kernels is first
  * checked against the buffers of the current call (loads: its inputs and
  * outputs; stores: its outputs, sized as documented for each call).  An access
- * outside them is skipped, sets TKQ_DEVICE_OUT_OF_BOUNDS in the device status
- * word (tkq_read_device_status) and records the first such address, read with
+ * not wholly inside them is skipped, sets TKQ_DEVICE_OUT_OF_BOUNDS in the
+ * device status word (tkq_read_device_status) and records the first byte of
+ * the first such access that lies outside the buffers, read with
  * tkq_read_check_address (bit 63 set for a store).  The checked build keeps one
  * table per kernel source file, so its calls must not run concurrently.  In
  * the release build no access is checked: the status bit is never set and the
