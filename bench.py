@@ -62,7 +62,7 @@ SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu",
 # one value in 10^4 is clamped; the clamp runs on every element either way)
 CLAMP_VALUE = 4.0
 KERNEL_SOURCES = {
-    "per_token_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_token_cast": ["token_cast.cu", "tkq_device.cuh"],
     "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_backward_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
@@ -72,7 +72,7 @@ KERNEL_SOURCES = {
     "cast_back": ["cast_back.cu", "tkq_device.cuh"],
     "swiglu_cast_clamp": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t_clamp": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
-    "per_token_cast_f32": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "per_token_cast_f32": ["token_cast.cu", "tkq_device.cuh"],
 }
 
 

@@ -1,10 +1,10 @@
-// row_cast.cu -- the per-token-group FP8 casts with row-major outputs:
-//   * the plain per_token_cast of a bf16 or fp32 [T, C] matrix ("DeepSeek开源
-//     TileKernels：用Python写的GPU算子逼近硬件性能上限" (itsolotime.com) §3.2);
+// row_cast.cu -- the per-token-group FP8 casts of SwiGLU values with
+// row-major outputs (the plain per_token_cast is token_cast.cu):
 //   * swiglu_forward_and_per_token_cast of a bf16 [T, 2H] gate|up matrix,
 //     optionally times a per-row routing weight and with the optional clamp
-//     (gate <= c, -c <= up <= c) whose changed values are counted (same page,
-//     §3.3);
+//     (gate <= c, -c <= up <= c) whose changed values are counted
+//     ("DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件性能上限"
+//     (itsolotime.com) §3.3);
 //   * swiglu_backward_and_per_token_cast ("TileKernels 与 DeepGEMM 的分界线"
 //     (chatdocs.ruinique.com) §2 and §6 step 13): the gradients [dg | du] of
 //     the same SwiGLU from the upstream gradient dy, cast per token.
@@ -12,19 +12,17 @@
 //
 // GB300 design: persistent CTAs (3 per SM) stream "chunks" of 32 rows x one
 // 128-channel block.  Warp 8 is the producer: one lane loads each chunk with
-// one 2-D TMA box per operand (32 x 128 bf16 = 8 KB: x; or gate and up; or
-// gate, up and dy; 16 KB of fp32 x) into a shared ring of 64-72 KB (8 plain,
-// 4 SwiGLU or fp32, 3 backward chunks in flight per CTA).  Rows past T are
+// one 2-D TMA box per operand (32 x 128 bf16 = 8 KB: gate and up; or gate, up
+// and dy) into a shared ring of 64-72 KB (4 SwiGLU, 3 backward chunks in
+// flight per CTA).  Rows past T are
 // zero-filled by the TMA unit and never stored, so ragged T needs no special
 // path.  Warps 0..7 are
 // consumers: warp w owns rows 4w..4w+3 of the chunk, eight lanes per row
 // (lane j holds elements [8j, 8j+8) and [64+8j, 64+8j+8), read as two
 // conflict-free 16-byte shared loads per operand), the group absmax is three
 // xor shuffles, and codes leave as 8-byte stores (eight lanes write one
-// 64-byte run).  The plain casts write the codes of the exact binary32
-// quotient fl(x / s) (`quotient` / `quotient2`), so they are bit-exact, or
-// with TKQ_Q_RECIPROCAL those of x * fl(1 / s); the SwiGLU casts write the
-// codes of y * fl(1 / s) as the page's kernel does.
+// 64-byte run).  The codes are those of y * fl(1 / s), as the page's kernel
+// computes them.
 // Elementwise fp32 steps run on packed pairs (tkq_device.cuh); a clamp bound
 // that is a bf16 value is applied, and its changes counted, on the packed bf16
 // input pairs before they are widened (same values, half the instructions).
@@ -44,8 +42,7 @@ constexpr int kRows = 32;                 // rows per chunk (4 per consumer warp
 constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
 
 enum Mode {
-    kPlain, kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kBackward,
-    kBackwardWeighted, kPlainF32
+    kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kBackward, kBackwardWeighted
 };
 
 template <int MODE>
@@ -54,9 +51,8 @@ struct ModeTraits {
     static constexpr bool kClamp = MODE == kSwigluClamp || MODE == kSwigluWeightedClamp;
     static constexpr bool kWeighted =
         MODE == kSwigluWeighted || MODE == kSwigluWeightedClamp || MODE == kBackwardWeighted;
-    static constexpr bool kF32 = MODE == kPlainF32;   // fp32 input, 32 x 128 fp32 boxes
-    static constexpr int kOperands = (MODE == kPlain || kF32) ? 1 : (kBwd ? 3 : 2);  // boxes
-    static constexpr int kRowBytes = kF32 ? 512 : 256;  // one box row in shared memory
+    static constexpr int kOperands = kBwd ? 3 : 2;  // boxes per chunk
+    static constexpr int kRowBytes = 256;            // one box row in shared memory
     static constexpr int kStageBytes = kOperands * kRows * kRowBytes;
     static constexpr int kRingBytes = kBwd ? 3 * kStageBytes : 65536;
     static constexpr int kStages = kRingBytes / kStageBytes;
@@ -71,13 +67,10 @@ struct alignas(1024) RowSmem {
 };
 
 // absmax of one 1x128 group held by eight lanes (16 values each), its scale,
-// and the codes and scale stored for a live row.  EXACT selects the codes of
-// the exact quotient (plain cast) or of the product by the reciprocal scale.
-// SFX: the launch uses scale-layout options (power-of-two scales, packed
-// UE8M0, column-major) or the reciprocal reading of the plain cast's codes
-// (products by fl32(1/s) instead of exact quotients); without it the scales
-// are row-major fp32 at sfp.
-template <int FMT, bool EXACT, bool SFX>
+// and the codes (of the products by fl32(1/s)) and scale stored for a live
+// row.  SFX: the launch uses scale-layout options (power-of-two scales, packed
+// UE8M0, column-major); without it the scales are row-major fp32 at sfp.
+template <int FMT, bool SFX>
 __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, float* sfp,
                                            int j, void* sf, const SfLayout& lay, int64_t row,
                                            int gj) {
@@ -87,26 +80,12 @@ __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, 
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
     float sc, inv;
     group_scale<FMT>(m, sc, inv);
-    bool exact_div = EXACT;
     if constexpr (SFX) {
-        if (lay.flags & kQReciprocal) exact_div = false;
-        if (lay.flags & (kSfRoundPow2 | kSfPacked)) {
-            // y / s = y * 2^-k is then exact, so the product needs no correction
-            pow2_scale(sc, inv);
-            exact_div = false;
-        }
+        if (lay.flags & (kSfRoundPow2 | kSfPacked)) pow2_scale(sc, inv);  // inv = 2^-k exactly
     }
     if (live) {
-        uint2 lo, hi;
-        if (exact_div) {
-            lo = quantize8<FMT>(v, sc, inv);
-            hi = quantize8<FMT>(v + 8, sc, inv);
-        } else {
-            lo = quantize8_mul<FMT>(v, inv);
-            hi = quantize8_mul<FMT>(v + 8, inv);
-        }
-        st_stream(o + j, lo);
-        st_stream(o + 8 + j, hi);
+        st_stream(o + j, quantize8_mul<FMT>(v, inv));
+        st_stream(o + 8 + j, quantize8_mul<FMT>(v + 8, inv));
     }
     if (j == 0) {
         if constexpr (SFX) {
@@ -121,18 +100,6 @@ __device__ __forceinline__ void emit_group(const float* v, bool live, uint2* o, 
 __device__ __forceinline__ void load16(const uint8_t* p, float* v) {
     unpack8(*reinterpret_cast<const uint4*>(p), v);
     unpack8(*reinterpret_cast<const uint4*>(p + 128), v + 8);
-}
-
-// The same 16 elements of an fp32 box row (p = row + 32 j): four 16-byte loads.
-// (Eight lanes of a row then read 256 bytes at a 32-byte stride, a 2-way bank
-// conflict; shared-memory bandwidth is not what bounds this mode.)
-__device__ __forceinline__ void load16_f32(const uint8_t* p, float* v) {
-    const float4* q = reinterpret_cast<const float4*>(p);
-    const float4* h = reinterpret_cast<const float4*>(p + 256);
-    *reinterpret_cast<float4*>(v) = q[0];
-    *reinterpret_cast<float4*>(v + 4) = q[1];
-    *reinterpret_cast<float4*>(v + 8) = h[0];
-    *reinterpret_cast<float4*>(v + 12) = h[1];
 }
 
 // The SwiGLU clamp of one launch: bound c (> 0), the counter that the number
@@ -188,8 +155,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 uint64_t* full = &sm.full[pos.stage];
                 mbar_arrive_expect_tx(full, MT::kStageBytes);
                 tma_load_2d(dst, &tmap, x0, y0, full);
-                if constexpr (MT::kOperands >= 2)
-                    tma_load_2d(dst + kBoxBytes, &tmap, C_out + x0, y0, full);
+                tma_load_2d(dst + kBoxBytes, &tmap, C_out + x0, y0, full);
                 if constexpr (MT::kOperands == 3)
                     tma_load_2d(dst + 2 * kBoxBytes, &tmap_dy, x0, y0, full);
                 pos.advance();
@@ -233,15 +199,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         const uint8_t* p = sm.stage[s] + r * MT::kRowBytes + j * (MT::kRowBytes / 16);
         uint2* o = out + (row * out_ld + cb * 128) / 8;
         float* sfp = sf + row * sf_ld + cb;
-        if constexpr (MODE == kPlain) {
-            float v[16];
-            load16(p, v);
-            emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
-        } else if constexpr (MT::kF32) {
-            float v[16];
-            load16_f32(p, v);
-            emit_group<FMT, true, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
-        } else if constexpr (!MT::kBwd) {
+        if constexpr (!MT::kBwd) {
             float g[16], u[16], v[16];
             if constexpr (MT::kClamp) {
                 uint4 gq[2] = {*reinterpret_cast<const uint4*>(p),
@@ -290,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 v[k] = y.x;
                 v[k + 1] = y.y;
             }
-            emit_group<FMT, false, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
+            emit_group<FMT, SFX>(v, live, o, sfp, j, sf, lay, row, cb);
         } else {
             float g[16], u[16], d[16], dg[16], du[16];
             load16(p, g);
@@ -310,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 3)
                 du[k] = b.x;
                 du[k + 1] = b.y;
             }
-            emit_group<FMT, false, SFX>(dg, live, o, sfp, j, sf, lay, row, cb);
-            emit_group<FMT, false, SFX>(du, live, o + C_out / 8, sfp + CB, j, sf, lay, row,
+            emit_group<FMT, SFX>(dg, live, o, sfp, j, sf, lay, row, cb);
+            emit_group<FMT, SFX>(du, live, o + C_out / 8, sfp + CB, j, sf, lay, row,
                                           static_cast<int>(CB) + cb);
         }
         // Release the stage only now: the stores above consume every value
@@ -352,12 +310,9 @@ cudaError_t launch(const void* x, const void* dy, const float* w, void* out, voi
                    int64_t T, int64_t C_out, unsigned sf_flags, Clamp clamp,
                    cudaStream_t stream) {
     using MT = ModeTraits<MODE>;
-    // x as a bf16 [T, cols] matrix: C columns (plain) or 2H (gate | up)
-    const int64_t cols = (MT::kOperands == 1 ? 1 : 2) * C_out;
+    // x as a bf16 [T, 2H] matrix (gate | up)
     CUtensorMap map, map_dy;
-    const bool mapped = MT::kF32 ? encode_f32_2d(&map, x, cols, T, 128, kRows)
-                                 : encode_bf16_2d(&map, x, cols, T, 128, kRows);
-    if (!mapped) return cudaErrorInvalidValue;
+    if (!encode_bf16_2d(&map, x, 2 * C_out, T, 128, kRows)) return cudaErrorInvalidValue;
     if constexpr (MT::kBwd) {
         if (!encode_bf16_2d(&map_dy, dy, C_out, T, 128, kRows)) return cudaErrorInvalidValue;
     } else {
@@ -387,16 +342,6 @@ cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, v
 }
 
 }  // namespace
-
-cudaError_t launch_per_token_cast(const void* x, void* out, void* sf, int64_t T, int64_t C,
-                                  int fmt, unsigned sf_flags, cudaStream_t stream) {
-    return launch_fmt<kPlain>(fmt, x, nullptr, nullptr, out, sf, T, C, sf_flags, stream);
-}
-
-cudaError_t launch_per_token_cast_f32(const float* x, void* out, void* sf, int64_t T, int64_t C,
-                                      int fmt, unsigned sf_flags, cudaStream_t stream) {
-    return launch_fmt<kPlainF32>(fmt, x, nullptr, nullptr, out, sf, T, C, sf_flags, stream);
-}
 
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
                                int64_t H, int fmt, unsigned sf_flags, const float* clamp,

@@ -118,11 +118,6 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t ro
                      box_rows);
 }
 
-bool encode_f32_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                   uint32_t box_cols, uint32_t box_rows) {
-    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, cols, rows, box_cols,
-                     box_rows);
-}
 
 unsigned int* device_status_word() {
     int dev = 0;

@@ -15,9 +15,6 @@ namespace tkq {
 // or rejects the arguments.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
                     uint32_t box_cols, uint32_t box_rows);
-// The same for a row-major fp32 matrix (row stride cols * 4 bytes).
-bool encode_f32_2d(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                   uint32_t box_cols, uint32_t box_rows);
 
 // Number of SMs of the current device (cached per device; the environment
 // variable TKQ_NUM_SMS overrides it for grid sizing experiments).
