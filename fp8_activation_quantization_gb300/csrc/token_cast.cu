@@ -155,11 +155,12 @@ cudaError_t launch(const void* x, void* out, void* sf, int64_t T, int64_t C, int
     const int64_t n_walk = (sf_flags & kSfColMajor) ? lay.rows4 * lay.groups : n_groups;
     float* s = static_cast<float*>(sf);
     if (fmt == kFmtE4M3)
-        return sf_flags ? launch_layout<kFmtE4M3, F32, true>(x, out, s, lay, n_groups, n_walk, stream)
-                        : launch_layout<kFmtE4M3, F32, false>(x, out, s, lay, n_groups, n_walk,
-                                                              stream);
-    return sf_flags ? launch_layout<kFmtE5M2, F32, true>(x, out, s, lay, n_groups, n_walk, stream)
-                    : launch_layout<kFmtE5M2, F32, false>(x, out, s, lay, n_groups, n_walk, stream);
+        return sf_flags
+                   ? launch_layout<kFmtE4M3, F32, true>(x, out, s, lay, n_groups, n_walk, stream)
+                   : launch_layout<kFmtE4M3, F32, false>(x, out, s, lay, n_groups, n_walk, stream);
+    return sf_flags
+               ? launch_layout<kFmtE5M2, F32, true>(x, out, s, lay, n_groups, n_walk, stream)
+               : launch_layout<kFmtE5M2, F32, false>(x, out, s, lay, n_groups, n_walk, stream);
 }
 
 }  // namespace
