@@ -80,6 +80,18 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
     int64_t u = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
 
+    // row and group-in-row of this lane's group, for the scale layouts: found
+    // by one division here, then advanced by the fixed stride with one carry
+    int64_t row = 0, drow = 0;
+    int gj = 0, dgj = 0;
+    if constexpr (SFX) {
+        const int64_t g0 = u * 4 + sub;
+        row = g0 / lay.groups;
+        gj = static_cast<int>(g0 - row * lay.groups);
+        drow = step * 4 / lay.groups;
+        dgj = static_cast<int>(step * 4 - drow * lay.groups);
+    }
+
     Slice<F32> cur;
     cur.clear();
     if (u < units && u * 4 + sub < n_groups) cur.load(x, u, lane);
@@ -118,13 +130,16 @@ __global__ void __launch_bounds__(kThreads, 4)
             }
             st_stream(out + u * 32 + lane, make_uint4(lo.x, lo.y, hi.x, hi.y));
         }
-        if (j == 0 && g < n_walk) {
-            if constexpr (SFX) {
-                const int64_t row = g / lay.groups;
-                store_scale(sf, lay, row, live, static_cast<int>(g - row * lay.groups), sc);
-            } else {
-                st_stream(sf + g, sc);
+        if constexpr (SFX) {
+            if (j == 0 && g < n_walk) store_scale(sf, lay, row, live, gj, sc);
+            row += drow;
+            gj += dgj;
+            if (gj >= lay.groups) {
+                gj -= lay.groups;
+                ++row;
             }
+        } else {
+            if (j == 0 && live) st_stream(sf + g, sc);
         }
     }
 }
