@@ -63,14 +63,14 @@ SYNTH_OF = {"per_channel_t": "per_channel", "swiglu_clamp": "swiglu",
 CLAMP_VALUE = 4.0
 KERNEL_SOURCES = {
     "per_token_cast": ["token_cast.cu", "tkq_device.cuh"],
-    "swiglu_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_cast": ["row_cast.cu", "swiglu_flat.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_backward_cast": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_channel_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_channel_cast_t": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_block_cast": ["tile_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "cast_back": ["cast_back.cu", "tkq_device.cuh"],
-    "swiglu_cast_clamp": ["row_cast.cu", "tkq_device.cuh", "tkq_async.cuh"],
+    "swiglu_cast_clamp": ["row_cast.cu", "swiglu_flat.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "swiglu_cast_t_clamp": ["swiglu_cast_t.cu", "tkq_device.cuh", "tkq_async.cuh"],
     "per_token_cast_f32": ["token_cast.cu", "tkq_device.cuh"],
 }

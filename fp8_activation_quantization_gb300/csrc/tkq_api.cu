@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <functional>
 #include <initializer_list>
 #include <mutex>
@@ -74,6 +75,14 @@ int num_sms() {
         v = 1;
     if (dev < kMaxDevices) g_sms[dev].store(v, std::memory_order_relaxed);
     return v;
+}
+
+bool swiglu_flat_chosen(int64_t T, int64_t H) {
+    if (const char* env = std::getenv("TKQ_SWIGLU_KERNEL")) {
+        if (std::strcmp(env, "flat") == 0) return true;
+        if (std::strcmp(env, "ring") == 0) return false;
+    }
+    return T * 2 * H * 2 <= kSwigluFlatMaxBytes;
 }
 
 namespace {

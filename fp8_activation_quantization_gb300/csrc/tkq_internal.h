@@ -72,6 +72,19 @@ cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* s
                                int64_t H, int fmt, unsigned sf_flags, const float* clamp,
                                unsigned long long* clamp_count, cudaStream_t stream);
 
+// The same operation as a flat stream (swiglu_flat.cu), bit-identical; the
+// kernel for short launches.
+cudaError_t launch_swiglu_cast_flat(const void* x, const float* w, void* out, void* sf, int64_t T,
+                                    int64_t H, int fmt, unsigned sf_flags, const float* clamp,
+                                    unsigned long long* clamp_count, cudaStream_t stream);
+
+// Whether a SwiGLU forward cast of [T, 2H] runs as the flat stream: yes when
+// its bf16 input is at most kSwigluFlatMaxBytes, unless the environment
+// variable TKQ_SWIGLU_KERNEL names one kernel ("flat" or "ring"; for tests
+// and measurements).
+constexpr int64_t kSwigluFlatMaxBytes = int64_t{256} << 20;
+bool swiglu_flat_chosen(int64_t T, int64_t H);
+
 cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
                                         void* sf, int64_t T, int64_t H, int fmt,
                                         unsigned sf_flags, cudaStream_t stream);

@@ -42,6 +42,11 @@
  *   T == 0 is an empty batch: TKQ_OK, nothing is launched and the pointers
  *   may be NULL.
  * - A failed launch returns TKQ_ERR_CUDA (cudaGetLastError after the launch).
+ * - Environment (for tests and measurements; no result depends on it):
+ *   TKQ_NUM_SMS=n sizes the persistent grids for n SMs; TKQ_SWIGLU_KERNEL=flat
+ *   or =ring runs the SwiGLU forward cast through one of its two bit-identical
+ *   kernels, which are otherwise chosen by size (the flat stream up to 256 MiB
+ *   of input, the TMA ring above).
  * - Inputs must be finite; NaN or Inf inputs give unspecified codes, and so
  *   does a SwiGLU value or gradient that overflows binary32.
  * - Calls on the same buffers from different streams must be ordered by the
@@ -197,8 +202,9 @@ tkq_status tkq_swiglu_cast_t_ex(const void* x, const float* w, void* out, void* 
                                 unsigned sf_flags, tkq_stream_t stream);
 
 /*
- * Device status word.  The pipelined kernels (every cast above) wait on
- * shared-memory barriers for their bulk copies; every such wait gives up after
+ * Device status word.  The kernels fed by TMA bulk copies (the transposed,
+ * per-channel and per-block casts, and the SwiGLU casts on long launches) wait
+ * on shared-memory barriers for those copies; every such wait gives up after
  * one second, sets TKQ_DEVICE_TIMEOUT in the current device's status word and
  * lets the kernel return (its outputs are then incomplete) instead of hanging.
  * tkq_read_device_status synchronizes the current device, stores the word in

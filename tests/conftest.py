@@ -21,3 +21,12 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("this test is marked gpu but no CUDA device is visible")
     return torch.device("cuda", 0)
+
+
+@pytest.fixture(params=["flat", "ring"])
+def swiglu_kernel(request, monkeypatch):
+    """The library has two kernels for the SwiGLU forward cast, a flat stream
+    for short launches and a TMA ring for long ones, and picks one by input
+    size; a test that takes this fixture runs once through each."""
+    monkeypatch.setenv("TKQ_SWIGLU_KERNEL", request.param)
+    return request.param

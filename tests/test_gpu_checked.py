@@ -125,7 +125,7 @@ def _bytes(t):
     return t.contiguous().view(torch.uint8).cpu().numpy()
 
 
-def test_every_entry_point_stays_inside_its_buffers(cuda_device):
+def test_every_entry_point_stays_inside_its_buffers(cuda_device, swiglu_kernel):
     tkq.tkq_read_device_status(clear=True)
     for name, fn in _cases(cuda_device):
         ref = [_bytes(t) for t in fn()]
@@ -140,7 +140,7 @@ def test_every_entry_point_stays_inside_its_buffers(cuda_device):
             assert np.array_equal(a, b), f"{name}: output {i} differs from the release build"
 
 
-def test_withheld_output_tails_are_refused_and_reported(cuda_device, monkeypatch):
+def test_withheld_output_tails_are_refused_and_reported(cuda_device, swiglu_kernel, monkeypatch):
     monkeypatch.setenv("TKQ_CHECK_WITHHOLD", str(WITHHOLD))
     cases = _cases(cuda_device)
     with tkq.use_checked_library():

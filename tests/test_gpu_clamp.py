@@ -88,7 +88,7 @@ def run_clamp(x_bits, w, fmt, clamp, dev, transposed=False, count=None, sf_flags
 @pytest.mark.parametrize("weighted", [False, True])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("T,H", [(1, 128), (1031, 384)])
-def test_clamped_swiglu_cast(cuda_device, clamp, weighted, fmt, T, H):
+def test_clamped_swiglu_cast(cuda_device, swiglu_kernel, clamp, weighted, fmt, T, H):
     x = synth.swiglu_bf16(71, T + H, T, H, gate_std=2.0)
     w = synth.routing_weights(72, T, -(-T // 8))[:T] if weighted else None
     codes, sf_raw, n = run_clamp(x, w, fmt, clamp, cuda_device)
@@ -139,7 +139,7 @@ def test_clamped_swiglu_cast_t_full_workload(cuda_device):
     parity.assert_codes_differ_only_at_ties("codes_t", ot, eot, q_cols(x, None, 4.0, est), "e4m3")
 
 
-def test_clamp_count_accumulates_and_null_counter_is_allowed(cuda_device):
+def test_clamp_count_accumulates_and_null_counter_is_allowed(cuda_device, swiglu_kernel):
     x = synth.swiglu_bf16(75, 76, 512, 256, gate_std=2.0)
     _, _, n1 = run_clamp(x, None, "e4m3", 1.0, cuda_device)
     _, _, n2 = run_clamp(x, None, "e4m3", 1.0, cuda_device, count=n1)
@@ -154,7 +154,7 @@ def test_clamp_count_accumulates_and_null_counter_is_allowed(cuda_device):
     assert int(cnt.item()) == n1
 
 
-def test_clamp_beyond_the_data_is_the_unclamped_cast(cuda_device):
+def test_clamp_beyond_the_data_is_the_unclamped_cast(cuda_device, swiglu_kernel):
     x = synth.swiglu_bf16(77, 78, 300, 256)
     xd = to_dev_bf16(x, cuda_device)
     q0, s0 = tkq.swiglu_forward_and_per_token_cast(xd)
@@ -164,7 +164,7 @@ def test_clamp_beyond_the_data_is_the_unclamped_cast(cuda_device):
     assert np.array_equal(s0.cpu().numpy().view(np.uint32).ravel(), s1.view(np.uint32))
 
 
-def test_clamp_with_column_major_scales(cuda_device):
+def test_clamp_with_column_major_scales(cuda_device, swiglu_kernel):
     """The clamp composes with a scale layout: column-major fp32 scales are the
     row-major scales of the same clamped launch, transposed (and padded)."""
     T, H = 301, 384
@@ -192,7 +192,7 @@ def _bf16_neighbours(c):
 # not (fp32 clamp).  NaN inputs are outside the contract and not drawn.
 @pytest.mark.parametrize("clamp", [2.0, 448.0, 2.0 + 2.0 ** -20, 0.3])
 @pytest.mark.parametrize("weighted", [False, True])
-def test_clamp_at_special_values(cuda_device, clamp, weighted):
+def test_clamp_at_special_values(cuda_device, swiglu_kernel, clamp, weighted):
     """Gates and ups drawn from infinities, the largest finite bf16, signed
     zeros, bf16 subnormals, and the bf16 values at and next to +-c: the count
     is exact and the outputs match the oracle (row and transposed casts)."""

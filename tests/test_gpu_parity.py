@@ -243,7 +243,7 @@ def test_swiglu_full_workload(cuda_device, name):
 @pytest.mark.parametrize("H", [128, 384, 2048])
 @pytest.mark.parametrize("weighted", [False, True])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_swiglu_ragged(cuda_device, T, H, weighted, fmt):
+def test_swiglu_ragged(cuda_device, swiglu_kernel, T, H, weighted, fmt):
     d = synth.workload("swiglu_moe", rows=T)
     x = np.ascontiguousarray(d["x"][:, np.r_[0:H, 2048:2048 + H]])
     w = d["w"] if weighted else None
@@ -254,7 +254,7 @@ def test_swiglu_ragged(cuda_device, T, H, weighted, fmt):
     parity.assert_codes_close("codes", out, ro, max_frac=max(1e-4, 1.0 / out.size))
 
 
-def test_swiglu_gate_orientation_and_zero_gate(cuda_device):
+def test_swiglu_gate_orientation_and_zero_gate(cuda_device, swiglu_kernel):
     H = 128
     x = np.zeros((2, 2 * H), np.uint16)
     x[0, :H] = synth.f32_to_bf16_bits(np.full(H, 10.0, np.float32))
@@ -267,6 +267,33 @@ def test_swiglu_gate_orientation_and_zero_gate(cuda_device):
     assert np.all(out[1] == 0x80)  # -0 keeps its sign
 
 
+@pytest.mark.parametrize("flags", [0, 1, 4, 6])
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("clamp", [None, 2.0, 2.9])
+@pytest.mark.parametrize("T,H", [(1031, 384), (4099, 2048)])
+def test_swiglu_kernels_agree_bytewise(cuda_device, monkeypatch, flags, weighted, clamp, T, H):
+    """The flat and the TMA-ring SwiGLU kernels give the same bytes (codes,
+    scales in every layout, clamp count) on the same input: the library may
+    pick either for a call."""
+    d = synth.workload("swiglu_moe", rows=T)
+    x = np.ascontiguousarray(d["x"][:, np.r_[0:H, 2048:2048 + H]])
+    xd = to_dev_bf16(x, cuda_device)
+    w = torch.from_numpy(d["w"]).to(cuda_device) if weighted else None
+    opts = dict(round_sf=bool(flags & 1), use_packed_ue8m0=bool(flags & 2),
+                use_tma_aligned_col_major_sf=bool(flags & 4))
+    got = {}
+    for kernel in ("flat", "ring"):
+        monkeypatch.setenv("TKQ_SWIGLU_KERNEL", kernel)
+        cnt = torch.zeros(1, dtype=torch.int64, device=cuda_device)
+        kw = dict(use_clamp=True, swiglu_clamp_value=clamp, clamp_count=cnt) if clamp else {}
+        q, s = tkq.swiglu_forward_and_per_token_cast(xd, topk_weights=w, **opts, **kw)
+        got[kernel] = [q.view(torch.uint8).cpu().numpy(), s.contiguous().view(torch.uint8).cpu().numpy(),
+                       cnt.cpu().numpy()]
+    for a, b, what in zip(got["flat"], got["ring"], ("codes", "scales", "clamp count")):
+        parity.assert_bit_exact(what, a, b)
+    assert tkq.tkq_read_device_status() == 0
+
+
 # ---------------------------------------------------------------------------
 # SwiGLU + transposed cast
 # ---------------------------------------------------------------------------
@@ -274,7 +301,7 @@ def test_swiglu_gate_orientation_and_zero_gate(cuda_device):
 @pytest.mark.parametrize("T,H", [(128, 128), (256, 384), (1024, 2048), (3072, 256)])
 @pytest.mark.parametrize("weighted", [False, True])
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-def test_swiglu_t_shapes(cuda_device, T, H, weighted, fmt):
+def test_swiglu_t_shapes(cuda_device, swiglu_kernel, T, H, weighted, fmt):
     d = synth.workload("swiglu_moe", rows=T)
     x = np.ascontiguousarray(d["x"][:, np.r_[0:H, 2048:2048 + H]])
     w = d["w"] if weighted else None
@@ -521,7 +548,7 @@ def _pow2_boundary(s0: np.ndarray, tol=2e-6) -> np.ndarray:
 
 @pytest.mark.parametrize("kind", ["swiglu", "backward"])
 @pytest.mark.parametrize("flags", [1, 2, 4, 6, 8])
-def test_swiglu_sf_layouts(cuda_device, kind, flags):
+def test_swiglu_sf_layouts(cuda_device, swiglu_kernel, kind, flags):
     if kind == "swiglu":
         d = synth.workload("swiglu_moe", rows=1031)
         x = np.ascontiguousarray(d["x"][:, np.r_[0:896, 2048:2944]])

@@ -64,7 +64,7 @@ def test_random_row_casts(cuda_device, case):
 
 
 @pytest.mark.parametrize("case", range(16))
-def test_random_swiglu_casts(cuda_device, case):
+def test_random_swiglu_casts(cuda_device, swiglu_kernel, case):
     rng = np.random.default_rng(2000 + case)
     transposed = bool(case % 4 == 0)
     T = 128 * int(rng.integers(1, 6)) if transposed else int(rng.choice([1, 7, 64, 129, 700]))

@@ -5,6 +5,8 @@ between a table's writes and reads) shows up as a rare differing launch; the
 full-grid and few-SM runs exercise short and long ring walks."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -43,6 +45,21 @@ def _ops(dev):
                                                            **kw), cnt)
         return run
 
+    def ring(op):
+        # the same call through the TMA-ring SwiGLU kernel (these inputs are
+        # small enough that the library picks the flat one)
+        def run():
+            saved = os.environ.get("TKQ_SWIGLU_KERNEL")
+            os.environ["TKQ_SWIGLU_KERNEL"] = "ring"
+            try:
+                return op()
+            finally:
+                if saved is None:
+                    os.environ.pop("TKQ_SWIGLU_KERNEL", None)
+                else:
+                    os.environ["TKQ_SWIGLU_KERNEL"] = saved
+        return run
+
     return {
         "plain": lambda: tkq.per_token_cast(x),
         "plain ue8m0 col-major": lambda: tkq.per_token_cast(
@@ -51,6 +68,9 @@ def _ops(dev):
         "plain fp32": lambda: tkq.per_token_cast(xf),
         "swiglu weighted": lambda: tkq.swiglu_forward_and_per_token_cast(xs, topk_weights=w),
         "swiglu clamp": clamped(topk_weights=w, swiglu_clamp_value=2.0),
+        "swiglu weighted, ring kernel": ring(
+            lambda: tkq.swiglu_forward_and_per_token_cast(xs, topk_weights=w)),
+        "swiglu clamp, ring kernel": ring(clamped(topk_weights=w, swiglu_clamp_value=2.0)),
         "swiglu_t weighted": lambda: tkq.swiglu_forward_and_per_token_cast(
             xs, topk_weights=w, with_transpose=True),
         "swiglu_t clamp": clamped(with_transpose=True, swiglu_clamp_value=2.9),

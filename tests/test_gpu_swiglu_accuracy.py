@@ -107,7 +107,7 @@ def test_random_values_within_the_bound(cuda_device):
 
 
 @pytest.mark.parametrize("weighted", [False, True])
-def test_casts_quantize_these_values(cuda_device, weighted):
+def test_casts_quantize_these_values(cuda_device, swiglu_kernel, weighted):
     """Scales of the SwiGLU cast = the oracle's scale rule on the diagnostic y
     (bit for bit); codes = the oracle's codes of that y except at FP8 ties
     (the cast multiplies by the rounded reciprocal, the oracle divides)."""
