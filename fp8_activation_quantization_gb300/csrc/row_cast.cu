@@ -346,7 +346,7 @@ cudaError_t launch_fmt(int fmt, const void* x, const void* dy, const float* w, v
 cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* sf, int64_t T,
                                int64_t H, int fmt, unsigned sf_flags, const float* clamp,
                                unsigned long long* clamp_count, cudaStream_t stream) {
-    if (swiglu_flat_chosen(T, H))
+    if (swiglu_flat_chosen(T, H, w != nullptr))
         return launch_swiglu_cast_flat(x, w, out, sf, T, H, fmt, sf_flags, clamp, clamp_count,
                                        stream);
     if (clamp) {

@@ -3,12 +3,12 @@
 // optional clamp (gate <= c, -c <= up <= c) whose changed values are counted
 // ("DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件性能上限"
 // (itsolotime.com) §3.3), as a flat stream: the second of the library's two
-// kernels for this operation, the one for short launches.  It computes the
-// same values and codes as the TMA-ring kernel of row_cast.cu (the same
-// packed steps of tkq_device.cuh, in the same order), so the two are
-// bit-identical; the ring's fill and drain cost more than it saves when a
-// launch moves a few hundred MB or less, while on longer launches its deeper
-// queue of loads wins (measured on both; the ABI layer picks by size).
+// kernels for this operation.  It computes the same values and codes as the
+// TMA-ring kernel of row_cast.cu (the same packed steps of tkq_device.cuh, in
+// the same order), so the two are bit-identical.  Measured on both, this one
+// is faster without a routing weight at every size, and with one on launches
+// up to a few hundred MB, where the ring's fill and drain cost more than its
+// deeper queue of loads saves; the launcher picks (swiglu_flat_chosen).
 //
 // GB300 design: the output groups g = t * GH + j (GH = H / 128) are visited in
 // order, a warp taking units of four (lane l: 16 consecutive channels of group

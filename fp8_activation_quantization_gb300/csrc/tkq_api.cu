@@ -77,12 +77,12 @@ int num_sms() {
     return v;
 }
 
-bool swiglu_flat_chosen(int64_t T, int64_t H) {
+bool swiglu_flat_chosen(int64_t T, int64_t H, bool weighted) {
     if (const char* env = std::getenv("TKQ_SWIGLU_KERNEL")) {
         if (std::strcmp(env, "flat") == 0) return true;
         if (std::strcmp(env, "ring") == 0) return false;
     }
-    return T * 2 * H * 2 <= kSwigluFlatMaxBytes;
+    return !weighted || T * 2 * H * 2 <= kSwigluFlatMaxBytes;
 }
 
 namespace {

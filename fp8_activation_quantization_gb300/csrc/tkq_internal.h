@@ -78,12 +78,15 @@ cudaError_t launch_swiglu_cast_flat(const void* x, const float* w, void* out, vo
                                     int64_t H, int fmt, unsigned sf_flags, const float* clamp,
                                     unsigned long long* clamp_count, cudaStream_t stream);
 
-// Whether a SwiGLU forward cast of [T, 2H] runs as the flat stream: yes when
-// its bf16 input is at most kSwigluFlatMaxBytes, unless the environment
-// variable TKQ_SWIGLU_KERNEL names one kernel ("flat" or "ring"; for tests
-// and measurements).
-constexpr int64_t kSwigluFlatMaxBytes = int64_t{256} << 20;
-bool swiglu_flat_chosen(int64_t T, int64_t H);
+// Whether a SwiGLU forward cast of [T, 2H] runs as the flat stream: yes
+// without a routing weight, and with one when its bf16 input is at most
+// kSwigluFlatMaxBytes (measured: the flat stream is faster at every size
+// without a weight, and with one up to 320 MiB of input; the two tie at
+// 384 MiB and the ring is faster above).  The environment variable
+// TKQ_SWIGLU_KERNEL ("flat" or "ring") overrides this for tests and
+// measurements.
+constexpr int64_t kSwigluFlatMaxBytes = int64_t{384} << 20;
+bool swiglu_flat_chosen(int64_t T, int64_t H, bool weighted);
 
 cudaError_t launch_swiglu_backward_cast(const void* x, const void* dy, const float* w, void* out,
                                         void* sf, int64_t T, int64_t H, int fmt,

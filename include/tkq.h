@@ -45,8 +45,9 @@
  * - Environment (for tests and measurements; no result depends on it):
  *   TKQ_NUM_SMS=n sizes the persistent grids for n SMs; TKQ_SWIGLU_KERNEL=flat
  *   or =ring runs the SwiGLU forward cast through one of its two bit-identical
- *   kernels, which are otherwise chosen by size (the flat stream up to 256 MiB
- *   of input, the TMA ring above).
+ *   kernels, which are otherwise chosen by measured speed (the flat stream
+ *   without a routing weight, and with one up to 384 MiB of input; the TMA
+ *   ring for weighted launches above that).
  * - Inputs must be finite; NaN or Inf inputs give unspecified codes, and so
  *   does a SwiGLU value or gradient that overflows binary32.
  * - Calls on the same buffers from different streams must be ordered by the

@@ -25,8 +25,8 @@ def cuda_device():
 
 @pytest.fixture(params=["flat", "ring"])
 def swiglu_kernel(request, monkeypatch):
-    """The library has two kernels for the SwiGLU forward cast, a flat stream
-    for short launches and a TMA ring for long ones, and picks one by input
-    size; a test that takes this fixture runs once through each."""
+    """The library has two bit-identical kernels for the SwiGLU forward cast,
+    a flat stream and a TMA ring, and picks one by a measured rule (weight,
+    input size); a test that takes this fixture runs once through each."""
     monkeypatch.setenv("TKQ_SWIGLU_KERNEL", request.param)
     return request.param

@@ -46,8 +46,8 @@ def _ops(dev):
         return run
 
     def ring(op):
-        # the same call through the TMA-ring SwiGLU kernel (these inputs are
-        # small enough that the library picks the flat one)
+        # the same call through the TMA-ring SwiGLU kernel (for these inputs
+        # the library picks the flat one)
         def run():
             saved = os.environ.get("TKQ_SWIGLU_KERNEL")
             os.environ["TKQ_SWIGLU_KERNEL"] = "ring"
