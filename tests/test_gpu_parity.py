@@ -632,8 +632,9 @@ def test_bounded_wait_times_out_and_context_survives(cuda_device):
 def test_repeated_launches_are_identical(cuda_device):
     """Many launches on the same input: every plain-cast result equals the
     oracle bit for bit and every transposed-cast result equals the first one.
-    A shared-memory stage released to the TMA producer before its readers are
-    done shows up here as a rare corrupted group."""
+    A shared-memory stage of the transposed cast's ring released to the TMA
+    producer before its readers are done shows up here as a rare corrupted
+    group."""
     dev = cuda_device
     x = synth.workload("plain_outlier")["x"]
     xd = to_dev_bf16(x, dev)
