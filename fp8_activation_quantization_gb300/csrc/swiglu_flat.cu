@@ -96,9 +96,13 @@ struct Slice {
     }
 };
 
+// The clamp of an instance: none, on packed bf16 pairs (the bound is a bf16
+// value), or in fp32.
+enum ClampKind { kNoClamp, kClampBf16, kClampF32 };
+
 // n_groups = T * GH groups hold data; n_walk >= n_groups are visited.
-template <int FMT, bool WEIGHTED, bool CLAMP, bool SFX>
-__global__ void __launch_bounds__(kThreads, CLAMP ? 3 : 4)
+template <int FMT, bool WEIGHTED, int CLAMP, bool SFX>
+__global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
     swiglu_flat_kernel(const uint4* __restrict__ x, const float* __restrict__ w,
                        uint4* __restrict__ out, float* __restrict__ sf, SfLayout lay, int64_t H,
                        int64_t n_groups, int64_t n_walk, FlatClamp clamp) {
@@ -125,39 +129,34 @@ __global__ void __launch_bounds__(kThreads, CLAMP ? 3 : 4)
         if (cur.u < units && cur.g < n_groups) in.load(x, w, cur.t, cur.j, k, H);
 
         float gv[16], uv[16];
-        if constexpr (CLAMP) {
-            uint32_t n = 0;
-            if (clamp.c2) {
-                // c is a bf16 value: clamp and count on the packed pairs
-                uint32_t n2 = 0;
+        uint32_t n = 0;
+        if constexpr (CLAMP == kClampBf16) {
+            // clamp and count on the packed pairs
+            uint32_t n2 = 0;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    n2 += clamp_pairs_bf16(gq[h].x, uq[h].x, clamp.c2);
-                    n2 += clamp_pairs_bf16(gq[h].y, uq[h].y, clamp.c2);
-                    n2 += clamp_pairs_bf16(gq[h].z, uq[h].z, clamp.c2);
-                    n2 += clamp_pairs_bf16(gq[h].w, uq[h].w, clamp.c2);
-                }
-                n = (n2 & 0xFFFFu) + (n2 >> 16);
+            for (int h = 0; h < 2; ++h) {
+                n2 += clamp_pairs_bf16(gq[h].x, uq[h].x, clamp.c2);
+                n2 += clamp_pairs_bf16(gq[h].y, uq[h].y, clamp.c2);
+                n2 += clamp_pairs_bf16(gq[h].z, uq[h].z, clamp.c2);
+                n2 += clamp_pairs_bf16(gq[h].w, uq[h].w, clamp.c2);
             }
-            unpack8(gq[0], gv);
-            unpack8(gq[1], gv + 8);
-            unpack8(uq[0], uv);
-            unpack8(uq[1], uv + 8);
-            if (!clamp.c2) {
-                const float c = clamp.value;
+            n = (n2 & 0xFFFFu) + (n2 >> 16);
+        }
+        unpack8(gq[0], gv);
+        unpack8(gq[1], gv + 8);
+        unpack8(uq[0], uv);
+        unpack8(uq[1], uv + 8);
+        if constexpr (CLAMP == kClampF32) {
+            const float c = clamp.value;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    n += (gv[e] > c) + (fabsf(uv[e]) > c);
-                    gv[e] = fminf(gv[e], c);
-                    uv[e] = fmaxf(fminf(uv[e], c), -c);
-                }
+            for (int e = 0; e < 16; ++e) {
+                n += (gv[e] > c) + (fabsf(uv[e]) > c);
+                gv[e] = fminf(gv[e], c);
+                uv[e] = fmaxf(fminf(uv[e], c), -c);
             }
+        }
+        if constexpr (CLAMP != kNoClamp) {
             if (live) n_clamped += n;
-        } else {
-            unpack8(gq[0], gv);
-            unpack8(gq[1], gv + 8);
-            unpack8(uq[0], uv);
-            unpack8(uq[1], uv + 8);
         }
 
         float v[16];
@@ -190,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, CLAMP ? 3 : 4)
             }
         }
     }
-    if constexpr (CLAMP) {
+    if constexpr (CLAMP != kNoClamp) {
         // one atomic per warp, and none when nothing was clamped
         unsigned long long c = n_clamped;
 #pragma unroll
@@ -199,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, CLAMP ? 3 : 4)
     }
 }
 
-template <int FMT, bool WEIGHTED, bool CLAMP, bool SFX>
+template <int FMT, bool WEIGHTED, int CLAMP, bool SFX>
 cudaError_t launch_layout(const void* x, const float* w, void* out, float* sf,
                           const SfLayout& lay, int64_t H, int64_t n_groups, int64_t n_walk,
                           FlatClamp clamp, cudaStream_t stream) {
@@ -213,7 +212,7 @@ cudaError_t launch_layout(const void* x, const float* w, void* out, float* sf,
     return cudaGetLastError();
 }
 
-template <int FMT, bool WEIGHTED, bool CLAMP>
+template <int FMT, bool WEIGHTED, int CLAMP>
 cudaError_t launch_flags(const void* x, const float* w, void* out, float* sf,
                          const SfLayout& lay, int64_t H, int64_t n_groups, int64_t n_walk,
                          FlatClamp clamp, cudaStream_t stream) {
@@ -229,12 +228,20 @@ cudaError_t launch_fmt(const void* x, const float* w, void* out, float* sf, cons
                        int64_t H, int64_t n_groups, int64_t n_walk, const FlatClamp* clamp,
                        cudaStream_t stream) {
     const FlatClamp c = clamp ? *clamp : FlatClamp{0.0f, nullptr, 0u};
+    if (clamp && c.c2)
+        return w ? launch_flags<FMT, true, kClampBf16>(x, w, out, sf, lay, H, n_groups, n_walk, c,
+                                                       stream)
+                 : launch_flags<FMT, false, kClampBf16>(x, w, out, sf, lay, H, n_groups, n_walk,
+                                                        c, stream);
     if (clamp)
-        return w ? launch_flags<FMT, true, true>(x, w, out, sf, lay, H, n_groups, n_walk, c, stream)
-                 : launch_flags<FMT, false, true>(x, w, out, sf, lay, H, n_groups, n_walk, c,
+        return w ? launch_flags<FMT, true, kClampF32>(x, w, out, sf, lay, H, n_groups, n_walk, c,
+                                                      stream)
+                 : launch_flags<FMT, false, kClampF32>(x, w, out, sf, lay, H, n_groups, n_walk, c,
+                                                       stream);
+    return w ? launch_flags<FMT, true, kNoClamp>(x, w, out, sf, lay, H, n_groups, n_walk, c,
+                                                 stream)
+             : launch_flags<FMT, false, kNoClamp>(x, w, out, sf, lay, H, n_groups, n_walk, c,
                                                   stream);
-    return w ? launch_flags<FMT, true, false>(x, w, out, sf, lay, H, n_groups, n_walk, c, stream)
-             : launch_flags<FMT, false, false>(x, w, out, sf, lay, H, n_groups, n_walk, c, stream);
 }
 
 }  // namespace
