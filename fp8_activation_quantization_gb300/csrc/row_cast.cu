@@ -210,15 +210,15 @@ __global__ void __launch_bounds__(kThreads, 3)
                 if (clamp.c2) {
                     // c is a bf16 value: clamp and count on the packed pairs
                     const uint32_t c2 = clamp.c2;
-                    uint32_t n2 = 0;
+                    __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);  // at most 16 a half
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        n2 += clamp_pairs_bf16(gq[h].x, uq[h].x, c2);
-                        n2 += clamp_pairs_bf16(gq[h].y, uq[h].y, c2);
-                        n2 += clamp_pairs_bf16(gq[h].z, uq[h].z, c2);
-                        n2 += clamp_pairs_bf16(gq[h].w, uq[h].w, c2);
+                        clamp_pairs_bf16(gq[h].x, uq[h].x, c2, n2);
+                        clamp_pairs_bf16(gq[h].y, uq[h].y, c2, n2);
+                        clamp_pairs_bf16(gq[h].z, uq[h].z, c2, n2);
+                        clamp_pairs_bf16(gq[h].w, uq[h].w, c2, n2);
                     }
-                    n = (n2 & 0xFFFFu) + (n2 >> 16);
+                    n = clamped_total(n2);
                     unpack8(gq[0], g);
                     unpack8(gq[1], g + 8);
                     unpack8(uq[0], u);

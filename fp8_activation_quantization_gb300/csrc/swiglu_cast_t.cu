@@ -149,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             // clamp counts of this tile: per half of the packed-bf16 clamp, and
             // of the fp32 clamp
-            [[maybe_unused]] uint32_t n2 = 0, n1 = 0;
+            [[maybe_unused]] __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);
+            [[maybe_unused]] uint32_t n1 = 0;
             const uint8_t* g_base = sm.stage[s] + warp * 8 * 256 + lane * 8;
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (clamp2) {
                         // c is a bf16 value: clamp and count on the packed pairs
                         // (at most 4 per half and row: 32 per tile)
-                        n2 += clamp_pairs_bf16(gq.x, uq.x, clamp2);
-                        n2 += clamp_pairs_bf16(gq.y, uq.y, clamp2);
+                        clamp_pairs_bf16(gq.x, uq.x, clamp2, n2);
+                        clamp_pairs_bf16(gq.y, uq.y, clamp2, n2);
                         unpack4(gq, gv);
                         unpack4(uq, uv);
                     } else {
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     y[r][k + 1] = p.y;
                 }
             }
-            if constexpr (CLAMP) n_clamped += (n2 & 0xFFFFu) + (n2 >> 16) + n1;
+            if constexpr (CLAMP) n_clamped += clamped_total(n2) + n1;
         }
 
         // ---- column maxima over this thread's 8 tokens -> shared table ----

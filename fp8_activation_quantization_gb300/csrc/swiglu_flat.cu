@@ -132,15 +132,15 @@ __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
         uint32_t n = 0;
         if constexpr (CLAMP == kClampBf16) {
             // clamp and count on the packed pairs
-            uint32_t n2 = 0;
+            __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);  // at most 16 a half
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                n2 += clamp_pairs_bf16(gq[h].x, uq[h].x, clamp.c2);
-                n2 += clamp_pairs_bf16(gq[h].y, uq[h].y, clamp.c2);
-                n2 += clamp_pairs_bf16(gq[h].z, uq[h].z, clamp.c2);
-                n2 += clamp_pairs_bf16(gq[h].w, uq[h].w, clamp.c2);
+                clamp_pairs_bf16(gq[h].x, uq[h].x, clamp.c2, n2);
+                clamp_pairs_bf16(gq[h].y, uq[h].y, clamp.c2, n2);
+                clamp_pairs_bf16(gq[h].z, uq[h].z, clamp.c2, n2);
+                clamp_pairs_bf16(gq[h].w, uq[h].w, clamp.c2, n2);
             }
-            n = (n2 & 0xFFFFu) + (n2 >> 16);
+            n = clamped_total(n2);
         }
         unpack8(gq[0], gv);
         unpack8(gq[1], gv + 8);

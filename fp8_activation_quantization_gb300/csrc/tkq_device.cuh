@@ -406,12 +406,16 @@ __device__ __forceinline__ uint32_t as_word(__nv_bfloat162 v) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Clamps the gate pair g and the up pair u in place (c2 = bf16x2_bound(c));
-// returns the number of changed values of each half in that half (0, 1 or 2).
-// The up clamp is one min.xorsign.abs: magnitude min(|u|, c), sign of u xor
-// sign of c (+), which is clamp(u, -c, c) for every u that is not NaN,
-// signed zeros and infinities included.
-__device__ __forceinline__ uint32_t clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint32_t c2) {
+// Clamps the gate pair g and the up pair u in place (c2 = bf16x2_bound(c))
+// and adds to each half of n the number of that half's two values (gate, up)
+// the clamp changed: the not-equal compares give 1.0 or 0.0 per half and are
+// summed in bf16, which is exact for counts up to 256 (callers convert n with
+// clamped_total before it could exceed that).  The up clamp is one
+// min.xorsign.abs: magnitude min(|u|, c), sign of u xor sign of c (+), which
+// is clamp(u, -c, c) for every u that is not NaN, signed zeros and infinities
+// included.
+__device__ __forceinline__ void clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint32_t c2,
+                                                 __nv_bfloat162& n) {
     const __nv_bfloat162 gb = as_bf162(g), ub = as_bf162(u);
     const __nv_bfloat162 gc = __hmin2(gb, as_bf162(c2));
     uint32_t uw;
@@ -419,7 +423,13 @@ __device__ __forceinline__ uint32_t clamp_pairs_bf16(uint32_t& g, uint32_t& u, u
     const __nv_bfloat162 uc = as_bf162(uw);
     g = as_word(gc);
     u = uw;
-    return (__hne2_mask(gb, gc) & 0x00010001u) + (__hne2_mask(ub, uc) & 0x00010001u);
+    n = __hadd2(n, __hne2(gb, gc));
+    n = __hadd2(n, __hne2(ub, uc));
+}
+
+// The total of a clamp_pairs_bf16 count pair (two small integers, exact).
+__device__ __forceinline__ uint32_t clamped_total(__nv_bfloat162 n) {
+    return static_cast<uint32_t>(__low2float(n) + __high2float(n));
 }
 
 // Gradient of y = silu(g) * u with respect to g and u, scaled by the upstream
