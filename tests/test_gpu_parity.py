@@ -294,6 +294,54 @@ def test_swiglu_kernels_agree_bytewise(cuda_device, monkeypatch, flags, weighted
     assert tkq.tkq_read_device_status() == 0
 
 
+def test_swiglu_beyond_2_31_input_elements(cuda_device, monkeypatch):
+    """x of 262,147 x 8192 bf16 (2.15e9 elements, 4.3 GB) with a routing
+    weight, through both SwiGLU kernels: input offsets beyond 2^32 bytes.  The
+    two outputs are compared byte for byte in full, and rows sampled at both
+    ends and the middle against the oracle."""
+    T, H = 262_147, 4096
+    dev = cuda_device
+    rng = np.random.default_rng(78)
+    xd = torch.empty((T, 2 * H), dtype=torch.int16, device=dev)
+    w = rng.uniform(0.0, 1.0, T).astype(np.float32)
+    wd = torch.from_numpy(w).to(dev)
+    chunk = 32768
+    keep = {}
+    sample_rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(T - 200, T),
+                                            rng.integers(0, T, 48)]))
+    for a in range(0, T, chunk):
+        b = min(T, a + chunk)
+        bits = rng.integers(0, 1 << 16, size=(b - a, 2 * H), dtype=np.uint16)
+        e = rng.integers(127 - 8, 127 + 3, size=(b - a, 2 * H), dtype=np.uint16)
+        bits = (bits & np.uint16(0x807F)) | (e << np.uint16(7)).astype(np.uint16)
+        xd[a:b] = torch.from_numpy(bits.view(np.int16)).to(dev)
+        sel = sample_rows[(sample_rows >= a) & (sample_rows < b)]
+        for r in sel:
+            keep[int(r)] = bits[r - a].copy()
+    got = {}
+    for kernel in ("flat", "ring"):
+        monkeypatch.setenv("TKQ_SWIGLU_KERNEL", kernel)
+        out = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        sf = torch.empty((T, H // 128), dtype=torch.float32, device=dev)
+        st = tkq.tkq_swiglu_cast(ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(wd.data_ptr()),
+                                 ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(sf.data_ptr()),
+                                 T, H, 128, 0, stream_of(dev))
+        assert st == 0
+        torch.cuda.synchronize()
+        got[kernel] = (out, sf)
+    assert torch.equal(got["flat"][0], got["ring"][0]), "codes of the two kernels differ"
+    assert torch.equal(got["flat"][1].view(torch.int32), got["ring"][1].view(torch.int32))
+    rows = np.array(sorted(keep))
+    xs = np.stack([keep[r] for r in rows])
+    ro, rs = oracle.swiglu_cast(xs, w[rows], "e4m3", threads=THREADS)
+    idx = torch.from_numpy(rows).to(dev)
+    out, sf = got["flat"]
+    parity.assert_scales_close("scales", sf.index_select(0, idx).cpu().numpy(), rs)
+    codes = out.index_select(0, idx).cpu().numpy()
+    parity.assert_codes_close("codes", codes, ro, max_frac=max(1e-4, 1.0 / codes.size))
+    assert tkq.tkq_read_device_status() == 0
+
+
 # ---------------------------------------------------------------------------
 # SwiGLU + transposed cast
 # ---------------------------------------------------------------------------
