@@ -125,6 +125,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------------- consumers
     const int ct = threadIdx.x;  // 0 .. kConsumers-1
     uint64_t n_clamped = 0;
+    // routing weights of this thread's 8 tokens, loaded one tile ahead so that
+    // their latency overlaps the previous tile's work
+    [[maybe_unused]] float wt_next[8];
+    if constexpr (WEIGHTED) {
+        const TileWalk first(blockIdx.x, gridDim.x, CB);
+        if (first.row < TB) {
+            const int64_t r0 = static_cast<int64_t>(first.row) * 128 + warp * 8;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) wt_next[r] = ld_ro(w + r0 + r);
+        }
+    }
     RingPos<kStages> pos;
     for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB; tw.next(), pos.advance()) {
         const int s = static_cast<int>(pos.stage);
@@ -139,7 +150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r) wt[r] = 1.0f;
         if constexpr (WEIGHTED) {
 #pragma unroll
-            for (int r = 0; r < 8; ++r) wt[r] = ld_ro(w + row0 + r);
+            for (int r = 0; r < 8; ++r) wt[r] = wt_next[r];
+            TileWalk nx = tw;
+            nx.next();
+            if (nx.row < TB) {
+                const int64_t r0 = static_cast<int64_t>(nx.row) * 128 + warp * 8;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) wt_next[r] = ld_ro(w + r0 + r);
+            }
         }
 
         const bool ok = mbar_wait_bounded(&sm.full[s], pos.phase, &sm.abort, status);
