@@ -226,7 +226,12 @@ class Problem:
     through the public tensor API (for the end-to-end measurement) for a named
     workload."""
 
-    def __init__(self, workload: str, fmt: str, dev, seed: int = 0, sf_flags: int = 0):
+    def __init__(self, workload: str, fmt: str, dev, seed: int = 0, sf_flags: int = 0,
+                 like: "Problem | None" = None, row_begin: int = 0):
+        """`like`: another Problem of the same workload whose inputs are copied
+        to new device buffers (a second buffer set of the same launch, for the
+        sustained timing); `row_begin`: the first row of this rank's shard of a
+        multi-GPU batch (rows [row_begin, row_begin + T) of one longer draw)."""
         import torch
         import fp8_activation_quantization_gb300 as tkq
         from fp8_activation_quantization_gb300 import synth
@@ -234,13 +239,20 @@ class Problem:
         self.kern = kern = KERNEL_OF[workload]
         self.fmt = fmt
         self.sf_flags = sf_flags
-        self.host = synth.workload(SYNTH_OF.get(workload, workload), seed=seed)
+        if like is not None:
+            self.host = like.host
+        else:
+            self.host = synth.workload(SYNTH_OF.get(workload, workload), seed=seed,
+                                       row_begin=row_begin)
         lead = self.host["x"] if "x" in self.host else self.host["codes"]
         self.T, self.C = T, C = lead.shape
         self.weighted = "w" in self.host
         self.bytes = algorithmic_bytes(workload, T, C, self.weighted)
         self.dev = dev
-        self.inp = {k: _to_torch(v).to(dev) for k, v in self.host.items()}
+        if like is not None:
+            self.inp = {k: v.clone() for k, v in like.inp.items()}
+        else:
+            self.inp = {k: _to_torch(v).to(dev) for k, v in self.host.items()}
         fcode = 0 if fmt == "e4m3" else 1
         fp8 = _fp8(fmt)
         P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
@@ -376,24 +388,6 @@ class Problem:
             raise RuntimeError(f"{self.kern} failed with status {st}")
 
 
-def time_steps(prob: Problem, steps: int, warmup: int, stream, barrier):
-    import torch
-    for _ in range(warmup):
-        prob.launch(stream)
-    torch.cuda.synchronize()
-    barrier()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(steps):
-        prob.launch(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    return start.elapsed_time(end) / 1000.0  # seconds
-
-
 def time_flushed(prob: Problem, reps: int, stream, flush):
     """Median per-launch time with L2 flushed before each launch.  The flush
     READS a buffer four times the size of L2, which leaves L2 full of clean
@@ -414,28 +408,80 @@ def time_flushed(prob: Problem, reps: int, stream, flush):
     return float(np.median(ts))
 
 
-def time_steps_flushed(prob: Problem, steps: int, warmup: int, stream, flush, barrier):
-    """K launches, each preceded by an L2 flush; returns the summed launch
-    times (seconds) measured with CUDA events around each launch."""
-    import torch
-    for _ in range(warmup):
-        flush.max()
-        prob.launch(stream)
-    torch.cuda.synchronize()
-    barrier()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
-    for s, e in evs:
-        flush.max()
-        s.record(stream)
-        prob.launch(stream)
-        e.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    return sum(s.elapsed_time(e) for s, e in evs) / 1000.0
-
-
 SMALL_BYTES = 512e6  # below this the working set could stay in L2 between steps
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (the ~8 TB/s the 80 % bar refers to)
+
+
+def l2_bytes(dev) -> int:
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size) or 129 << 20
+    except Exception:
+        return 129 << 20
+
+
+def rotation_sets(prob: Problem, l2: int) -> int:
+    """Buffer sets the sustained timing rotates over: enough that their inputs
+    and outputs together span at least four times L2, and at least two."""
+    return max(2, -(-4 * l2 // max(prob.bytes, 1)))
+
+
+def time_sustained(probs, stream, min_launches: int = 200):
+    """Per-launch time (seconds) of launches issued back to back over a rotation
+    of buffer sets (the Problems in `probs`, one per set).  With the sets
+    spanning several times L2, every launch reads inputs that are not in L2,
+    and the write-back of each launch's output is paid inside the launches that
+    follow it, as in a stream of casts; only the last launch's dirty lines fall
+    outside the timed region, one launch's worth over all of them.  The
+    launches (a multiple of the rotation, at least `min_launches`) are captured
+    in one CUDA graph and replayed, so that host launch cost cannot pace short
+    kernels; one warm-up pass over the rotation and one warm-up replay come
+    first.  Returns (seconds per launch, launches timed)."""
+    import torch
+    k = len(probs)
+    n = max(1, -(-min_launches // k)) * k
+    for p in probs:
+        p.launch(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+        for i in range(n):
+            probs[i % k].launch(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    e.record(stream)
+    e.synchronize()
+    dt = s.elapsed_time(e) / 1000.0 / n
+    del g
+    return dt, n
+
+
+def rotation(prob: Problem, l2: int):
+    """The buffer sets of a sustained timing: `prob` and copies of it."""
+    sets = [prob]
+    for _ in range(rotation_sets(prob, l2) - 1):
+        sets.append(Problem(prob.workload, prob.fmt, prob.dev, sf_flags=prob.sf_flags, like=prob))
+    return sets
+
+
+def rank_shard(workload: str, ws: int, rank: int, rows: int | None = None) -> tuple[int, int, int]:
+    """Weak scaling over `ws` ranks: the global batch is `ws` times the
+    workload's rows (or `rows` per rank), split by shard_rows into contiguous
+    ranges (multiples of 128 rows where the row count allows, so the transposed
+    cast's 128-token groups never straddle two ranks).  Returns (first row, end
+    row, global rows) of this rank's shard."""
+    from fp8_activation_quantization_gb300 import synth
+    from fp8_activation_quantization_gb300.sharding import shard_rows
+    T = synth.WORKLOADS[SYNTH_OF.get(workload, workload)][0] if rows is None else int(rows)
+    align = 128 if T % 128 == 0 else 1
+    a, b = shard_rows(T * ws, ws, rank, align)
+    return a, b, T * ws
 
 
 def e2e_steps(prob: Problem, steps: int, stream):
@@ -561,9 +607,22 @@ def cpu_baseline_single_thread(workload: str, fmt: str, host: dict | None = None
             "rows_per_s": round(done / spent, 1)}
 
 
+def max_over_ranks(dt: float, ws: int, dev=None) -> float:
+    """The slowest rank's time (every rank gets it)."""
+    if ws <= 1:
+        return dt
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([dt], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
+    if ws != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE is {ws}")
     if ws > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
@@ -583,27 +642,24 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
     peak, peak_src = measured_peaks()
 
-    prob = Problem(args.workload, args.fmt, dev)
+    # this rank's shard of a batch of ws workloads' worth of rows (weak scaling)
+    row0, row1, rows_global = rank_shard(args.workload, ws, rank)
+    prob = Problem(args.workload, args.fmt, dev, row_begin=row0)
+    assert prob.T == row1 - row0
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = None
     tkq.tkq_read_device_status(clear=True)
     small = prob.bytes < SMALL_BYTES
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if small else None
+    l2 = l2_bytes(dev)
+    sets = rotation(prob, l2) if small else [prob]
     with torch.cuda.stream(stream):
         with ClockSampler(uuid) as clk:
-            if small:
-                dt = time_steps_flushed(prob, args.steps, args.warmup, stream, flush, barrier)
-            else:
-                dt = time_steps(prob, args.steps, args.warmup, stream, barrier)
+            dt = time_rotation(sets, args.steps, args.warmup, stream, barrier)
     if tkq.tkq_read_device_status():
         raise RuntimeError("a bounded wait inside a kernel gave up: timing is invalid")
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dt], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
+    dt = max_over_ranks(dt, ws, dev)
     total_bytes = prob.bytes * args.steps * ws
     gbs = total_bytes / dt / 1e9
     per_launch = dt / args.steps
@@ -631,7 +687,9 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic (seeded, generated on the host; see config.workload)",
         "config": workload_config(args.workload, args.fmt, ws),
+        "buffer_sets": len(sets),
         "pct_of_peak": round(100.0 * gbs / ws / peak, 2),
+        "pct_of_nominal_peak": round(100.0 * gbs / ws / NOMINAL_HBM_GBS, 2),
         "rows_per_s": round(rows_per_s, 1),
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
@@ -642,28 +700,81 @@ def run_ours(args):
             "traffic": profiled_traffic(prob.kern, args.workload),
             "algorithmic_bytes_per_launch": prob.bytes,
             "peak_source": peak_src,
+            "nominal_peak": NOMINAL_HBM_GBS,
+            "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
         },
     }
+    if ws > 1:
+        res["shards"] = {"rows_per_rank": prob.T, "rows_global": rows_global,
+                         "rank0_rows": [row0, row1]}
+    del sets
     if not args.no_extras and ws == 1:
         e_steps = max(3, min(args.steps, 20))
         edt, h2d, d2h = e2e_steps(prob, e_steps, stream)
         res["e2e"] = {"value": round(prob.bytes * e_steps / edt / 1e9, 2), "unit": "GB/s",
                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                       "ms_per_step": round(edt / e_steps * 1e3, 3)}
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if small else None
         with torch.cuda.stream(stream):
             tc = d2d_copy_reference(prob, stream, flush)
+        del flush
         res["d2d_copy"] = {"us": round(tc * 1e6, 2), "GB/s": round(prob.bytes / tc / 1e9, 1),
                            "bytes": prob.bytes - prob.bytes % 2,
                            "kernel_time_over_copy_time": round(per_launch / tc, 3),
                            "note": "cudaMemcpyAsync device-to-device of half the algorithmic "
                                    "bytes (read + write = the same traffic), timed like the kernel"}
         res["cpu_baseline"] = cpu_baseline_single_thread(args.workload, args.fmt, prob.host)
+        del prob
+        torch.cuda.empty_cache()
         res["per_workload"] = other_workloads(dev, stream, peak, args)
+        res["bar_80pct"] = bar_table(res["per_workload"], peak)
     print(json.dumps(res), flush=True)
     if ws > 1:
         barrier()
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_rotation(sets, steps: int, warmup: int, stream, barrier) -> float:
+    """K timed launches (seconds, CUDA events around the whole run) issued back
+    to back, launch i on buffer set i mod len(sets); W untimed launches first.
+    With one set this is plain back-to-back timing (inputs larger than L2)."""
+    import torch
+    k = len(sets)
+    for i in range(max(warmup, k)):
+        sets[i % k].launch(stream)
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        sets[i % k].launch(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end) / 1000.0
+
+
+# the north_star bar: the plain and fused casts at T >= 8192, judged on the
+# sustained (write-back inclusive) rate
+BAR_WORKLOADS = ["plain_outlier/e4m3", "plain_outlier/e5m2", "swiglu/e4m3",
+                 "swiglu_moe/e4m3", "swiglu_t/e4m3"]
+
+
+def bar_table(per_workload: dict, peak: float) -> dict:
+    out = {}
+    for key in BAR_WORKLOADS:
+        e = per_workload.get(key)
+        if not e:
+            continue
+        gbs = e["sustained"]["GB/s"]
+        out[key] = {"GB/s_sustained": gbs, "frac_of_measured": round(gbs / peak, 4),
+                    "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
+                    "pass_measured": gbs >= 0.8 * peak,
+                    "pass_nominal": gbs >= 0.8 * NOMINAL_HBM_GBS}
+    return out
 
 
 def d2d_copy_reference(prob: Problem, stream, flush):
@@ -691,14 +802,21 @@ def d2d_copy_reference(prob: Problem, stream, flush):
 
 
 def other_workloads(dev, stream, peak, args):
-    """Each kernel on every workload shape: median L2-flushed launch time."""
+    """Each kernel on every workload shape, timed two ways: `us`, the median of
+    single launches each preceded by an L2 flush (a cold start; the launch's
+    own write-back is partly left to the next flush), and `sustained`, launches
+    back to back over a rotation of buffer sets spanning four times L2 (every
+    launch's write-back paid inside the timed region, as in a stream of casts;
+    see time_sustained)."""
     import torch
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    l2 = l2_bytes(dev)
     out = {}
     for name, fmt, flags in [("plain_small", "e4m3", 0), ("plain_outlier", "e4m3", 0),
                              ("plain_outlier", "e5m2", 0), ("plain_outlier", "e4m3", 6),
                              ("plain_outlier", "e4m3", 8),
-                             ("swiglu", "e4m3", 0), ("swiglu_moe", "e4m3", 0),
+                             ("swiglu", "e4m3", 0), ("swiglu", "e4m3", 6),
+                             ("swiglu_moe", "e4m3", 0),
                              ("swiglu_moe", "e4m3", 6), ("swiglu_t", "e4m3", 0),
                              ("swiglu_t", "e4m3", 6),
                              ("swiglu_bwd", "e4m3", 0), ("per_channel", "e4m3", 0),
@@ -708,11 +826,20 @@ def other_workloads(dev, stream, peak, args):
         prob = Problem(name, fmt, dev, sf_flags=flags)
         with torch.cuda.stream(stream):
             t = time_flushed(prob, 20, stream, flush)
+            sets = rotation(prob, l2)
+            ts, n = time_sustained(sets, stream)
+        k = len(sets)
+        del sets
         gbs = prob.bytes / t / 1e9
+        gbs_s = prob.bytes / ts / 1e9
         key = f"{name}/{fmt}" + {0: "", 6: "/ue8m0-col-major-sf", 8: "/sf-inv"}[flags]
         out[key] = {"kernel": prob.kern, "us": round(t * 1e6, 2),
-                                "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                                "rows_per_s": round(prob.T / t, 1), "bytes": prob.bytes}
+                    "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                    "rows_per_s": round(prob.T / t, 1), "bytes": prob.bytes,
+                    "sustained": {"us": round(ts * 1e6, 2), "GB/s": round(gbs_s, 1),
+                                  "frac": round(gbs_s / peak, 4),
+                                  "frac_of_nominal": round(gbs_s / NOMINAL_HBM_GBS, 4),
+                                  "buffer_sets": k, "launches": n}}
         del prob
         torch.cuda.empty_cache()
     return out
@@ -725,15 +852,21 @@ def workload_config(workload: str, fmt: str, ws: int) -> dict:
     T, C, _ = synth.WORKLOADS[syn]
     weighted = "w" in synth.workload(syn, rows=1)
     nbytes = algorithmic_bytes(workload, T, C, weighted)
+    if nbytes < SMALL_BYTES:
+        l2 = ("launches back to back over a rotation of buffer sets (inputs and outputs; "
+              "buffer_sets of them) spanning at least 4x L2: every launch reads inputs "
+              "not in L2 and pays the write-back of earlier launches")
+    else:
+        l2 = "inputs larger than L2 (no flush between steps)"
     return {
         "workload": _workload_desc(workload),
         "T": T, "cols": C, "fmt": fmt, "group": 128,
         "weighted": weighted,
         "algorithmic_bytes_per_step": nbytes,
-        "l2": "L2 flushed (read of a 512 MB buffer) before every timed launch; "
-              "value = summed per-launch event times"
-        if nbytes < SMALL_BYTES else "inputs larger than L2 (no flush between steps)",
-        "parallelism": f"replicas x{ws} (rows independent, no collective)",
+        "l2": l2,
+        "parallelism": (f"dp{ws}: each rank quantizes its own {T}-row shard of a "
+                        f"{T * ws}-row batch (rows independent, no collective)"
+                        if ws > 1 else "single GPU (rows independent, no collective)"),
     }
 
 
@@ -774,7 +907,7 @@ def run_reference(args):
     step(min(rows, x_all.shape[0]))
     t_cal = time.perf_counter() - t0
     per_row = t_cal / min(rows, x_all.shape[0])
-    budget = 150.0  # seconds for warmup + steps
+    budget = args.ref_seconds  # seconds for warmup + steps
     r = int(budget / max(args.steps + args.warmup, 1) / per_row)
     r = max(128, min(x_all.shape[0], (r // 128) * 128))
     for _ in range(args.warmup):
@@ -803,6 +936,19 @@ def run_reference(args):
     print(json.dumps(res), flush=True)
 
 
+def launch_ranks(args) -> int:
+    """--gpus N > 1 outside torchrun: start N ranks on this node, one per GPU,
+    through torch.distributed.run, or fail when the node has fewer GPUs."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -813,9 +959,22 @@ def main():
     ap.add_argument("--fmt", default="e4m3", choices=["e4m3", "e5m2"])
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e, CPU baseline and the per-workload table")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: oracle time to aim for over warmup + steps")
     args = ap.parse_args()
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be >= 1")
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "ours":
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            print(f"bench.py: --gpus {args.gpus} needs {args.gpus} GPUs, {have} visible",
+                  file=sys.stderr)
+            sys.exit(2)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args))
     if args.impl == "reference":
         run_reference(args)
     else:

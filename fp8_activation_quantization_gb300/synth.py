@@ -104,99 +104,115 @@ def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def _chunked(T: int, fill) -> None:
-    """Run fill(chunk_index, row_begin, row_end) over fixed row chunks.  Each fill
-    draws a whole chunk's worth of numbers and keeps the rows it needs, so a
-    short last chunk holds the same values as the full workload's chunk."""
-    n = -(-T // CHUNK_ROWS)
-    if n <= 1:
-        for i in range(n):
-            fill(i, 0, T)
+def _chunked(T: int, fill, row_begin: int = 0) -> None:
+    """Run fill(chunk_index, lo, hi, dst) over the fixed row chunks that cover
+    rows [row_begin, row_begin + T) of the stream: chunk i keeps its local rows
+    [lo, hi) and writes them to the output rows ``dst`` (a slice).  Each fill
+    draws a whole chunk's worth of numbers, so any row range holds the same
+    values as the same rows of a longer draw."""
+    T, row_begin = int(T), int(row_begin)
+    if T <= 0:
+        return
+    first, last = row_begin // CHUNK_ROWS, (row_begin + T - 1) // CHUNK_ROWS
+
+    def one(i):
+        a = max(row_begin, i * CHUNK_ROWS)
+        b = min(row_begin + T, (i + 1) * CHUNK_ROWS)
+        fill(i, a - i * CHUNK_ROWS, b - i * CHUNK_ROWS, slice(a - row_begin, b - row_begin))
+
+    if first == last:
+        one(first)
         return
     with ThreadPoolExecutor(_threads()) as ex:
-        list(ex.map(lambda i: fill(i, i * CHUNK_ROWS, min(T, (i + 1) * CHUNK_ROWS)), range(n)))
+        list(ex.map(one, range(first, last + 1)))
 
 
-def normal_bf16(seed: int, stream: int, T: int, C: int, std: float = 1.0) -> np.ndarray:
-    """bf16 bits of a [T, C] matrix of N(0, std^2) samples."""
+def normal_bf16(seed: int, stream: int, T: int, C: int, std: float = 1.0,
+                row_begin: int = 0) -> np.ndarray:
+    """bf16 bits of a [T, C] matrix of N(0, std^2) samples (rows row_begin ..
+    row_begin + T - 1 of the stream)."""
     out = np.empty((int(T), int(C)), np.uint16)
 
-    def fill(i, a, b):
-        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
+    def fill(i, a, b, dst):
+        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[a:b]
         if std != 1.0:
             v *= np.float32(std)
-        _to_bf16_into(v, out[a:b])
+        _to_bf16_into(v, out[dst])
 
-    _chunked(int(T), fill)
+    _chunked(T, fill, row_begin)
     return out
 
 
 def outlier_bf16(seed: int, stream: int, T: int, C: int, frac: float = 1e-3,
                  factor: float = 100.0, zero_row_every: int = 1024,
-                 as_f32: bool = False) -> np.ndarray:
+                 as_f32: bool = False, row_begin: int = 0) -> np.ndarray:
     """N(0,1) with a fraction ``frac`` of entries, chosen by the generator,
-    multiplied by ``factor`` and every ``zero_row_every``-th row (from row 0) zero.
-    bf16 bits, or the binary32 values themselves with ``as_f32``."""
+    multiplied by ``factor`` and every ``zero_row_every``-th row of the stream
+    (from row 0) zero.  bf16 bits, or the binary32 values themselves with
+    ``as_f32``; rows row_begin .. row_begin + T - 1 of the stream."""
     out = np.empty((int(T), int(C)), np.float32 if as_f32 else np.uint16)
 
-    def fill(i, a, b):
+    def fill(i, a, b, dst):
         rng = rng_for(seed, stream, i)
-        v = rng.standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
-        mask = rng.random((CHUNK_ROWS, C), dtype=np.float32)[:b - a] < np.float32(frac)
+        v = rng.standard_normal((CHUNK_ROWS, C), dtype=np.float32)[a:b]
+        mask = rng.random((CHUNK_ROWS, C), dtype=np.float32)[a:b] < np.float32(frac)
         v[mask] *= np.float32(factor)
         if as_f32:
-            out[a:b] = v
+            out[dst] = v
         else:
-            _to_bf16_into(v, out[a:b])
+            _to_bf16_into(v, out[dst])
 
-    _chunked(int(T), fill)
+    _chunked(T, fill, row_begin)
     if zero_row_every:
-        out[::zero_row_every] = 0
+        out[(-int(row_begin)) % zero_row_every::zero_row_every] = 0
     return out
 
 
 def swiglu_bf16(seed: int, stream: int, T: int, H: int, gate_std: float = 1.0,
-                up_std: float = 1.0) -> np.ndarray:
-    """bf16 bits of a [T, 2H] gate | up matrix."""
+                up_std: float = 1.0, row_begin: int = 0) -> np.ndarray:
+    """bf16 bits of a [T, 2H] gate | up matrix (rows row_begin .. row_begin + T - 1
+    of the stream)."""
     out = np.empty((int(T), 2 * int(H)), np.uint16)
 
-    def fill(i, a, b):
+    def fill(i, a, b, dst):
         rng = rng_for(seed, stream, i)
-        g = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[:b - a]
+        g = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[a:b]
         if gate_std != 1.0:
             g *= np.float32(gate_std)
-        u = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[:b - a]
+        u = rng.standard_normal((CHUNK_ROWS, H), dtype=np.float32)[a:b]
         if up_std != 1.0:
             u *= np.float32(up_std)
-        _to_bf16_into(g, out[a:b, :H])
-        _to_bf16_into(u, out[a:b, H:])
+        _to_bf16_into(g, out[dst, :H])
+        _to_bf16_into(u, out[dst, H:])
 
-    _chunked(int(T), fill)
+    _chunked(T, fill, row_begin)
     return out
 
 
 def channel_outlier_bf16(seed: int, stream: int, T: int, C: int, every: int = 64,
-                         factor: float = 20.0) -> np.ndarray:
-    """N(0,1) with every ``every``-th channel (from channel 0) multiplied by ``factor``."""
+                         factor: float = 20.0, row_begin: int = 0) -> np.ndarray:
+    """N(0,1) with every ``every``-th channel (from channel 0) multiplied by
+    ``factor`` (rows row_begin .. row_begin + T - 1 of the stream)."""
     out = np.empty((int(T), int(C)), np.uint16)
 
-    def fill(i, a, b):
-        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[:b - a]
+    def fill(i, a, b, dst):
+        v = rng_for(seed, stream, i).standard_normal((CHUNK_ROWS, C), dtype=np.float32)[a:b]
         v[:, ::every] *= np.float32(factor)
-        _to_bf16_into(v, out[a:b])
+        _to_bf16_into(v, out[dst])
 
-    _chunked(int(T), fill)
+    _chunked(T, fill, row_begin)
     return out
 
 
-def random_bytes(seed: int, stream: int, T: int, C: int) -> np.ndarray:
-    """uint8 [T, C], every byte value equally likely."""
+def random_bytes(seed: int, stream: int, T: int, C: int, row_begin: int = 0) -> np.ndarray:
+    """uint8 [T, C], every byte value equally likely (rows row_begin ..
+    row_begin + T - 1 of the stream)."""
     out = np.empty((int(T), int(C)), np.uint8)
 
-    def fill(i, a, b):
-        out[a:b] = rng_for(seed, stream, i).integers(0, 256, (CHUNK_ROWS, C), np.uint8)[:b - a]
+    def fill(i, a, b, dst):
+        out[dst] = rng_for(seed, stream, i).integers(0, 256, (CHUNK_ROWS, C), np.uint8)[a:b]
 
-    _chunked(int(T), fill)
+    _chunked(T, fill, row_begin)
     return out
 
 
@@ -213,40 +229,47 @@ def routing_weights(seed: int, stream: int, tokens: int, topk: int = 8) -> np.nd
     return np.ascontiguousarray(w.astype(np.float32).reshape(-1))
 
 
-def workload(name: str, seed: int = 0, rows: int | None = None) -> dict:
+def workload(name: str, seed: int = 0, rows: int | None = None, row_begin: int = 0) -> dict:
     """Inputs of a named workload: dict with ``x`` (uint16 bf16 bits, row-major)
     and, for the weighted SwiGLU, ``w`` (fp32, one per row).  ``rows`` cuts the
-    workload to its first rows (same distribution), which quick tests use."""
+    workload to its first rows (same distribution), which quick tests use.
+    ``row_begin`` shifts the window: the result is rows [row_begin, row_begin +
+    rows) of one longer draw of the same workload (a shard of a batch of several
+    workloads' worth of rows, as the ranks of a multi-GPU run quantize it)."""
     if name not in WORKLOADS:
         raise KeyError(name)
     T, C, _ = WORKLOADS[name]
     if rows is not None:
         T = int(rows)
+    a = int(row_begin)
+    if a < 0:
+        raise ValueError("row_begin must be >= 0")
     sid = _WORKLOAD_IDS[name]
     if name == "plain_small":
-        return {"x": normal_bf16(seed, sid, T, C)}
+        return {"x": normal_bf16(seed, sid, T, C, row_begin=a)}
     if name == "plain_outlier":
-        return {"x": outlier_bf16(seed, sid, T, C)}
+        return {"x": outlier_bf16(seed, sid, T, C, row_begin=a)}
     if name == "swiglu":
-        return {"x": swiglu_bf16(seed, sid, T, C // 2, gate_std=2.0, up_std=1.0)}
-    if name == "swiglu_moe":
+        return {"x": swiglu_bf16(seed, sid, T, C // 2, gate_std=2.0, up_std=1.0, row_begin=a)}
+    if name in ("swiglu_moe", "swiglu_bwd"):
         topk = 8
-        w = routing_weights(seed, sid, -(-T // topk), topk)[:T]
-        return {"x": swiglu_bf16(seed, sid, T, C // 2), "w": np.ascontiguousarray(w)}
+        # the weights of every token up to the window's end, then the window
+        w = routing_weights(seed, sid, -(-(a + T) // topk), topk)[a:a + T]
+        d = {"x": swiglu_bf16(seed, sid, T, C // 2, row_begin=a)}
+        if name == "swiglu_bwd":
+            d["dy"] = normal_bf16(seed, sid + 100, T, C // 2, row_begin=a)
+        d["w"] = np.ascontiguousarray(w)
+        return d
     if name == "swiglu_t":
-        return {"x": swiglu_bf16(seed, sid, T, C // 2)}
-    if name == "swiglu_bwd":
-        topk = 8
-        w = routing_weights(seed, sid, -(-T // topk), topk)[:T]
-        return {"x": swiglu_bf16(seed, sid, T, C // 2),
-                "dy": normal_bf16(seed, sid + 100, T, C // 2), "w": np.ascontiguousarray(w)}
+        return {"x": swiglu_bf16(seed, sid, T, C // 2, row_begin=a)}
     if name == "per_channel":
-        return {"x": channel_outlier_bf16(seed, sid, T, C)}
+        return {"x": channel_outlier_bf16(seed, sid, T, C, row_begin=a)}
     if name == "per_block":
-        return {"x": outlier_bf16(seed, sid, T, C, zero_row_every=0)}
+        return {"x": outlier_bf16(seed, sid, T, C, zero_row_every=0, row_begin=a)}
     if name == "plain_f32":
-        return {"x": outlier_bf16(seed, sid, T, C, as_f32=True)}
+        return {"x": outlier_bf16(seed, sid, T, C, as_f32=True, row_begin=a)}
     if name == "cast_back":
-        return {"codes": random_bytes(seed, sid, T, C),
-                "sf": log_uniform_f32(seed, sid, (T, C // 128), -22.0, 4.0)}
+        sf = log_uniform_f32(seed, sid, (a + T, C // 128), -22.0, 4.0)[a:]
+        return {"codes": random_bytes(seed, sid, T, C, row_begin=a),
+                "sf": np.ascontiguousarray(sf)}
     raise KeyError(name)

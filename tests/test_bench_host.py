@@ -98,4 +98,5 @@ def test_both_arms_describe_the_same_config():
     assert bench.workload_config("swiglu_moe", "e4m3", 1)["weighted"]
     assert not bench.workload_config("swiglu_t", "e4m3", 1)["weighted"]
     assert "larger than L2" in bench.workload_config("swiglu_t", "e4m3", 1)["l2"]
-    assert "flushed" in bench.workload_config("plain_outlier", "e4m3", 1)["l2"]
+    assert "rotation of buffer sets" in bench.workload_config("plain_outlier", "e4m3", 1)["l2"]
+    assert "dp2" in bench.workload_config("swiglu_t", "e4m3", 2)["parallelism"]
