@@ -462,6 +462,30 @@ def time_sustained(probs, stream, min_launches: int = 200):
     return dt, n
 
 
+class CopyProblem:
+    """A device-to-device copy moving the same bytes as one launch of a
+    workload (half read, half written): what the memory system gives a launch
+    of that size, timed the same way as the kernel."""
+
+    def __init__(self, nbytes: int, dev):
+        import torch
+        n = max(16, nbytes // 2)
+        self.src = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.dst = torch.empty_like(self.src)
+        self.bytes = 2 * n
+
+    def launch(self, stream):
+        import torch
+        with torch.cuda.stream(stream):
+            self.dst.copy_(self.src)
+
+
+def copy_rotation(nbytes: int, dev, l2: int):
+    first = CopyProblem(nbytes, dev)
+    return [first] + [CopyProblem(nbytes, dev)
+                      for _ in range(max(2, -(-4 * l2 // first.bytes)) - 1)]
+
+
 def rotation(prob: Problem, l2: int):
     """The buffer sets of a sustained timing: `prob` and copies of it."""
     sets = [prob]
@@ -644,7 +668,7 @@ def run_ours(args):
 
     # this rank's shard of a batch of ws workloads' worth of rows (weak scaling)
     row0, row1, rows_global = rank_shard(args.workload, ws, rank)
-    prob = Problem(args.workload, args.fmt, dev, row_begin=row0)
+    prob = Problem(args.workload, args.fmt, dev, row_begin=row0, sf_flags=args.sf_flags)
     assert prob.T == row1 - row0
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -657,9 +681,13 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         with ClockSampler(uuid) as clk:
             dt = time_rotation(sets, args.steps, args.warmup, stream, barrier)
+        # the same launches issued one by one from the host, for comparison
+        dt_stream = time_rotation(sets, min(args.steps, 200), 0, stream, barrier, graph=False)
+        dt_stream *= args.steps / min(args.steps, 200)
     if tkq.tkq_read_device_status():
         raise RuntimeError("a bounded wait inside a kernel gave up: timing is invalid")
     dt = max_over_ranks(dt, ws, dev)
+    dt_stream = max_over_ranks(dt_stream, ws, dev)
     total_bytes = prob.bytes * args.steps * ws
     gbs = total_bytes / dt / 1e9
     per_launch = dt / args.steps
@@ -692,6 +720,8 @@ def run_ours(args):
         "pct_of_nominal_peak": round(100.0 * gbs / ws / NOMINAL_HBM_GBS, 2),
         "rows_per_s": round(rows_per_s, 1),
         "gpu_launches": args.steps,
+        "launch": "the K timed launches captured in one CUDA graph, timed as one replay",
+        "ms_per_step_stream_launches": round(dt_stream / args.steps * 1e3, 5),
         "clocks": clk.summary(),
         "roofline": {
             "bound": "hbm", "kernel": prob.kern,
@@ -735,22 +765,39 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def time_rotation(sets, steps: int, warmup: int, stream, barrier) -> float:
-    """K timed launches (seconds, CUDA events around the whole run) issued back
-    to back, launch i on buffer set i mod len(sets); W untimed launches first.
-    With one set this is plain back-to-back timing (inputs larger than L2)."""
+def time_rotation(sets, steps: int, warmup: int, stream, barrier, graph: bool = True) -> float:
+    """K timed launches (seconds, CUDA events around the whole run) back to
+    back, launch i on buffer set i mod len(sets); W untimed launches first.
+    With one set this is plain back-to-back timing (inputs larger than L2).
+    graph: the K launches are captured in one CUDA graph and the timed region
+    is its replay (the warm-up launches run before the capture, and one
+    untimed replay after it); otherwise each launch is issued from the host
+    inside the timed region."""
     import torch
     k = len(sets)
     for i in range(max(warmup, k)):
         sets[i % k].launch(stream)
+    torch.cuda.synchronize()
+    g = None
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for i in range(steps):
+                sets[i % k].launch(stream)
+        with torch.cuda.stream(stream):
+            g.replay()
     torch.cuda.synchronize()
     barrier()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(steps):
-        sets[i % k].launch(stream)
+    if graph:
+        with torch.cuda.stream(stream):
+            g.replay()
+    else:
+        for i in range(steps):
+            sets[i % k].launch(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -828,8 +875,11 @@ def other_workloads(dev, stream, peak, args):
             t = time_flushed(prob, 20, stream, flush)
             sets = rotation(prob, l2)
             ts, n = time_sustained(sets, stream)
-        k = len(sets)
-        del sets
+            k = len(sets)
+            del sets
+            copies = copy_rotation(prob.bytes, dev, l2)
+            tc, _ = time_sustained(copies, stream)
+            del copies
         gbs = prob.bytes / t / 1e9
         gbs_s = prob.bytes / ts / 1e9
         key = f"{name}/{fmt}" + {0: "", 6: "/ue8m0-col-major-sf", 8: "/sf-inv"}[flags]
@@ -839,7 +889,9 @@ def other_workloads(dev, stream, peak, args):
                     "sustained": {"us": round(ts * 1e6, 2), "GB/s": round(gbs_s, 1),
                                   "frac": round(gbs_s / peak, 4),
                                   "frac_of_nominal": round(gbs_s / NOMINAL_HBM_GBS, 4),
-                                  "buffer_sets": k, "launches": n}}
+                                  "buffer_sets": k, "launches": n,
+                                  "copy_us": round(tc * 1e6, 2),
+                                  "kernel_time_over_copy_time": round(ts / tc, 3)}}
         del prob
         torch.cuda.empty_cache()
     return out
@@ -959,6 +1011,8 @@ def main():
     ap.add_argument("--fmt", default="e4m3", choices=["e4m3", "e5m2"])
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e, CPU baseline and the per-workload table")
+    ap.add_argument("--sf-flags", type=int, default=0,
+                    help="scale-layout flags (TKQ_SF_*) of the timed cast")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="--impl reference: oracle time to aim for over warmup + steps")
     args = ap.parse_args()

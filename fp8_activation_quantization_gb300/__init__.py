@@ -144,6 +144,7 @@ def _open(path):
 
 
 DEVICE_TIMEOUT = 1
+ERR_TIMEOUT = 7    # tkq_read_device_status: the status word holds DEVICE_TIMEOUT
 DEVICE_OUT_OF_BOUNDS = 2
 
 
@@ -164,10 +165,11 @@ def tkq_read_check_address(clear: bool = False) -> int:
 
 def tkq_read_device_status(clear: bool = False) -> int:
     """Synchronize the current device and return its status word (bit
-    DEVICE_TIMEOUT: a bounded wait inside a kernel gave up)."""
+    DEVICE_TIMEOUT: a bounded wait inside a kernel gave up; the C call then
+    returns ERR_TIMEOUT, which here is the word's bit, not an exception)."""
     v = ctypes.c_uint32(0)
     st = (_lib or load_library()).tkq_read_device_status(ctypes.byref(v), 1 if clear else 0)
-    if st:
+    if st and st != ERR_TIMEOUT:
         raise TkqError(st, "tkq_read_device_status")
     return int(v.value)
 
@@ -404,7 +406,8 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
     ``with_transpose``, also (codes_t [H, T], scales_t [H, T/128]).
     ``topk_weights``: optional fp32 [T] routing weight per row.  The scale-layout
     options apply to the row scales and, with ``with_transpose``, to the column
-    scales as an [H, T/128] matrix (see ``sf_tensor`` for the shapes).
+    scales as an [H, T/128] matrix (see ``sf_tensor`` for the shapes).  Codes
+    are those of the product y * fl32(1 / s) (the TileKernels sf_inv reading).
     ``use_clamp``: clamp the gate to <= swiglu_clamp_value and the up projection
     to [-swiglu_clamp_value, swiglu_clamp_value] before the SwiGLU; the number of
     changed values is added to ``clamp_count`` (a zeroed int64 CUDA tensor of one
@@ -469,7 +472,8 @@ def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int 
                                        use_tma_aligned_col_major_sf: bool = False):
     """Gradients of y = silu(gate) * up [* w] from dy, cast per token.
     x: bf16 [T, 2H] (gate | up); dy: bf16 [T, H] -> (codes [T, 2H] of [dg | du],
-    scales [T, 2H/128] or the chosen scale layout)."""
+    scales [T, 2H/128] or the chosen scale layout); codes of the products by
+    fl32(1 / s), like the forward cast."""
     import torch
     _check_input(x)
     _check_input(dy, "dy")

@@ -22,8 +22,10 @@ LIB_CHECKED = os.path.join(LIBDIR, "libtkq_checked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# no --use_fast_math: the kernels rely on IEEE division / reciprocal and an
-# accurate expf
+# no --use_fast_math: the scale and the exact quotient of every cast are built
+# from IEEE-rounded products, FMAs and the correctly rounded reciprocal
+# (__frcp_rn), which fast math would replace; the SwiGLU kernels' ex2.approx /
+# rcp.approx are requested explicitly in inline PTX
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC"]
 
 

@@ -82,6 +82,7 @@ template <int FMT, int GC, int GR_SHIFT, bool BF16>
 __global__ void __launch_bounds__(kThreads, BF16 ? 8 : 6)
     cast_back_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ sf,
                      uint8_t* __restrict__ out, int64_t T, int64_t C) {
+    grid_dependency_sync();  // the previous grid on the stream is done
     constexpr int kOutBytes = BF16 ? 2 : 4;
     constexpr int kVecs = kOutBytes;   // 16-byte output vectors per thread and unit
     __shared__ __align__(128) uint4 buf[2][kThreads * kVecs];
@@ -142,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, BF16 ? 8 : 6)
                 }
 #pragma unroll
                 for (int i = 0; i < 8; i += 2) {
-                    const float2 p = mul2(make_float2(y[i], y[i + 1]), make_float2(sc[i], sc[i + 1]));
+                    const float2 p =
+                        mul2(make_float2(y[i], y[i + 1]), make_float2(sc[i], sc[i + 1]));
                     y[i] = p.x;
                     y[i + 1] = p.y;
                 }
@@ -181,9 +183,8 @@ cudaError_t launch(const void* codes, const float* sf, void* out, int64_t T, int
     const int64_t n_units = (T * C + kChunk - 1) / kChunk;
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0, n_units);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kThreads, 0, stream>>>(static_cast<const uint8_t*>(codes), sf,
-                                     static_cast<uint8_t*>(out), T, C);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint8_t*>(codes), sf,
+                      static_cast<uint8_t*>(out), T, C);
 }
 
 template <int FMT, bool BF16>

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dependency_sync();  // the previous grid on the stream is done
 
     // ------------------------------------------------------------ producer
     if (warp == kConsumerWarps) {
@@ -300,9 +301,10 @@ cudaError_t launch_mode(const CUtensorMap& map, const CUtensorMap& map_dy, const
     const int64_t n_chunks = ((T + kRows - 1) / kRows) * (C_out / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, smem, n_chunks);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kThreads, smem, stream>>>(map, map_dy, w, static_cast<uint2*>(out), sf, lay, T,
-                                        static_cast<int>(C_out), clamp, device_status_word());
-    return cudaGetLastError();
+    // the backward cast measured slower with programmatic dependent launch
+    return launch_pdl(k, grid, kThreads, smem, stream, !ModeTraits<MODE>::kBwd, map, map_dy, w,
+                      static_cast<uint2*>(out), sf, lay, T, static_cast<int>(C_out), clamp,
+                      device_status_word());
 }
 
 template <int FMT, int MODE>

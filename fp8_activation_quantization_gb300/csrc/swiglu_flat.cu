@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
     swiglu_flat_kernel(const uint4* __restrict__ x, const float* __restrict__ w,
                        uint4* __restrict__ out, float* __restrict__ sf, SfLayout lay, int64_t H,
                        int64_t n_groups, int64_t n_walk, FlatClamp clamp) {
+    grid_dependency_sync();  // the previous grid on the stream is done
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;   // group within the unit
     const int k = lane & 7;      // lane within the group
@@ -207,9 +208,8 @@ cudaError_t launch_layout(const void* x, const float* w, void* out, float* sf,
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0,
                                      (units + kWarps - 1) / kWarps);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(x), w, static_cast<uint4*>(out),
-                                     sf, lay, H, n_groups, n_walk, clamp);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint4*>(x), w,
+                      static_cast<uint4*>(out), sf, lay, H, n_groups, n_walk, clamp);
 }
 
 template <int FMT, bool WEIGHTED, int CLAMP>

@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(kChThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dependency_sync();  // the previous grid on the stream is done
     if (warp == kChWarps) {
         if (lane == 0)
             produce_tiles<kChStages, kTileBytes>(sm.stage, sm.full, sm.empty, &sm.abort, &tmap, CB,
@@ -179,9 +180,8 @@ cudaError_t launch_channel(const void* x, void* out, float* sf, int64_t T, int64
     const int64_t n_tiles = (T / 128) * (C / 128);
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kChThreads, smem, n_tiles);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kChThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
-                                          static_cast<int>(C), device_status_word());
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kChThreads, smem, stream, true, map, static_cast<uint8_t*>(out),
+                      sf, T, static_cast<int>(C), device_status_word());
 }
 
 // ---------------------------------------------------------------------------
@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dependency_sync();  // the previous grid on the stream is done
 
     if (warp == kCtGroups * kCtGroupWarps) {   // producer
         if (lane == 0)
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dependency_sync();  // the previous grid on the stream is done
 
     if (warp == kCtGroups * kCtGroupWarps) {   // producer
         if (lane == 0)
@@ -482,9 +484,8 @@ cudaError_t launch_block(const void* x, void* out, float* sf, int64_t T, int64_t
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
                                      (n_tiles + 1) / 2);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kCtThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
-                                          static_cast<int>(C), device_status_word());
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kCtThreads, smem, stream, true, map, static_cast<uint8_t*>(out),
+                      sf, T, static_cast<int>(C), device_status_word());
 }
 
 template <int FMT>
@@ -498,9 +499,9 @@ cudaError_t launch_channel_t(const void* x, void* out, float* sf, int64_t T, int
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
                                      (n_tiles + 1) / 2);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kCtThreads, smem, stream>>>(map, static_cast<uint8_t*>(out), sf, T,
-                                            static_cast<int>(C), device_status_word());
-    return cudaGetLastError();
+    // measured slower with programmatic dependent launch
+    return launch_pdl(k, grid, kCtThreads, smem, stream, false, map, static_cast<uint8_t*>(out),
+                      sf, T, static_cast<int>(C), device_status_word());
 }
 
 }  // namespace

@@ -595,7 +595,7 @@ tkq_status tkq_read_device_status(uint32_t* flags, int clear) {
             return TKQ_ERR_CUDA;
     }
     *flags = v;
-    return TKQ_OK;
+    return (v & TKQ_DEVICE_TIMEOUT) ? TKQ_ERR_TIMEOUT : TKQ_OK;
 }
 
 tkq_status tkq_selftest_wait_timeout(int64_t limit_ns, tkq_stream_t stream) {
@@ -616,6 +616,8 @@ const char* tkq_status_string(int status) {
         case TKQ_ERR_FMT: return "TKQ_ERR_FMT: unknown FP8 format";
         case TKQ_ERR_ALIGN: return "TKQ_ERR_ALIGN: misaligned pointer";
         case TKQ_ERR_CUDA: return "TKQ_ERR_CUDA: kernel launch failed";
+        case TKQ_ERR_TIMEOUT:
+            return "TKQ_ERR_TIMEOUT: a bounded wait inside a kernel gave up (outputs incomplete)";
         case TKQ_ERR_ALIAS: return "TKQ_ERR_ALIAS: buffers overlap";
         case TKQ_ERR_FLAGS: return "TKQ_ERR_FLAGS: unknown option flags";
         case TKQ_ERR_VALUE: return "TKQ_ERR_VALUE: invalid scalar argument";
@@ -623,7 +625,7 @@ const char* tkq_status_string(int status) {
     }
 }
 
-int tkq_version(void) { return 100; }
+int tkq_version(void) { return 200; }
 
 int tkq_checked_build(void) {
 #ifdef TKQ_CHECKED

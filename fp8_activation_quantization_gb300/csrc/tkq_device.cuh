@@ -81,6 +81,19 @@ __device__ __forceinline__ bool access_ok(const void* p, unsigned bytes, bool wr
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Called by every thread of a cast before its first global access (launched
+// by launch_pdl, tkq_internal.h): first lets the next grid on the stream be
+// scheduled (it will wait here in turn), then waits until the grid before it
+// has completed and its memory operations are visible.  Without a preceding
+// PDL launch the wait returns at once.
+__device__ __forceinline__ void grid_dependency_sync() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // memory access
 // ---------------------------------------------------------------------------
 
@@ -93,6 +106,15 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
     return r;
+}
+
+// Asks L2 to fetch `bytes` (a multiple of 16) from global memory at p (16-byte
+// aligned) ahead of the loads that will read them: one bulk prefetch, which
+// holds no registers and which nothing waits on.  The range must lie inside
+// an input buffer of the call (checked like a load in the checked build).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    if (!access_ok(p, bytes, false)) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Read-only loads through the non-coherent path (small per-row operands).
@@ -348,8 +370,9 @@ __device__ __forceinline__ float absmax8(const float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// SwiGLU ("DeepSeek开源TileKernels..." §3.3: val_l / (1 + exp(-val_l)) * val_r)
-// with the SM's transcendental unit:
+// SwiGLU, y = silu(g) * u with silu(g) = g / (1 + exp(-g)), g the gate and u
+// the up half ("DeepSeek开源TileKernels..." §3.3), with the SM's
+// transcendental unit:
 //   exp(-g) = 2^(-g * log2 e)      hardware base-2 exponential (ex2.approx)
 //   g / (1 + exp(-g))              hardware reciprocal (rcp.approx) times g
 // Error against exactly rounded binary32 steps: the product t = -g * log2 e is
@@ -475,9 +498,11 @@ __device__ __forceinline__ uint32_t quantize4(const float* v, float s, float inv
 
 // The SwiGLU kernels quantize y * inv, the product by the rounded reciprocal of
 // the scale, as the TileKernels per-token kernel does (x * sf_inv, "DeepSeek开源
-// TileKernels..." §3.2 step 4).  It is within one ulp of y / s; y itself carries
-// a few ulp of exp error, so the exact quotient would buy nothing measurable
-// there, while the plain cast keeps `quotient` to be bit-exact.
+// TileKernels..." §3.2, step 4).  It is within one ulp of y / s, and y itself
+// carries a few ulp of exp error.  The exact quotient (quotient2) was measured
+// in all three SwiGLU kernels: free in the flat stream, +2 % in the TMA ring,
+// +6 to +17 % in the transposed kernel, whose rows must equal the row cast's;
+// the plain casts keep `quotient` and are bit-exact.
 template <int FMT>
 __device__ __forceinline__ uint32_t quantize4_mul(const float* v, float inv) {
     const float2 i2 = make_float2(inv, inv);

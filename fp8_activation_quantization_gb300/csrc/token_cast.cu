@@ -73,6 +73,7 @@ template <int FMT, bool F32, bool SFX>
 __global__ void __launch_bounds__(kThreads, 4)
     token_cast_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
                       float* __restrict__ sf, SfLayout lay, int64_t n_groups, int64_t n_walk) {
+    grid_dependency_sync();  // the previous grid on the stream is done
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;    // group within the unit
     const int j = lane & 7;       // lane within the group
@@ -152,9 +153,8 @@ cudaError_t launch_layout(const void* x, void* out, float* sf, const SfLayout& l
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0,
                                      (units + kWarps - 1) / kWarps);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    k<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(out), sf,
-                                     lay, n_groups, n_walk);
-    return cudaGetLastError();
+    return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint4*>(x),
+                      static_cast<uint4*>(out), sf, lay, n_groups, n_walk);
 }
 
 template <bool F32>

@@ -42,6 +42,11 @@
  *   T == 0 is an empty batch: TKQ_OK, nothing is launched and the pointers
  *   may be NULL.
  * - A failed launch returns TKQ_ERR_CUDA (cudaGetLastError after the launch).
+ * - A kernel that runs into trouble on the device (a bounded wait for its
+ *   copies that gave up, see tkq_read_device_status) cannot change the status
+ *   its asynchronous call already returned; it records the event in the
+ *   device status word, and tkq_read_device_status reports it as
+ *   TKQ_ERR_TIMEOUT.
  * - Environment (for tests and measurements; no result depends on it):
  *   TKQ_NUM_SMS=n sizes the persistent grids for n SMs; TKQ_SWIGLU_KERNEL=flat
  *   or =ring runs the SwiGLU forward cast through one of its two bit-identical
@@ -75,9 +80,10 @@ typedef enum {
     TKQ_ERR_FMT = 4,
     TKQ_ERR_ALIGN = 5,
     TKQ_ERR_CUDA = 6,
-    TKQ_ERR_ALIAS = 7,
-    TKQ_ERR_FLAGS = 8,
-    TKQ_ERR_VALUE = 9
+    TKQ_ERR_TIMEOUT = 7,  /* a bounded in-kernel wait gave up (tkq_read_device_status) */
+    TKQ_ERR_ALIAS = 8,
+    TKQ_ERR_FLAGS = 9,
+    TKQ_ERR_VALUE = 10
 } tkq_status;
 
 /* A cudaStream_t passed as an opaque pointer. */
@@ -209,8 +215,10 @@ tkq_status tkq_swiglu_cast_t_ex(const void* x, const float* w, void* out, void* 
  * one second, sets TKQ_DEVICE_TIMEOUT in the current device's status word and
  * lets the kernel return (its outputs are then incomplete) instead of hanging.
  * tkq_read_device_status synchronizes the current device, stores the word in
- * *flags and, if clear != 0, resets it.  Errors: TKQ_ERR_NULL (flags NULL),
- * TKQ_ERR_CUDA (the synchronization or copy failed).
+ * *flags and, if clear != 0, resets it.  Returns TKQ_ERR_TIMEOUT when the word
+ * it read holds TKQ_DEVICE_TIMEOUT (*flags is set then too), else TKQ_OK.
+ * Errors: TKQ_ERR_NULL (flags NULL), TKQ_ERR_CUDA (the synchronization or
+ * copy failed).
  * (Not from the source pages: this is the library's failure reporting.)
  */
 #define TKQ_DEVICE_TIMEOUT 1u

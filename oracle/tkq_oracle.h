@@ -12,7 +12,8 @@
  *  [P2] "DeepSeek开源TileKernels：用Python写的GPU算子逼近硬件性能上限"
  *       (itsolotime.com): §3.1 quantisation config (clamp_min_value),
  *       §3.2 per-token cast kernel (group absmax -> scale -> codes),
- *       §3.3 SwiGLU fused with the cast (val_l / (1 + exp(-val_l)) * val_r * w).
+ *       §3.3 SwiGLU fused with the cast (y = silu(g) * u * w, g the gate and u
+ *       the up half).
  *  [P1] "TileKernels 与 DeepGEMM 的分界线：DeepSeek 开源内核栈的分工"
  *       (chatdocs.ruinique.com): §2 operator table (per_token_cast,
  *       per_channel_cast (+transpose / fused), swiglu_forward_and_per_token_cast).

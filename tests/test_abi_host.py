@@ -61,11 +61,14 @@ def test_library_is_built_for_sm_103a():
 def test_status_strings(lib):
     import fp8_activation_quantization_gb300 as tkq
     for code, word in [(0, "TKQ_OK"), (1, "NULL"), (2, "SHAPE"), (3, "GROUP"), (4, "FMT"),
-                       (5, "ALIGN"), (6, "CUDA"), (7, "ALIAS"), (99, "UNKNOWN")]:
+                       (5, "ALIGN"), (6, "CUDA"), (7, "TIMEOUT"), (8, "ALIAS"), (9, "FLAGS"),
+                       (10, "VALUE"), (99, "UNKNOWN")]:
         assert word in tkq.tkq_status_string(code)
 
 
 FAKE = 0x7F0000000000  # never dereferenced: every case below fails validation first
+# the status codes of tkq.h that follow TKQ_ERR_CUDA = 6 and TKQ_ERR_TIMEOUT = 7
+ALIAS, FLAGS, VALUE = 8, 9, 10
 
 
 def p(off=0):
@@ -82,8 +85,8 @@ def p(off=0):
     ((p(8), p(1 << 20), p(2 << 20), 4, 256, 128, 0), 5),          # x misaligned
     ((p(), p((1 << 20) + 4), p(2 << 20), 4, 256, 128, 0), 5),     # out misaligned
     ((p(), p(1 << 20), p((2 << 20) + 2), 4, 256, 128, 0), 5),     # sf misaligned
-    ((p(), p(512), p(2 << 20), 4, 256, 128, 0), 7),               # out overlaps x
-    ((p(), p(1 << 20), p((1 << 20) + 512), 4, 256, 128, 0), 7),   # sf overlaps out
+    ((p(), p(512), p(2 << 20), 4, 256, 128, 0), ALIAS),               # out overlaps x
+    ((p(), p(1 << 20), p((1 << 20) + 512), 4, 256, 128, 0), ALIAS),   # sf overlaps out
     ((None, None, None, 0, 256, 128, 0), 0),                      # empty batch
 ])
 def test_per_token_cast_validation(lib, args, expected):
@@ -92,7 +95,7 @@ def test_per_token_cast_validation(lib, args, expected):
 
 @pytest.mark.parametrize("args,expected", [
     ((p(), None, p(1 << 24), None, 4, 256, 128, 0), 1),
-    ((p(), p((1 << 24) + 4), p(1 << 24), p(2 << 24), 4, 256, 128, 0), 7),  # w overlaps out
+    ((p(), p((1 << 24) + 4), p(1 << 24), p(2 << 24), 4, 256, 128, 0), ALIAS),  # w overlaps out
     ((p(), p(4), p(1 << 24), p(2 << 24), 0, 256, 128, 0), 0),     # empty batch
     ((p(), p(1 << 26), p(1 << 24), p(2 << 24), 4, 100, 128, 0), 2),
     ((p(), p((1 << 26) + 2), p(1 << 24), p(2 << 24), 4, 256, 128, 0), 5),
@@ -115,8 +118,8 @@ def test_swiglu_cast_t_validation(lib, T, expected):
     ((p(), None, None, p(1 << 24), p(2 << 24), 4, 256, 128, 0), 1),          # dy NULL
     ((p(), p(1 << 22), None, p(1 << 24), p(2 << 24), 4, 200, 128, 0), 2),    # H % 128
     ((p(), p((1 << 22) + 8), None, p(1 << 24), p(2 << 24), 4, 256, 128, 0), 5),  # dy misaligned
-    ((p(), p(1 << 22), None, p(512), p(2 << 24), 4, 256, 128, 0), 7),        # out overlaps x
-    ((p(), p(1 << 22), None, p(1 << 24), p((1 << 24) + 64), 4, 256, 128, 0), 7),  # sf in out
+    ((p(), p(1 << 22), None, p(512), p(2 << 24), 4, 256, 128, 0), ALIAS),        # out overlaps x
+    ((p(), p(1 << 22), None, p(1 << 24), p((1 << 24) + 64), 4, 256, 128, 0), ALIAS),  # sf in out
     ((None, None, None, None, None, 0, 256, 128, 0), 0),                       # empty batch
 ])
 def test_swiglu_backward_validation(lib, args, expected):
@@ -136,7 +139,7 @@ def test_sf_bytes(lib):
 
 
 @pytest.mark.parametrize("flags,sf_off,expected", [
-    (16, 0, 8),           # unknown flag bit
+    (16, 0, FLAGS),           # unknown flag bit
     (4, 4, 5),            # column-major scales must be 16-byte aligned
     (6, 8, 5),            # packed column-major too
     (2, 2, 5),            # packed row-major: 4-byte aligned
@@ -149,8 +152,8 @@ def test_ex_validation(lib, flags, sf_off, expected):
 def test_ex_empty_batch_and_flags(lib):
     assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 6, None) == 0
     assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 9, None) == 0
-    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 17, None) == 8
-    assert lib.tkq_swiglu_cast_ex(None, None, None, None, 0, 256, 128, 0, 16, None) == 8
+    assert lib.tkq_per_token_cast_ex(None, None, None, 0, 256, 128, 0, 17, None) == FLAGS
+    assert lib.tkq_swiglu_cast_ex(None, None, None, None, 0, 256, 128, 0, 16, None) == FLAGS
     assert lib.tkq_swiglu_backward_cast_ex(None, None, None, None, None, 0, 256, 128, 0, 4,
                                            None) == 0
 
@@ -164,7 +167,7 @@ def test_status_calls_validate_before_cuda(lib):
 def test_swiglu_cast_t_output_alias(lib):
     # out_t overlapping out
     assert lib.tkq_swiglu_cast_t(p(), None, p(1 << 24), p(2 << 24), p((1 << 24) + 256),
-                                 p(4 << 24), 128, 256, 128, 0, None) == 7
+                                 p(4 << 24), 128, 256, 128, 0, None) == ALIAS
 
 
 @pytest.mark.parametrize("args,expected", [
@@ -175,8 +178,8 @@ def test_swiglu_cast_t_output_alias(lib):
     ((p(), p(1 << 20), p(2 << 20), 256, 256, 128, 5, 0), 4),          # fmt
     ((p(), p((1 << 20) + 8), p(2 << 20), 256, 256, 128, 0, 1), 5),    # out misaligned
     ((p(), p(1 << 20), p((2 << 20) + 1), 256, 256, 128, 0, 0), 5),    # sf misaligned
-    ((p(), p(1 << 16), p(2 << 20), 256, 256, 128, 0, 0), 7),          # out overlaps x
-    ((p(), p(1 << 20), p((1 << 20) + 4096), 256, 256, 128, 0, 1), 7), # sf overlaps out
+    ((p(), p(1 << 16), p(2 << 20), 256, 256, 128, 0, 0), ALIAS),          # out overlaps x
+    ((p(), p(1 << 20), p((1 << 20) + 4096), 256, 256, 128, 0, 1), ALIAS), # sf overlaps out
     ((None, None, None, 0, 256, 128, 0, 1), 0),                       # empty batch
 ])
 def test_per_channel_cast_validation(lib, args, expected):
@@ -189,7 +192,7 @@ def test_per_channel_cast_validation(lib, args, expected):
     ((p(), p(1 << 20), p(2 << 20), 300, 256, 256, 0), 3),             # block
     ((p(), p(1 << 20), p(2 << 20), 300, 256, 128, -1), 4),            # fmt
     ((p(4), p(1 << 20), p(2 << 20), 300, 256, 128, 0), 5),            # x misaligned
-    ((p(), p(1 << 20), p((1 << 20) + 65536), 300, 256, 128, 0), 7),   # sf overlaps out
+    ((p(), p(1 << 20), p((1 << 20) + 65536), 300, 256, 128, 0), ALIAS),   # sf overlaps out
     ((None, None, None, 0, 256, 128, 0), 0),                          # empty batch
 ])
 def test_per_block_cast_validation(lib, args, expected):
@@ -206,8 +209,8 @@ def test_per_block_cast_validation(lib, args, expected):
     ((p(), p(1 << 20), p(2 << 20), 4, 256, 1, 128, 0, 2), 4),         # out dtype
     ((p(), p((1 << 20) + 4), p(2 << 20), 4, 256, 128, 1, 0, 0), 5),   # per-channel sf / 16
     ((p(), p(1 << 20), p((2 << 20) + 8), 4, 256, 1, 128, 0, 1), 5),   # out misaligned
-    ((p(), p(1 << 20), p(512), 4, 256, 1, 128, 0, 0), 7),             # out overlaps codes
-    ((p(), p(1 << 20), p((1 << 20) - 1024), 4, 256, 1, 128, 0, 1), 7),  # out overlaps sf
+    ((p(), p(1 << 20), p(512), 4, 256, 1, 128, 0, 0), ALIAS),             # out overlaps codes
+    ((p(), p(1 << 20), p((1 << 20) - 1024), 4, 256, 1, 128, 0, 1), ALIAS),  # out overlaps sf
     ((None, None, None, 0, 256, 128, 128, 1, 1), 0),                  # empty batch
 ])
 def test_cast_back_validation(lib, args, expected):
@@ -215,13 +218,13 @@ def test_cast_back_validation(lib, args, expected):
 
 
 @pytest.mark.parametrize("clamp,count_off,expected", [
-    (0.0, 0, 9),              # bound must be > 0
-    (-1.0, 0, 9),
-    (float("inf"), 0, 9),
-    (float("nan"), 0, 9),
+    (0.0, 0, VALUE),              # bound must be > 0
+    (-1.0, 0, VALUE),
+    (float("inf"), 0, VALUE),
+    (float("nan"), 0, VALUE),
     (4.0, 4, 5),              # counter not 8-byte aligned
-    (4.0, -(4 << 20) + 64, 7),   # counter inside x
-    (4.0, -(1 << 20) + 64, 7),   # counter inside out
+    (4.0, -(4 << 20) + 64, ALIAS),   # counter inside x
+    (4.0, -(1 << 20) + 64, ALIAS),   # counter inside out
 ])
 def test_swiglu_clamp_validation(lib, clamp, count_off, expected):
     T, H = 256, 256
@@ -235,8 +238,8 @@ def test_swiglu_clamp_validation(lib, clamp, count_off, expected):
 
 def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
     assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 1.0, None, None) == 0
-    assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 0.0, None, None) == 9
-    assert "VALUE" in __import__("fp8_activation_quantization_gb300").tkq_status_string(9)
+    assert lib.tkq_swiglu_cast_clamp(None, None, None, None, 0, 256, 128, 0, 0, 0.0, None, None) == VALUE
+    assert "VALUE" in __import__("fp8_activation_quantization_gb300").tkq_status_string(VALUE)
 
 
 @pytest.mark.parametrize("args,expected", [
@@ -244,9 +247,9 @@ def test_swiglu_clamp_empty_batch_checks_the_bound(lib):
     ((p(), p(1 << 20), p(2 << 20), 4, 200, 128, 0, 0), 2),             # C % 128
     ((p(), p(1 << 20), p(2 << 20), 4, 256, 64, 0, 0), 3),              # group
     ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 7, 0), 4),             # fmt
-    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 16), 8),            # flags
+    ((p(), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 16), FLAGS),            # flags
     ((p(4), p(1 << 20), p(2 << 20), 4, 256, 128, 0, 0), 5),            # x misaligned
-    ((p(), p(2048), p(2 << 20), 4, 256, 128, 0, 0), 7),                # out inside x (4 B/elem)
+    ((p(), p(2048), p(2 << 20), 4, 256, 128, 0, 0), ALIAS),                # out inside x (4 B/elem)
     ((None, None, None, 0, 256, 128, 0, 0), 0),                        # empty batch
 ])
 def test_per_token_cast_f32_validation(lib, args, expected):
@@ -258,7 +261,7 @@ def test_per_token_cast_f32_validation(lib, args, expected):
     ((p(), None, p(1 << 24), 4, 100), 2),                  # H % 128
     ((p(4), None, p(1 << 24), 4, 128), 5),                 # x misaligned
     ((p(), p(2), p(1 << 24), 4, 128), 5),                  # w misaligned
-    ((p(), None, p(1024), 4, 128), 7),                     # y inside x (2048 bytes)
+    ((p(), None, p(1024), 4, 128), ALIAS),                     # y inside x (2048 bytes)
     ((None, None, None, 0, 128), 0),                       # empty batch
 ])
 def test_swiglu_values_validation(lib, args, expected):
@@ -270,8 +273,8 @@ def test_swiglu_values_validation(lib, args, expected):
     ((p(), p(1 << 20), None, p(1 << 24), 4, 200), 2),       # H % 128
     ((p(), p((1 << 20) + 8), None, p(1 << 24), 4, 128), 5),  # dy misaligned
     ((p(), p(1 << 20), None, p((1 << 24) + 4), 4, 128), 5),  # y misaligned
-    ((p(), p(1 << 20), None, p((1 << 20) + 512), 4, 128), 7),  # y overlaps dy (1024 bytes)
-    ((p(), p(1 << 20), p(1 << 22), p((1 << 22) - 4096 + 16), 4, 128), 7),  # w inside y
+    ((p(), p(1 << 20), None, p((1 << 20) + 512), 4, 128), ALIAS),  # y overlaps dy (1024 bytes)
+    ((p(), p(1 << 20), p(1 << 22), p((1 << 22) - 4096 + 16), 4, 128), ALIAS),  # w inside y
     ((None, None, None, None, 0, 128), 0),                  # empty batch
 ])
 def test_swiglu_backward_values_validation(lib, args, expected):
@@ -285,7 +288,7 @@ def test_swiglu_backward_values_validation(lib, args, expected):
     ((None, p(1 << 24), 16, 0), 1),           # NULL x
     ((p(8), p(1 << 24), 16, 0), 5),           # x misaligned
     ((p(), p(2), 16, 0), 5),                  # out misaligned
-    ((p(), p(32), 16, 0), 7),                 # out inside x (64 bytes)
+    ((p(), p(32), 16, 0), ALIAS),                 # out inside x (64 bytes)
     ((None, None, 0, 1), 0),                  # empty
 ])
 def test_fp8_encode_validation(lib, args, expected):
@@ -293,10 +296,10 @@ def test_fp8_encode_validation(lib, args, expected):
 
 
 @pytest.mark.parametrize("flags,sf_t_addr,expected", [
-    (16, 7 << 20, 8),                      # unknown flag bit
+    (16, 7 << 20, FLAGS),                      # unknown flag bit
     (4, (7 << 20) + 4, 5),                 # column-major sf_t must be 16-byte aligned
     (0, (7 << 20) + 4, 0),                 # empty batch: valid flags return OK, no launch
-    (6, (5 << 20) + 16, 7),                # sf_t inside sf (both sized by their layouts)
+    (6, (5 << 20) + 16, ALIAS),                # sf_t inside sf (both sized by their layouts)
 ])
 def test_swiglu_cast_t_ex_validation(lib, flags, sf_t_addr, expected):
     T, H = (0 if expected == 0 else 256), 256

@@ -5,6 +5,13 @@ oracle's quotient y / s lies at an FP8 rounding tie (clamping makes such ties
 common: see parity.assert_codes_differ_only_at_ties); the clamp count is an
 integer decided by exact comparisons of bf16 inputs with the bound, so it must
 equal the oracle's count exactly.
+
+For a bound that is itself a bf16 value the clamp of a bf16 input is again a
+bf16 value, so the clamped cast must quantize exactly the kernels' own y of the
+input clipped on the host (tkq_swiglu_values): its codes and scales then equal
+bit for bit the oracle's reading of that y (the product by the rounded
+reciprocal of the scale, which the SwiGLU kernels compute), with no exception
+at ties.
 """
 from __future__ import annotations
 
@@ -108,6 +115,67 @@ def test_clamped_swiglu_full_workload(cuda_device):
     parity.assert_scales_close("sf", sf_raw.view(np.float32).reshape(T, H // 128), e_sf)
     parity.assert_codes_differ_only_at_ties("codes", codes, e_codes,
                                             q_rows(x, None, 4.0, e_sf), "e4m3")
+
+
+def clip_on_host(x_bits, c):
+    """The clamp applied to the bf16 input itself (c a bf16 value, > 0): gates
+    to <= c, ups to [-c, c]; the results are bf16 values, returned as bits."""
+    H = x_bits.shape[1] // 2
+    v = synth.bf16_bits_to_f32(x_bits)
+    v[:, :H] = np.minimum(v[:, :H], np.float32(c))
+    v[:, H:] = np.clip(v[:, H:], np.float32(-c), np.float32(c))
+    bits = np.ascontiguousarray((v.view(np.uint32) >> 16).astype(np.uint16))
+    assert np.array_equal(synth.bf16_bits_to_f32(bits), v)   # exact: c is a bf16 value
+    return bits
+
+
+@pytest.mark.parametrize("clamp", [4.0, 0.5])
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_clamped_casts_quantize_the_clipped_values(cuda_device, swiglu_kernel, clamp, weighted,
+                                                   fmt):
+    """With a bf16 bound, the clamped row cast and the clamped transposed cast
+    quantize exactly the kernels' y of the host-clipped input: codes and
+    scales, rows and columns, bit for bit against the oracle's reading of that
+    y; the count is the number of values the clip changed."""
+    T, H = 1024, 384
+    x = synth.swiglu_bf16(81, 82, T, H, gate_std=2.0)
+    w = synth.routing_weights(83, 84, T // 8) if weighted else None
+    xc = clip_on_host(x, clamp)
+    wd = None if w is None else torch.from_numpy(np.ascontiguousarray(w)).to(cuda_device)
+    y = tkq.swiglu_values(to_dev_bf16(xc, cuda_device), wd).cpu().numpy()
+    e_q, e_s = oracle.cast_rows_f32_ex(y, fmt, 128, oracle.Q_RECIPROCAL)
+    changed = int(np.count_nonzero(xc != x))
+    codes, sf_raw, n = run_clamp(x, w, fmt, clamp, cuda_device)
+    assert n == changed > 0
+    parity.assert_bit_exact("codes", codes, e_q)
+    parity.assert_bit_exact("scales", sf_raw.view(np.float32).reshape(T, H // 128), e_s)
+    o, s, ot, st, n_t = run_clamp(x, w, fmt, clamp, cuda_device, transposed=True)
+    e_qt, e_st = oracle.cast_rows_f32_ex(np.ascontiguousarray(y.T), fmt, 128, oracle.Q_RECIPROCAL)
+    assert n_t == changed
+    parity.assert_bit_exact("rows", o, e_q)
+    parity.assert_bit_exact("row scales", s, e_s)
+    parity.assert_bit_exact("column codes", ot, e_qt)
+    parity.assert_bit_exact("column scales", st, e_st)
+
+
+def test_clamped_full_workload_quantizes_the_clipped_values(cuda_device):
+    """The swiglu workload with c = 4 (about 2.3 % of the gates clipped) through
+    the clamped transposed cast: rows and columns bit for bit against the
+    oracle's reading of the kernels' y of the host-clipped input."""
+    x = synth.workload("swiglu")["x"]
+    xc = clip_on_host(x, 4.0)
+    y = tkq.swiglu_values(to_dev_bf16(xc, cuda_device)).cpu().numpy()
+    o, s, ot, st, n = run_clamp(x, None, "e4m3", 4.0, cuda_device, transposed=True)
+    assert n == int(np.count_nonzero(xc != x))
+    e_q, e_s = oracle.cast_rows_f32_ex(y, "e4m3", 128, oracle.Q_RECIPROCAL, threads=THREADS)
+    parity.assert_bit_exact("rows", o, e_q)
+    parity.assert_bit_exact("row scales", s, e_s)
+    del e_q, e_s
+    e_qt, e_st = oracle.cast_rows_f32_ex(np.ascontiguousarray(y.T), "e4m3", 128,
+                                         oracle.Q_RECIPROCAL, threads=THREADS)
+    parity.assert_bit_exact("column codes", ot, e_qt)
+    parity.assert_bit_exact("column scales", st, e_st)
 
 
 @pytest.mark.parametrize("clamp", [2.0, 1.3])

@@ -649,7 +649,7 @@ def test_argument_errors_launch_nothing(cuda_device):
         (tkq.tkq_per_token_cast(ctypes.c_void_p(x.data_ptr() + 2), out.ptr, sf.ptr, 256, 4096,
                                 128, 0, s), 5),
         (tkq.tkq_per_token_cast(xp, ctypes.c_void_p(x.data_ptr() + 1024), sf.ptr, 256, 4096,
-                                128, 0, s), 7),
+                                128, 0, s), 8),   # TKQ_ERR_ALIAS
         (tkq.tkq_swiglu_cast_t(xp, None, out.ptr, sf.ptr, out.ptr, sf.ptr, 100, 2048, 128, 0, s), 2),
     ]
     for got, exp in cases:
@@ -668,7 +668,13 @@ def test_bounded_wait_times_out_and_context_survives(cuda_device):
     working (a cast afterwards is still correct)."""
     tkq.tkq_read_device_status(clear=True)
     assert tkq.tkq_selftest_wait_timeout(2_000_000, stream_of(cuda_device)) == 0
-    assert tkq.tkq_read_device_status(clear=True) & tkq.DEVICE_TIMEOUT
+    assert tkq.tkq_read_device_status() & tkq.DEVICE_TIMEOUT
+    # the C call reports it as TKQ_ERR_TIMEOUT (7), with the word in *flags
+    import ctypes
+    word = ctypes.c_uint32(0)
+    assert tkq.load_library().tkq_read_device_status(ctypes.byref(word), 1) == tkq.ERR_TIMEOUT
+    assert word.value & tkq.DEVICE_TIMEOUT
+    assert tkq.load_library().tkq_read_device_status(ctypes.byref(word), 0) == 0
     assert tkq.tkq_read_device_status() == 0
     x = synth.workload("swiglu", rows=256)["x"]
     out, sf, out_t, sf_t = run_swiglu(x, None, "e4m3", cuda_device, transposed=True)
