@@ -10,9 +10,10 @@
 //
 // An HBM-bound stream (1 byte in, 4 or 2 bytes out per element): persistent
 // CTAs of 256 threads walk units of 4096 consecutive codes (rows wrap inside
-// a unit); each thread turns 16 codes (one 16-byte load) into 16 outputs in a
-// shared buffer, and the unit's 8 or 16 KB of output leave as one bulk-async
-// store (cp.async.bulk global <- shared), double-buffered per CTA.  Written from the
+// a unit); each thread turns 16 codes (two 8-code or four 4-code pieces, see
+// PieceShape) into 16 outputs in a shared buffer, and the unit's 8 or 16 KB
+// of output leave as one bulk-async store (cp.async.bulk global <- shared),
+// double-buffered per CTA.  Written from the
 // threads with 16-byte stores, this 1:2 read:write mix ran at 5.7 TB/s; the
 // bulk stores and the occupancy of a lean kernel move it faster.
 #include <cuda_runtime.h>
@@ -70,22 +71,50 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
 // outputs are contiguous, so they leave as one bulk store.
 constexpr int kChunk = kThreads * 16;
 
-// Per unit: each thread loads its 16 codes (one 16-byte load) and their scale,
-// waits until the shared buffer it writes (one of two) has been read by the
-// bulk store issued from it two units earlier, decodes and scales eight
-// values at a time into the buffer, and thread 0 issues the unit's bulk store.
-// Many CTAs per SM (few registers) keep loads and stores in flight; the bulk
-// stores write the output in 8 or 16 KB runs, which moves this 1:2
-// read:write mix faster than 16-byte stores from the threads.  GR_SHIFT:
-// log2 of the scale group's rows (0 or 7).
+// A thread's 16 codes of a unit are kPieces pieces of kPiece consecutive
+// codes, piece p at unit offset p * kPieceStride + kPiece * thread: each piece
+// makes 16 output bytes, which land next to the neighbouring thread's piece
+// in the shared buffer, so every 16-byte store of a warp covers 512
+// consecutive bytes (no bank conflicts; one 16-code run per thread would put
+// a thread's two or four 16-byte stores 32 or 64 bytes apart, two-way
+// conflicts).  A unit's length is a multiple of 128 codes (C is), so a piece
+// is wholly in or out of it, and never crosses a 128-column scale group.
+template <bool BF16>
+struct PieceShape {
+    static constexpr int kPiece = BF16 ? 8 : 4;          // codes per piece
+    static constexpr int kPieces = 16 / kPiece;           // pieces per thread
+    static constexpr int kStride = kThreads * kPiece;     // unit offset between pieces
+};
+
+__device__ __forceinline__ uint2 ld_stream_u2(const uint8_t* p) {
+    uint2 r = make_uint2(0, 0);
+    if (!access_ok(p, 8, false)) return r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_stream_u1(const uint8_t* p) {
+    uint32_t r = 0;
+    if (!access_ok(p, 4, false)) return r;
+    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
+// Per unit: each thread loads its pieces' codes and scales, waits until the
+// shared buffer it writes (one of two) has been read by the bulk store issued
+// from it two units earlier, decodes and scales the pieces into the buffer,
+// and thread 0 issues the unit's bulk store.  Many CTAs per SM (few
+// registers) keep loads and stores in flight; the bulk stores write the
+// output in 8 or 16 KB runs, which moves this 1:2 read:write mix faster than
+// 16-byte stores from the threads.  GR_SHIFT: log2 of the scale group's rows
+// (0 or 7).
 template <int FMT, int GC, int GR_SHIFT, bool BF16>
 __global__ void __launch_bounds__(kThreads, BF16 ? 8 : 6)
     cast_back_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ sf,
                      uint8_t* __restrict__ out, int64_t T, int64_t C) {
     grid_dependency_sync();  // the previous grid on the stream is done
+    using PS = PieceShape<BF16>;
     constexpr int kOutBytes = BF16 ? 2 : 4;
-    constexpr int kVecs = kOutBytes;   // 16-byte output vectors per thread and unit
-    __shared__ __align__(128) uint4 buf[2][kThreads * kVecs];
+    __shared__ __align__(128) uint4 buf[2][kThreads * PS::kPieces];
     const int64_t total = T * C;
     const int64_t n_units = (total + kChunk - 1) / kChunk;
     const int64_t G = C / GC;                        // scales per row of sf
@@ -100,65 +129,80 @@ __global__ void __launch_bounds__(kThreads, BF16 ? 8 : 6)
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, b ^= 1) {
         const int64_t f0 = u * kChunk;
         const int len = static_cast<int>(total - f0 < kChunk ? total - f0 : kChunk);
-        const bool active = 16 * static_cast<int>(threadIdx.x) < len;
-        // this thread's vector: row t, column c (rows wrap inside a unit)
-        int64_t t = t0;
-        uint32_t c = static_cast<uint32_t>(c0) + 16u * threadIdx.x;
-        if (C >= kChunk) {
-            if (c >= Cu) {
-                c -= Cu;
-                ++t;
+        uint32_t q[PS::kPieces][PS::kPiece / 4];
+        float sc[PS::kPieces][PS::kPiece];
+        bool live[PS::kPieces];
+#pragma unroll
+        for (int p = 0; p < PS::kPieces; ++p) {
+            const int off = p * PS::kStride + PS::kPiece * static_cast<int>(threadIdx.x);
+            live[p] = off < len;
+            // this piece's row t and column c (rows wrap inside a unit)
+            int64_t t = t0;
+            uint32_t c = static_cast<uint32_t>(c0) + static_cast<uint32_t>(off);
+            if (C >= kChunk) {
+                if (c >= Cu) {
+                    c -= Cu;
+                    ++t;
+                }
+            } else {
+                const uint32_t wrap = c / Cu;
+                t += wrap;
+                c -= wrap * Cu;
             }
-        } else {
-            const uint32_t wrap = c / Cu;
-            t += wrap;
-            c -= wrap * Cu;
-        }
-        const float* srow = sf + (t >> GR_SHIFT) * G;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        float s1 = 0.0f;
-        if (active) {
-            q = ld_stream(reinterpret_cast<const uint4*>(codes + f0) + threadIdx.x);
-            if constexpr (GC != 1) s1 = ld_ro(srow + c / GC);
+            const float* srow = sf + (t >> GR_SHIFT) * G;
+#pragma unroll
+            for (int k = 0; k < PS::kPiece / 4; ++k) q[p][k] = 0;
+#pragma unroll
+            for (int k = 0; k < PS::kPiece; ++k) sc[p][k] = 0.0f;
+            if (live[p]) {
+                if constexpr (BF16) {
+                    const uint2 v = ld_stream_u2(codes + f0 + off);
+                    q[p][0] = v.x;
+                    q[p][1] = v.y;
+                } else {
+                    q[p][0] = ld_stream_u1(codes + f0 + off);
+                }
+                if constexpr (GC == 1) {
+#pragma unroll
+                    for (int k = 0; k < PS::kPiece; k += 4) {
+                        const float4 a = ld_ro(reinterpret_cast<const float4*>(srow + c + k));
+                        sc[p][k] = a.x;
+                        sc[p][k + 1] = a.y;
+                        sc[p][k + 2] = a.z;
+                        sc[p][k + 3] = a.w;
+                    }
+                } else {
+                    const float s1 = ld_ro(srow + c / GC);
+#pragma unroll
+                    for (int k = 0; k < PS::kPiece; ++k) sc[p][k] = s1;
+                }
+            }
         }
         if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         __syncthreads();   // buffer b is free
-        if (active) {
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float y[8], sc[8];
-                f16x2_to_f32(fp8x2_to_f16x2<FMT>(w[2 * h]), y[0], y[1]);
-                f16x2_to_f32(fp8x2_to_f16x2<FMT>(w[2 * h] >> 16), y[2], y[3]);
-                f16x2_to_f32(fp8x2_to_f16x2<FMT>(w[2 * h + 1]), y[4], y[5]);
-                f16x2_to_f32(fp8x2_to_f16x2<FMT>(w[2 * h + 1] >> 16), y[6], y[7]);
-                if constexpr (GC == 1) {
-                    const float4* s4 = reinterpret_cast<const float4*>(srow + c + 8 * h);
-                    const float4 a = ld_ro(s4), e = ld_ro(s4 + 1);
-                    sc[0] = a.x; sc[1] = a.y; sc[2] = a.z; sc[3] = a.w;
-                    sc[4] = e.x; sc[5] = e.y; sc[6] = e.z; sc[7] = e.w;
-                } else {
+        for (int p = 0; p < PS::kPieces; ++p) {
+            if (!live[p]) continue;
+            float y[PS::kPiece];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) sc[i] = s1;
-                }
-#pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const float2 p =
-                        mul2(make_float2(y[i], y[i + 1]), make_float2(sc[i], sc[i + 1]));
-                    y[i] = p.x;
-                    y[i + 1] = p.y;
-                }
-                uint4* dst = &buf[b][threadIdx.x * kVecs];
-                if constexpr (BF16) {
-                    dst[h] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                        pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-                } else {
-                    dst[2 * h] = make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]),
-                                            __float_as_uint(y[2]), __float_as_uint(y[3]));
-                    dst[2 * h + 1] = make_uint4(__float_as_uint(y[4]), __float_as_uint(y[5]),
-                                                __float_as_uint(y[6]), __float_as_uint(y[7]));
-                }
+            for (int k = 0; k < PS::kPiece / 4; ++k) {
+                f16x2_to_f32(fp8x2_to_f16x2<FMT>(q[p][k]), y[4 * k], y[4 * k + 1]);
+                f16x2_to_f32(fp8x2_to_f16x2<FMT>(q[p][k] >> 16), y[4 * k + 2], y[4 * k + 3]);
             }
+#pragma unroll
+            for (int i = 0; i < PS::kPiece; i += 2) {
+                const float2 r = mul2(make_float2(y[i], y[i + 1]),
+                                      make_float2(sc[p][i], sc[p][i + 1]));
+                y[i] = r.x;
+                y[i + 1] = r.y;
+            }
+            uint4& dst = buf[b][p * kThreads + threadIdx.x];
+            if constexpr (BF16)
+                dst = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+            else
+                dst = make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]),
+                                 __float_as_uint(y[2]), __float_as_uint(y[3]));
         }
         // the buffer's generic-proxy writes before the bulk copy reads it
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

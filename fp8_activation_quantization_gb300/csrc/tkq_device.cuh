@@ -108,15 +108,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     return r;
 }
 
-// Asks L2 to fetch `bytes` (a multiple of 16) from global memory at p (16-byte
-// aligned) ahead of the loads that will read them: one bulk prefetch, which
-// holds no registers and which nothing waits on.  The range must lie inside
-// an input buffer of the call (checked like a load in the checked build).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    if (!access_ok(p, bytes, false)) return;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Read-only loads through the non-coherent path (small per-row operands).
 __device__ __forceinline__ float ld_ro(const float* p) {
     return access_ok(p, 4, false) ? __ldg(p) : 0.0f;
