@@ -100,3 +100,35 @@ def test_both_arms_describe_the_same_config():
     assert "larger than L2" in bench.workload_config("swiglu_t", "e4m3", 1)["l2"]
     assert "rotation of buffer sets" in bench.workload_config("plain_outlier", "e4m3", 1)["l2"]
     assert "dp2" in bench.workload_config("swiglu_t", "e4m3", 2)["parallelism"]
+
+
+class _Sized:
+    def __init__(self, nbytes):
+        self.bytes = nbytes
+
+
+@pytest.mark.parametrize("nbytes,l2,expected", [
+    (12_713_984, 129 << 20, 43),      # plain_small: 43 sets span >= 4 x L2
+    (177_995_776, 129 << 20, 4),      # plain_outlier
+    (675_545_088, 129 << 20, 2),      # larger than 4 x L2: still two sets
+    (1, 129 << 20, 4 * (129 << 20)),  # degenerate tiny launch
+])
+def test_rotation_spans_four_times_l2(nbytes, l2, expected):
+    k = bench.rotation_sets(_Sized(nbytes), l2)
+    assert k == expected
+    assert k >= 2 and k * nbytes >= 4 * l2
+    assert (k - 1) * nbytes < 4 * l2 or k == 2
+
+
+def test_bar_table_judges_the_sustained_rate():
+    peak = 6759.6
+    pw = {"plain_outlier/e4m3": {"sustained": {"GB/s": 6159.0}},
+          "swiglu_t/e4m3": {"sustained": {"GB/s": 6964.0}},
+          "swiglu/e4m3": {"sustained": {"GB/s": 5000.0}},
+          "cast_back/e4m3": {"sustained": {"GB/s": 1.0}}}       # not a bar workload
+    t = bench.bar_table(pw, peak)
+    assert set(t) == {"plain_outlier/e4m3", "swiglu_t/e4m3", "swiglu/e4m3"}
+    assert t["plain_outlier/e4m3"]["pass_measured"] and not t["plain_outlier/e4m3"]["pass_nominal"]
+    assert t["swiglu_t/e4m3"]["pass_measured"] and t["swiglu_t/e4m3"]["pass_nominal"]
+    assert not t["swiglu/e4m3"]["pass_measured"]   # 5000 < 0.8 x 6759.6
+    assert t["swiglu_t/e4m3"]["frac_of_nominal"] == round(6964.0 / bench.NOMINAL_HBM_GBS, 4)
