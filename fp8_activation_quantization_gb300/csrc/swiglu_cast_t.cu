@@ -66,17 +66,14 @@ struct alignas(1024) SharedStorage {
     int abort;
 };
 
-// Scale layouts of an instance: none (fp32 row-major, as documented for
-// tkq_swiglu_cast_t), the layouts a TMA-fed FP8 GEMM reads fixed at compile
-// time (UE8M0 packed column-major, fp32 column-major), or any TKQ_SF_*
-// combination read from the launch's flags at run time.  The fixed instances
-// exist because the run-time one is measurably slower in this latency-bound
-// body (244.7 against 232.0 us for UE8M0 column-major on the swiglu_t
-// workload, back to back; the flag-free instance takes 233.4 us).
-constexpr unsigned kSfcNone = 0u;
-constexpr unsigned kSfcUe8m0ColMajor = kSfRoundPow2 | kSfPacked | kSfColMajor;
-constexpr unsigned kSfcF32ColMajor = kSfColMajor;
-constexpr unsigned kSfcRuntime = ~0u;
+// Scale layouts of an instance (kSfc* of tkq_device.cuh): none (fp32
+// row-major, as documented for tkq_swiglu_cast_t), the layouts a TMA-fed FP8
+// GEMM reads fixed at compile time (UE8M0 packed column-major, fp32
+// column-major), or any TKQ_SF_* combination read from the launch's flags at
+// run time.  The fixed instances exist because the run-time one is measurably
+// slower in this latency-bound body (244.7 against 232.0 us for UE8M0
+// column-major on the swiglu_t workload, back to back; the flag-free instance
+// takes 233.4 us).
 
 // The clamp of an instance: none, on packed bf16 pairs (the bound is a bf16
 // value), or in fp32.  Fixed at compile time for the same reason as the
@@ -425,9 +422,8 @@ cudaError_t launch_w(const void* x, const float* w, void* out, float* sf, void* 
                      unsigned long long* clamp_count, cudaStream_t stream) {
     const SfLayout lr = layout_of(sf_flags, T, H / 128), lc = layout_of(sf_flags, H, T / 128);
     // the reciprocal-reading bit changes nothing here (the SwiGLU casts always
-    // multiply by the reciprocal), and packed scales are powers of two
-    unsigned f = sf_flags & (kSfRoundPow2 | kSfPacked | kSfColMajor);
-    if (f & kSfPacked) f |= kSfRoundPow2;
+    // multiply by the reciprocal)
+    const unsigned f = sfc_of(sf_flags, false);
     if (f == kSfcNone)
         return launch_sfc<FMT, CLAMP, kSfcNone>(x, w, out, sf, out_t, sf_t, T, H, lr, lc, clamp,
                                                 clamp_count, stream);

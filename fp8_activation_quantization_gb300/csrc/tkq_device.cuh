@@ -215,6 +215,31 @@ struct SfLayout {
 };
 constexpr unsigned kSfRoundPow2 = 1u, kSfPacked = 2u, kSfColMajor = 4u, kQReciprocal = 8u;
 
+// Option sets a kernel instance may fix at compile time (its SFC template
+// argument): none, the two scale layouts a TMA-fed FP8 GEMM reads (UE8M0
+// packed column-major, fp32 column-major), the reciprocal reading alone, or
+// kSfcRuntime for flags read from the launch.  A flag test that is a run-time
+// branch inside a kernel's loop measurably slows the latency-bound ones.
+constexpr unsigned kSfcNone = 0u;
+constexpr unsigned kSfcUe8m0ColMajor = kSfRoundPow2 | kSfPacked | kSfColMajor;
+constexpr unsigned kSfcF32ColMajor = kSfColMajor;
+constexpr unsigned kSfcReciprocal = kQReciprocal;
+constexpr unsigned kSfcRuntime = ~0u;
+
+// The instance for sf_flags: packed scales are powers of two, and with
+// power-of-two scales the reciprocal reading is the quotient; `recip` says
+// whether the kernel distinguishes the reciprocal reading at all.
+__host__ __device__ inline unsigned sfc_of(unsigned sf_flags, bool recip) {
+    unsigned f = sf_flags & (kSfRoundPow2 | kSfPacked | kSfColMajor | kQReciprocal);
+    if (!recip) f &= ~kQReciprocal;
+    if (f & kSfPacked) f |= kSfRoundPow2;
+    if (f & kSfRoundPow2) f &= ~kQReciprocal;
+    if (f == kSfcNone || f == kSfcUe8m0ColMajor || f == kSfcF32ColMajor ||
+        f == kSfcReciprocal)
+        return f;
+    return kSfcRuntime;
+}
+
 // The scale rounded up to a power of two, s = 2^ceil(log2 s) (the mantissa
 // bits dropped and the exponent raised when any were set), and its reciprocal,
 // exact: 2^-k has the biased exponent 254 minus that of 2^k.
