@@ -41,16 +41,23 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRows = 32;                 // rows per chunk (4 per consumer warp)
 constexpr int kBoxBytes = kRows * 256;    // one 32 x 128 bf16 box
 
+// The clamp modes come in two kinds fixed at compile time: the bound is a bf16
+// value (the clamp runs on the packed bf16 inputs) or not (fp32 clamp); a
+// choice made inside the loop costs the latency-bound kernels measurably.
 enum Mode {
-    kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kBackward, kBackwardWeighted
+    kSwiglu, kSwigluWeighted, kSwigluClamp, kSwigluWeightedClamp, kSwigluClampF32,
+    kSwigluWeightedClampF32, kBackward, kBackwardWeighted
 };
 
 template <int MODE>
 struct ModeTraits {
     static constexpr bool kBwd = MODE == kBackward || MODE == kBackwardWeighted;
-    static constexpr bool kClamp = MODE == kSwigluClamp || MODE == kSwigluWeightedClamp;
-    static constexpr bool kWeighted =
-        MODE == kSwigluWeighted || MODE == kSwigluWeightedClamp || MODE == kBackwardWeighted;
+    static constexpr bool kClampBf16 = MODE == kSwigluClamp || MODE == kSwigluWeightedClamp;
+    static constexpr bool kClamp =
+        kClampBf16 || MODE == kSwigluClampF32 || MODE == kSwigluWeightedClampF32;
+    static constexpr bool kWeighted = MODE == kSwigluWeighted || MODE == kSwigluWeightedClamp ||
+                                      MODE == kSwigluWeightedClampF32 ||
+                                      MODE == kBackwardWeighted;
     static constexpr int kOperands = kBwd ? 3 : 2;  // boxes per chunk
     static constexpr int kRowBytes = 256;            // one box row in shared memory
     static constexpr int kStageBytes = kOperands * kRows * kRowBytes;
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 uint4 uq[2] = {*reinterpret_cast<const uint4*>(p + kBoxBytes),
                                *reinterpret_cast<const uint4*>(p + kBoxBytes + 128)};
                 uint32_t n = 0;
-                if (clamp.c2) {
+                if constexpr (MT::kClampBf16) {
                     // c is a bf16 value: clamp and count on the packed pairs
                     const uint32_t c2 = clamp.c2;
                     __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);  // at most 16 a half
@@ -353,9 +360,15 @@ cudaError_t launch_swiglu_cast(const void* x, const float* w, void* out, void* s
                                        stream);
     if (clamp) {
         const Clamp c{*clamp, clamp_count, bf16x2_bound(*clamp)};
-        return w ? launch_fmt<kSwigluWeightedClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags,
-                                                    stream, c)
-                 : launch_fmt<kSwigluClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream, c);
+        if (c.c2)
+            return w ? launch_fmt<kSwigluWeightedClamp>(fmt, x, nullptr, w, out, sf, T, H,
+                                                        sf_flags, stream, c)
+                     : launch_fmt<kSwigluClamp>(fmt, x, nullptr, w, out, sf, T, H, sf_flags,
+                                                stream, c);
+        return w ? launch_fmt<kSwigluWeightedClampF32>(fmt, x, nullptr, w, out, sf, T, H,
+                                                       sf_flags, stream, c)
+                 : launch_fmt<kSwigluClampF32>(fmt, x, nullptr, w, out, sf, T, H, sf_flags,
+                                               stream, c);
     }
     return w ? launch_fmt<kSwigluWeighted>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream)
              : launch_fmt<kSwiglu>(fmt, x, nullptr, w, out, sf, T, H, sf_flags, stream);
