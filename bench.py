@@ -804,7 +804,7 @@ def time_rotation(sets, steps: int, warmup: int, stream, barrier, graph: bool = 
     return start.elapsed_time(end) / 1000.0
 
 
-# the benchmark spec bar: the plain and fused casts at T >= 8192, judged on the
+# the 80 % bar of the plain and fused casts at T >= 8192, judged on the
 # sustained (write-back inclusive) rate
 BAR_WORKLOADS = ["plain_outlier/e4m3", "plain_outlier/e5m2", "swiglu/e4m3",
                  "swiglu_moe/e4m3", "swiglu_t/e4m3"]
