@@ -286,17 +286,23 @@ def tkq_swiglu_backward_cast_ex(x, dy, w, out, sf, T, H, group=GROUP, fmt=FMT_E4
                                                       sf_flags, stream)
 
 
+def _sf_shape(T: int, groups_per_row: int, sf_flags: int):
+    """Shape and element type of the scales in the layout `sf_flags` selects:
+    fp32 [T, G], fp32 [G, T4], int32 [T, W] or int32 [W, T4] (T4 = T rounded
+    up to 4, W = G / 4 rounded up)."""
+    T4 = (T + 3) // 4 * 4
+    W = (groups_per_row + 3) // 4
+    if sf_flags & SF_UE8M0_PACKED:
+        return ((W, T4) if sf_flags & SF_COL_MAJOR else (T, W)), "int32"
+    return ((groups_per_row, T4) if sf_flags & SF_COL_MAJOR else (T, groups_per_row)), "float32"
+
+
 def sf_tensor(T: int, groups_per_row: int, sf_flags: int, device):
     """An empty scale tensor shaped for the layout `sf_flags` selects:
     fp32 [T, G], fp32 [G, T4], int32 [T, W] or int32 [W, T4]."""
     import torch
-    T4 = (T + 3) // 4 * 4
-    W = (groups_per_row + 3) // 4
-    if sf_flags & SF_UE8M0_PACKED:
-        shape = (W, T4) if sf_flags & SF_COL_MAJOR else (T, W)
-        return torch.empty(shape, dtype=torch.int32, device=device)
-    shape = (groups_per_row, T4) if sf_flags & SF_COL_MAJOR else (T, groups_per_row)
-    return torch.empty(shape, dtype=torch.float32, device=device)
+    shape, dt = _sf_shape(T, groups_per_row, sf_flags)
+    return torch.empty(shape, dtype=getattr(torch, dt), device=device)
 
 
 # ---------------------------------------------------------------------------
@@ -324,6 +330,29 @@ def _check_input(x, name="x", allow_f32=False):
     if x.dtype not in ok or x.dim() != 2 or not x.is_contiguous():
         raise TypeError(f"{name} must be a contiguous 2-D "
                         + ("bfloat16 or float32" if allow_f32 else "bfloat16") + " tensor")
+
+
+def _check_out(t, name, x, nbytes, itemsize=None, dtype=None):
+    """A caller-supplied output buffer: a contiguous CUDA tensor on x's device
+    of at least `nbytes` bytes (the kernels write exactly the bytes the call's
+    shape and layout give, so a smaller buffer would be written past its end).
+    `itemsize` / `dtype` pin the element size or type where the layout fixes
+    them; scale buffers of any element type are accepted by size."""
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device != x.device or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA tensor on x's device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise TypeError(f"{name} must have {itemsize}-byte elements")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes; "
+                         f"the call writes {nbytes}")
+
+
+def _check_sf_out(t, name, x, rows, groups_per_row, sf_flags):
+    shape, _ = _sf_shape(rows, groups_per_row, sf_flags)
+    _check_out(t, name, x, 4 * shape[0] * shape[1])
 
 
 def _stream_handle(dev):
@@ -382,10 +411,15 @@ def per_token_cast(x, fmt="e4m3", num_per_channels: int = GROUP, out=None, out_s
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
     if use_sf_inv:
         flags |= Q_RECIPROCAL
+    G = C // max(num_per_channels, 1)
     if out is None:
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
+    else:
+        _check_out(out, "out", x, T * C, itemsize=1)
     if out_sf is None:
-        out_sf = sf_tensor(T, max(C // max(num_per_channels, 1), 0), flags, x.device)
+        out_sf = sf_tensor(T, G, flags, x.device)
+    else:
+        _check_sf_out(out_sf, "out_sf", x, T, G, flags)
     with _device_ctx(x.device):
         call = tkq_per_token_cast_f32 if x.dtype == torch.float32 else tkq_per_token_cast_ex
         st = call(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f, flags,
@@ -434,8 +468,12 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
     if out is None:
         out = torch.empty((T, H), dtype=_fp8_dtype(f), device=x.device)
+    else:
+        _check_out(out, "out", x, T * H, itemsize=1)
     if out_sf is None:
         out_sf = sf_tensor(T, H // g, flags, x.device)
+    else:
+        _check_sf_out(out_sf, "out_sf", x, T, H // g, flags)
     with _device_ctx(x.device):
         stream = _stream_handle(x.device)
         if not with_transpose:
@@ -451,8 +489,12 @@ def swiglu_forward_and_per_token_cast(x, fmt="e4m3", num_per_channels: int = GRO
             return out, out_sf
         if out_t is None:
             out_t = torch.empty((H, T), dtype=_fp8_dtype(f), device=x.device)
+        else:
+            _check_out(out_t, "out_t", x, H * T, itemsize=1)
         if out_sf_t is None:
             out_sf_t = sf_tensor(H, T // g, flags, x.device)
+        else:
+            _check_sf_out(out_sf_t, "out_sf_t", x, H, T // g, flags)
         if clamp is None:
             st = tkq_swiglu_cast_t_ex(_ptr(x), _ptr(topk_weights), _ptr(out), _ptr(out_sf),
                                       _ptr(out_t), _ptr(out_sf_t), T, H, num_per_channels, f,
@@ -487,8 +529,12 @@ def swiglu_backward_and_per_token_cast(x, dy, fmt="e4m3", num_per_channels: int 
     flags = _sf_flags(round_sf, use_packed_ue8m0, use_tma_aligned_col_major_sf)
     if out is None:
         out = torch.empty((T, 2 * H), dtype=_fp8_dtype(f), device=x.device)
+    else:
+        _check_out(out, "out", x, T * 2 * H, itemsize=1)
     if out_sf is None:
         out_sf = sf_tensor(T, 2 * H // g, flags, x.device)
+    else:
+        _check_sf_out(out_sf, "out_sf", x, T, 2 * H // g, flags)
     with _device_ctx(x.device):
         st = tkq_swiglu_backward_cast_ex(_ptr(x), _ptr(dy), _ptr(topk_weights), _ptr(out),
                                          _ptr(out_sf), T, H, num_per_channels, f, flags,
@@ -510,9 +556,13 @@ def per_channel_cast(x, fmt="e4m3", num_per_channels: int = GROUP, transpose: bo
     g = max(num_per_channels, 1)
     if out is None:
         out = torch.empty((C, T) if transpose else (T, C), dtype=_fp8_dtype(f), device=x.device)
+    else:
+        _check_out(out, "out", x, T * C, itemsize=1)
     if out_sf is None:
         out_sf = torch.empty((C, T // g) if transpose else (T // g, C), dtype=torch.float32,
                              device=x.device)
+    else:
+        _check_out(out_sf, "out_sf", x, 4 * C * (T // g))
     with _device_ctx(x.device):
         st = tkq_per_channel_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, num_per_channels, f,
                                   int(transpose), _stream_handle(x.device))
@@ -531,8 +581,12 @@ def per_block_cast(x, fmt="e4m3", block_size: int = GROUP, out=None, out_sf=None
     b = max(block_size, 1)
     if out is None:
         out = torch.empty((T, C), dtype=_fp8_dtype(f), device=x.device)
+    else:
+        _check_out(out, "out", x, T * C, itemsize=1)
     if out_sf is None:
         out_sf = torch.empty(((T + b - 1) // b, C // b), dtype=torch.float32, device=x.device)
+    else:
+        _check_out(out_sf, "out_sf", x, 4 * ((T + b - 1) // b) * (C // b))
     with _device_ctx(x.device):
         st = tkq_per_block_cast(_ptr(x), _ptr(out), _ptr(out_sf), T, C, block_size, f,
                                 _stream_handle(x.device))
@@ -571,6 +625,9 @@ def cast_back(x, sf, fmt=None, group_size=(1, GROUP), out_dtype=None, out=None):
         raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
     if out is None:
         out = torch.empty((T, C), dtype=out_dtype, device=x.device)
+    else:
+        _check_out(out, "out", x, T * C * (4 if out_dtype == torch.float32 else 2),
+                   dtype=out_dtype)
     code = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
     with _device_ctx(x.device):
         st = tkq_cast_back(_ptr(x), _ptr(sf), _ptr(out), T, C, gr, gc, f, code,
