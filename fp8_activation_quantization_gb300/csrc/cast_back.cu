@@ -110,13 +110,22 @@ __device__ __forceinline__ uint32_t ld_stream_u1(const uint8_t* p) {
 template <int FMT, int GC, int GR_SHIFT, bool BF16>
 __global__ void __launch_bounds__(kThreads, BF16 ? 8 : 6)
     cast_back_kernel(const uint8_t* __restrict__ codes, const float* __restrict__ sf,
-                     uint8_t* __restrict__ out, int64_t T, int64_t C) {
-    grid_dependency_sync();  // the previous grid on the stream is done
+                     uint8_t* __restrict__ out, int64_t T, int64_t C, int prefetch_units) {
     using PS = PieceShape<BF16>;
     constexpr int kOutBytes = BF16 ? 2 : 4;
     __shared__ __align__(128) uint4 buf[2][kThreads * PS::kPieces];
     const int64_t total = T * C;
     const int64_t n_units = (total + kChunk - 1) / kChunk;
+    grid_dependency_launch();
+    // the codes of the CTA's first prefetch_units units go to L2 while the
+    // grid before this one drains; then wait until it is done
+    if (threadIdx.x == 0) {
+        for (int p = 0; p < prefetch_units; ++p) {
+            const int64_t u = blockIdx.x + static_cast<int64_t>(p) * gridDim.x;
+            if ((u + 1) * kChunk <= total) prefetch_l2(codes + u * kChunk, kChunk);
+        }
+    }
+    grid_dependency_wait();
     const int64_t G = C / GC;                        // scales per row of sf
     // (row, column) of this CTA's unit starts u * kChunk, u = blockIdx.x +
     // k * gridDim.x, advanced by constants instead of divided out per unit
@@ -228,7 +237,7 @@ cudaError_t launch(const void* codes, const float* sf, void* out, int64_t T, int
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0, n_units);
     if (const cudaError_t e = upload_checks(stream)) return e;
     return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint8_t*>(codes), sf,
-                      static_cast<uint8_t*>(out), T, C);
+                      static_cast<uint8_t*>(out), T, C, prologue_prefetch_units(T * C));
 }
 
 template <int FMT, bool BF16>

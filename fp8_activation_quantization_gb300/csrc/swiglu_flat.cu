@@ -105,8 +105,8 @@ template <int FMT, bool WEIGHTED, int CLAMP, bool SFX>
 __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
     swiglu_flat_kernel(const uint4* __restrict__ x, const float* __restrict__ w,
                        uint4* __restrict__ out, float* __restrict__ sf, SfLayout lay, int64_t H,
-                       int64_t n_groups, int64_t n_walk, FlatClamp clamp) {
-    grid_dependency_sync();  // the previous grid on the stream is done
+                       int64_t n_groups, int64_t n_walk, FlatClamp clamp, int prefetch_units) {
+    grid_dependency_launch();
     const int lane = threadIdx.x & 31;
     const int sub = lane >> 3;   // group within the unit
     const int k = lane & 7;      // lane within the group
@@ -115,6 +115,20 @@ __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
     const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
 
     Walk cur(static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5), sub, step, GH);
+    {
+        // the gate and up runs of the warp's first prefetch_units units go to
+        // L2 while the grid before this one drains; then wait until it is done
+        Walk pre = cur;
+        for (int p = 0; p < prefetch_units; ++p) {
+            if (k == 0 && pre.u < units && pre.g < n_groups) {
+                const uint4* pg = x + pre.t * (H / 4) + pre.j * 16;
+                prefetch_l2(pg, 256);
+                prefetch_l2(pg + H / 8, 256);
+            }
+            pre.next(step);
+        }
+    }
+    grid_dependency_wait();
     Slice<WEIGHTED> in;
     in.clear();
     if (cur.u < units && cur.g < n_groups) in.load(x, w, cur.t, cur.j, k, H);
@@ -209,7 +223,8 @@ cudaError_t launch_layout(const void* x, const float* w, void* out, float* sf,
                                      (units + kWarps - 1) / kWarps);
     if (const cudaError_t e = upload_checks(stream)) return e;
     return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint4*>(x), w,
-                      static_cast<uint4*>(out), sf, lay, H, n_groups, n_walk, clamp);
+                      static_cast<uint4*>(out), sf, lay, H, n_groups, n_walk, clamp,
+                      prologue_prefetch_units(n_groups * 512));
 }
 
 template <int FMT, bool WEIGHTED, int CLAMP>

@@ -53,6 +53,18 @@ __device__ __forceinline__ void produce_tiles(uint8_t (*stage)[TILE_BYTES], uint
         mbar_wait_bounded(&full[k % STAGES], (k / STAGES) & 1u, nullptr, status);
 }
 
+// Called by the producer lane between grid_dependency_launch and
+// grid_dependency_wait: the boxes of the CTA's first STAGES tiles (those it
+// loads first) go to L2 while the grid before this one drains.
+template <int STAGES>
+__device__ __forceinline__ void prefetch_first_tiles(const CUtensorMap* tmap, uint32_t CB,
+                                                     uint32_t TB, int box_cols) {
+    int k = 0;
+    for (TileWalk tw(blockIdx.x, gridDim.x, CB); tw.row < TB && k < STAGES; tw.next(), ++k)
+        tma_prefetch_2d(tmap, static_cast<int>(tw.col) * box_cols,
+                        static_cast<int>(tw.row * 128));
+}
+
 // ---------------------------------------------------------------------------
 // In-place per-channel cast: 16 consumer warps, each holding an 8-token x
 // 4-channel block of a 128 x 128 tile (warp w: tokens 8w..8w+7, lane l:
@@ -96,7 +108,9 @@ __global__ void __launch_bounds__(kChThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
-    grid_dependency_sync();  // the previous grid on the stream is done
+    grid_dependency_launch();
+    if (warp == kChWarps && lane == 0) prefetch_first_tiles<kChStages>(&tmap, CB, TB, 128);
+    grid_dependency_wait();  // the previous grid on the stream is done
     if (warp == kChWarps) {
         if (lane == 0)
             produce_tiles<kChStages, kTileBytes>(sm.stage, sm.full, sm.empty, &sm.abort, &tmap, CB,
@@ -243,7 +257,10 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
-    grid_dependency_sync();  // the previous grid on the stream is done
+    grid_dependency_launch();
+    if (warp == kCtGroups * kCtGroupWarps && lane == 0)
+        prefetch_first_tiles<kCtStages>(&tmap, CB, TB, kCtTileCols);
+    grid_dependency_wait();  // the previous grid on the stream is done
 
     if (warp == kCtGroups * kCtGroupWarps) {   // producer
         if (lane == 0)
@@ -401,7 +418,10 @@ __global__ void __launch_bounds__(kCtThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
-    grid_dependency_sync();  // the previous grid on the stream is done
+    grid_dependency_launch();
+    if (warp == kCtGroups * kCtGroupWarps && lane == 0)
+        prefetch_first_tiles<kBgStages>(&tmap, CB, TB, 128);
+    grid_dependency_wait();  // the previous grid on the stream is done
 
     if (warp == kCtGroups * kCtGroupWarps) {   // producer
         if (lane == 0)

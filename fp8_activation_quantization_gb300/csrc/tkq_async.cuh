@@ -91,6 +91,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// L2 prefetch of the box a tma_load_2d at (x, y) would copy.  A hint that
+// changes no value any load returns, so, like prefetch_l2, it may be issued
+// before grid_dependency_wait.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Walk of a persistent CTA over a [rows x cols] grid of tiles (cols fastest):
 // tiles start, start + step, start + 2 step, ...  The row/column of each tile
 // is updated incrementally, so the loop needs no integer division.

@@ -88,9 +88,26 @@ __device__ __forceinline__ bool access_ok(const void* p, unsigned bytes, bool wr
 // scheduled (it will wait here in turn), then waits until the grid before it
 // has completed and its memory operations are visible.  Without a preceding
 // PDL launch the wait returns at once.
-__device__ __forceinline__ void grid_dependency_sync() {
+__device__ __forceinline__ void grid_dependency_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_sync() {
+    grid_dependency_launch();
+    grid_dependency_wait();
+}
+
+// A bulk prefetch of `bytes` bytes at p into L2 (p 16-byte aligned, bytes a
+// multiple of 16), issued by the calling thread alone.  A prefetch is a hint:
+// it changes no value that any load returns, so a kernel may issue it between
+// grid_dependency_launch and grid_dependency_wait, while the grid before it
+// still runs and may still be writing those bytes (its writes land in L2,
+// the point of coherence, after the prefetched lines or instead of them).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+    if (!access_ok(p, bytes, false)) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -45,13 +45,28 @@ CheckTable& host_check_table();
 // Persistent grid: min(blocks needed, SMs x resident blocks per SM).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
 
+// How many units of its walk each warp of a flat stream (token_cast.cu,
+// swiglu_flat.cu) sends to L2 before it waits for the grid before it: a
+// CTA of the next launch starts on an SM as soon as a CTA of the draining one
+// exits there, so these prefetches fill the DRAM time the drain leaves idle.
+// Measured back to back on one GB300: one unit took the plain cast of
+// [8192, 7168] from 29.44 to 29.15 us and the SwiGLU cast of [16384, 4096]
+// from 27.07 to 26.38 us, two units less (29.26, 26.57 us); on an input of a
+// few MB, where every warp has one or two units, prefetching them all took
+// the plain cast of [1024, 4096] from 3.67 to 2.67 us.
+inline int prologue_prefetch_units(int64_t input_bytes) {
+    return input_bytes <= (int64_t{16} << 20) ? 4 : 1;
+}
+
 // Launch of one of the library's casts, with programmatic dependent launch
 // allowed when `allow`: its grid may then be scheduled while the kernel before
 // it on the stream is still draining, once every CTA of that kernel has
 // started (the casts signal that at entry, grid_dependency_sync in
 // tkq_device.cuh).  Each cast waits there for the previous grid to complete,
-// its memory visible, before any global access, so what overlaps is the launch
-// and the CTAs' start-up, never data.  After a kernel that does not signal, or
+// its memory visible, before any global load or store.  What overlaps is the
+// launch, the CTAs' start-up and the L2 prefetches the flat streams issue
+// before that wait (prologue_prefetch_units), which change no value any load
+// returns.  After a kernel that does not signal, or
 // after a copy, the launch is ordered as usual.  Measured back to back, this
 // takes 2.5-3.5 % off the ~30 us flat casts and leaves the long TMA-ring casts
 // unchanged, but made the SwiGLU backward cast 3.5 % and the transposed

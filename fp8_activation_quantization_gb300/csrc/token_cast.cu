@@ -11,10 +11,10 @@
 // the T * C / 128 groups with no row or tile bookkeeping and no ragged edge:
 // a warp takes units of four consecutive groups (lane l: 16 consecutive
 // elements, eight lanes per group, the group absmax in three xor shuffles),
-// grid-stride over persistent CTAs of 256 threads (four per SM at <= 64
-// registers).  Each lane issues the global loads of its next unit before it
-// works on the current one, so two units per warp are in flight; a warp's
-// loads are 16-byte vectors covering 1 KB (bf16) or 2 KB (fp32) of
+// grid-stride over persistent CTAs of 256 threads (five per SM for bf16
+// input, four for fp32).  Each lane issues the global loads of its next unit
+// before it works on the current one, so two units per warp are in flight; a
+// warp's loads are 16-byte vectors covering 1 KB (bf16) or 2 KB (fp32) of
 // consecutive input, its code stores 16-byte vectors covering 512 B.
 // (A TMA ring in shared memory is not needed for this access pattern: the
 // flat stream measured 8-14 % faster than one on the same inputs.)
@@ -69,11 +69,23 @@ struct Slice {
 
 // n_groups = T * G groups hold data; n_walk >= n_groups groups are visited
 // (the column-major layouts' padding rows); G = C / 128 groups per row.
+// CTAs per SM: five (<= 48 registers) for bf16 input, four (<= 64) for fp32,
+// whose lanes hold twice the input bytes.  Measured back to back on
+// [8192, 7168] bf16, five took every option set from 29.1-29.4 us (four) to
+// 27.9-28.3 us: the extra warps keep more loads in flight, and the two
+// layouts that spill a few bytes at that cap gained as much as the rest.  Six
+// (<= 40 registers) spill 16-56 bytes per thread.
+template <bool F32>
+constexpr int ctas_per_sm() {
+    return F32 ? 4 : 5;
+}
+
 template <int FMT, bool F32, unsigned SFC>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<F32>())
     token_cast_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
-                      float* __restrict__ sf, SfLayout lay, int64_t n_groups, int64_t n_walk) {
-    grid_dependency_sync();  // the previous grid on the stream is done
+                      float* __restrict__ sf, SfLayout lay, int64_t n_groups, int64_t n_walk,
+                      int prefetch_units) {
+    grid_dependency_launch();
     // LAYOUT: the scales are not flat row-major fp32 (store_scale needs the
     // group's row and index in the row); a fixed option set's flags are
     // compile-time constants from here on
@@ -85,6 +97,18 @@ __global__ void __launch_bounds__(kThreads, 4)
     const int64_t units = (n_walk + 3) / 4;
     const int64_t step = static_cast<int64_t>(gridDim.x) * kWarps;
     int64_t u = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    // the warp's first prefetch_units (<= 4) units go to L2 while the grid
+    // before this one drains; then wait until it is done.  (A loop bounded by
+    // prefetch_units alone compiled the fp32 instance into one that ran
+    // 52.1 us instead of 48.3 us on [8192, 7168]; this unrolled form does not.)
+    constexpr unsigned kUnitBytes = 32 * Slice<F32>::kVecs * 16;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int64_t up = u + p * step;
+        if (p < prefetch_units && lane == 0 && up < units && up * 4 + 3 < n_groups)
+            prefetch_l2(x + up * 32 * Slice<F32>::kVecs, kUnitBytes);
+    }
+    grid_dependency_wait();
 
     // row and group-in-row of this lane's group, for the scale layouts: found
     // by one division here, then advanced by the fixed stride with one carry
@@ -158,8 +182,10 @@ cudaError_t launch_layout(const void* x, void* out, float* sf, const SfLayout& l
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kThreads, 0,
                                      (units + kWarps - 1) / kWarps);
     if (const cudaError_t e = upload_checks(stream)) return e;
+    const int64_t in_bytes = n_groups * 128 * (F32 ? 4 : 2);
     return launch_pdl(k, grid, kThreads, 0, stream, true, static_cast<const uint4*>(x),
-                      static_cast<uint4*>(out), sf, lay, n_groups, n_walk);
+                      static_cast<uint4*>(out), sf, lay, n_groups, n_walk,
+                      prologue_prefetch_units(in_bytes));
 }
 
 // The instance for the launch's flags: fixed option sets for no options, the
