@@ -519,8 +519,7 @@ cudaError_t launch_channel_t(const void* x, void* out, float* sf, int64_t T, int
     const int grid = persistent_grid(reinterpret_cast<const void*>(k), kCtThreads, smem,
                                      (n_tiles + 1) / 2);
     if (const cudaError_t e = upload_checks(stream)) return e;
-    // measured slower with programmatic dependent launch
-    return launch_pdl(k, grid, kCtThreads, smem, stream, false, map, static_cast<uint8_t*>(out),
+    return launch_pdl(k, grid, kCtThreads, smem, stream, true, map, static_cast<uint8_t*>(out),
                       sf, T, static_cast<int>(C), device_status_word());
 }
 

@@ -61,16 +61,17 @@ inline int prologue_prefetch_units(int64_t input_bytes) {
 // Launch of one of the library's casts, with programmatic dependent launch
 // allowed when `allow`: its grid may then be scheduled while the kernel before
 // it on the stream is still draining, once every CTA of that kernel has
-// started (the casts signal that at entry, grid_dependency_sync in
-// tkq_device.cuh).  Each cast waits there for the previous grid to complete,
-// its memory visible, before any global load or store.  What overlaps is the
-// launch, the CTAs' start-up and the L2 prefetches the flat streams issue
-// before that wait (prologue_prefetch_units), which change no value any load
-// returns.  After a kernel that does not signal, or
-// after a copy, the launch is ordered as usual.  Measured back to back, this
-// takes 2.5-3.5 % off the ~30 us flat casts and leaves the long TMA-ring casts
-// unchanged, but made the SwiGLU backward cast 3.5 % and the transposed
-// per-channel cast 1.7 % slower; their launchers pass allow = false.
+// started (the casts signal that at entry, grid_dependency_launch in
+// tkq_device.cuh).  Each cast then waits (grid_dependency_wait) for the
+// previous grid to complete, its memory visible, before any global load or
+// store.  What overlaps is the launch, the CTAs' start-up and the L2
+// prefetches the casts issue before that wait (prologue_prefetch_units and the
+// rings' first boxes), which change no value any load returns.  After a kernel
+// that does not signal, or after a copy, the launch is ordered as usual.
+// Measured back to back, this takes 2.5-3.5 % off the ~30 us flat casts and,
+// with the prefetches, 4.4 % off the transposed per-channel cast (56.5 to
+// 54.0 us); it made the SwiGLU backward cast slower (152.0 against 154.5 us
+// with the prefetches, 156.1 without), whose launcher passes allow = false.
 // Returns the launch's error.
 template <typename... Params, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int block, size_t smem,
