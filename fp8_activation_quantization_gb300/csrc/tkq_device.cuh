@@ -83,20 +83,18 @@ __device__ __forceinline__ bool access_ok(const void* p, unsigned bytes, bool wr
 // ---------------------------------------------------------------------------
 // programmatic dependent launch
 // ---------------------------------------------------------------------------
-// Called by every thread of a cast before its first global access (launched
-// by launch_pdl, tkq_internal.h): first lets the next grid on the stream be
-// scheduled (it will wait here in turn), then waits until the grid before it
-// has completed and its memory operations are visible.  Without a preceding
-// PDL launch the wait returns at once.
+// Every thread of a cast (launched by launch_pdl, tkq_internal.h) calls
+// grid_dependency_launch at entry, which lets the next grid on the stream be
+// scheduled (it waits in turn), and grid_dependency_wait before its first
+// global load or store, which returns once the grid before it has completed
+// and its memory operations are visible.  Between the two a cast issues only
+// L2 prefetches (prefetch_l2, tma_prefetch_2d).  Without a preceding PDL
+// launch the wait returns at once.
 __device__ __forceinline__ void grid_dependency_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_sync() {
-    grid_dependency_launch();
-    grid_dependency_wait();
 }
 
 // A bulk prefetch of `bytes` bytes at p into L2 (p 16-byte aligned, bytes a

@@ -137,3 +137,58 @@ def test_short_output_buffers_are_refused_before_launch(cuda_device):
                       out=torch.empty(256, 1024, dtype=torch.float32, device=cuda_device))
     torch.cuda.synchronize()
     assert torch.all(guard == 0xA5)
+
+
+def _chain_tiles(x0, w, rounds, sync):
+    """The tile, ring and backward casts chained the same way: per-channel
+    (transposed) -> cast back -> per-block -> cast back into the per-block
+    cast's own input -> SwiGLU cast (x weight) of that -> cast back -> SwiGLU
+    backward cast, then the in-place per-channel cast of x and its cast back
+    into x for the next round."""
+    x = x0.clone()
+    outs = []
+
+    def step():
+        if sync:
+            torch.cuda.synchronize()
+
+    for _ in range(rounds):
+        qt, st = tkq.per_channel_cast(x, transpose=True)            # reads x
+        step()
+        yt = tkq.cast_back(qt.view(torch.uint8), st, fmt="e4m3", group_size=(1, 128),
+                           out_dtype=torch.bfloat16)
+        step()
+        qb, sb = tkq.per_block_cast(yt)                              # reads yt
+        step()
+        tkq.cast_back(qb.view(torch.uint8), sb, fmt="e4m3", group_size=(128, 128),
+                      out_dtype=torch.bfloat16, out=yt)              # writes yt
+        step()
+        q2, s2 = tkq.swiglu_forward_and_per_token_cast(yt, topk_weights=w)
+        step()
+        dy = tkq.cast_back(q2.view(torch.uint8), s2, fmt="e4m3", group_size=(1, 128),
+                           out_dtype=torch.bfloat16)
+        step()
+        q3, s3 = tkq.swiglu_backward_and_per_token_cast(yt, dy, topk_weights=w)
+        step()
+        qc, sc = tkq.per_channel_cast(x)                             # reads x
+        step()
+        tkq.cast_back(qc.view(torch.uint8), sc, fmt="e4m3", group_size=(128, 1),
+                      out_dtype=torch.bfloat16, out=x)               # writes x
+        step()
+        outs += [t.view(torch.uint8).clone() if t.element_size() == 1 else t.clone()
+                 for t in (qt, st, qb, sb, q2, s2, q3, s3, qc, sc)]
+    outs.append(x.clone())
+    return outs
+
+
+def test_chained_tile_ring_and_backward_casts(cuda_device, swiglu_kernel):
+    """Every other cast in one unsynchronized chain, through both SwiGLU forward
+    kernels, against the same chain with a synchronization after each launch."""
+    x0 = to_dev_bf16(synth.outlier_bf16(95, 1, 512, 768, zero_row_every=0), cuda_device)
+    w = torch.rand(768, generator=torch.Generator().manual_seed(96)).to(cuda_device)
+    ref = _chain_tiles(x0, w, 3, sync=True)
+    for _ in range(10):
+        got = _chain_tiles(x0, w, 3, sync=False)
+        torch.cuda.synchronize()
+        _same(got, ref)
+    assert tkq.tkq_read_device_status() == 0
