@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                 if constexpr (MT::kClampBf16) {
                     // c is a bf16 value: clamp and count on the packed pairs
                     const uint32_t c2 = clamp.c2;
-                    __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);  // at most 16 a half
+                    uint32_t n2 = 0;  // at most 16 a half
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         clamp_pairs_bf16(gq[h].x, uq[h].x, c2, n2);

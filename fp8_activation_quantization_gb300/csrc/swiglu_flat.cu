@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
     Slice<WEIGHTED> in;
     in.clear();
     if (cur.u < units && cur.g < n_groups) in.load(x, w, cur.t, cur.j, k, H);
-    uint64_t n_clamped = 0;
+    uint32_t n_clamped = 0;
     while (cur.u < units) {
         const int64_t g = cur.g, t = cur.t;
         const int j = cur.j;
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, CLAMP == kClampF32 ? 3 : 4)
         uint32_t n = 0;
         if constexpr (CLAMP == kClampBf16) {
             // clamp and count on the packed pairs
-            __nv_bfloat162 n2 = __float2bfloat162_rn(0.0f);  // at most 16 a half
+            uint32_t n2 = 0;  // at most 16 a half
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 clamp_pairs_bf16(gq[h].x, uq[h].x, clamp.c2, n2);

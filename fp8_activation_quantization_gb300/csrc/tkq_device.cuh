@@ -461,13 +461,31 @@ __device__ __forceinline__ uint32_t as_word(__nv_bfloat162 v) {
 }
 
 // Clamps the gate pair g and the up pair u in place (c2 = bf16x2_bound(c))
-// and adds to each half of n the number of that half's two values (gate, up)
-// the clamp changed: the not-equal compares give 1.0 or 0.0 per half and are
-// summed in bf16, which is exact for counts up to 256 (callers convert n with
-// clamped_total before it could exceed that).  The up clamp is one
+// and counts the values the clamp changed into n.  The up clamp is one
 // min.xorsign.abs: magnitude min(|u|, c), sign of u xor sign of c (+), which
 // is clamp(u, -c, c) for every u that is not NaN, signed zeros and infinities
-// included.
+// included.  The count: each not-equal compare gives a 32-bit mask with
+// 0xFFFF in every half whose value changed, and n adds both masks (one
+// three-input integer add).  Modulo 2^32 a low-half mask is 2^16 - 1 and a
+// high-half mask -2^16, so n = 2^16 (L - H) - L for L low-half and H
+// high-half changes; clamped_total recovers L + H while both stay below 2^15
+// (callers convert n after at most 16 pairs).
+__device__ __forceinline__ void clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint32_t c2,
+                                                 uint32_t& n) {
+    const __nv_bfloat162 gc = __hmin2(as_bf162(g), as_bf162(c2));
+    const uint32_t gw = as_word(gc);
+    uint32_t uw, mg, mu;
+    asm("min.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(uw) : "r"(u), "r"(c2));
+    asm("set.ne.u32.bf16x2 %0, %1, %2;" : "=r"(mg) : "r"(g), "r"(gw));
+    asm("set.ne.u32.bf16x2 %0, %1, %2;" : "=r"(mu) : "r"(u), "r"(uw));
+    n += mg + mu;
+    g = gw;
+    u = uw;
+}
+
+// The same clamp with the count kept as two bf16 halves (each compare gives
+// 1.0 or 0.0 per half, summed exactly up to 256); the transposed cast uses
+// this form, measured faster there than the integer count.
 __device__ __forceinline__ void clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint32_t c2,
                                                  __nv_bfloat162& n) {
     const __nv_bfloat162 gb = as_bf162(g), ub = as_bf162(u);
@@ -480,10 +498,16 @@ __device__ __forceinline__ void clamp_pairs_bf16(uint32_t& g, uint32_t& u, uint3
     n = __hadd2(n, __hne2(gb, gc));
     n = __hadd2(n, __hne2(ub, uc));
 }
-
-// The total of a clamp_pairs_bf16 count pair (two small integers, exact).
 __device__ __forceinline__ uint32_t clamped_total(__nv_bfloat162 n) {
     return static_cast<uint32_t>(__low2float(n) + __high2float(n));
+}
+
+// The number of changes a clamp_pairs_bf16 count n holds: L = -n mod 2^16,
+// L - H = (n + L) / 2^16 as a signed value, L + H = 2 L - (L - H).
+__device__ __forceinline__ uint32_t clamped_total(uint32_t n) {
+    const uint32_t lo = (0u - n) & 0xFFFFu;
+    const int32_t diff = static_cast<int32_t>(n + lo) >> 16;
+    return 2u * lo - static_cast<uint32_t>(diff);
 }
 
 // Gradient of y = silu(g) * u with respect to g and u, scaled by the upstream
