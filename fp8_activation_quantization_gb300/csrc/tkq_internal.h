@@ -46,14 +46,15 @@ CheckTable& host_check_table();
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t blocks_needed);
 
 // How many units of its walk each warp of a flat stream (token_cast.cu,
-// swiglu_flat.cu) sends to L2 before it waits for the grid before it: a
-// CTA of the next launch starts on an SM as soon as a CTA of the draining one
-// exits there, so these prefetches fill the DRAM time the drain leaves idle.
-// Measured back to back on one GB300: one unit took the plain cast of
-// [8192, 7168] from 29.44 to 29.15 us and the SwiGLU cast of [16384, 4096]
-// from 27.07 to 26.38 us, two units less (29.26, 26.57 us); on an input of a
-// few MB, where every warp has one or two units, prefetching them all took
-// the plain cast of [1024, 4096] from 3.67 to 2.67 us.
+// swiglu_flat.cu), or each CTA of cast back, sends to L2 before it waits for
+// the grid before it: a CTA of the next launch starts on an SM as soon as a
+// CTA of the draining one exits there, so these prefetches fill the DRAM time
+// the drain leaves idle.  Measured back to back on one GB300 (four CTAs per
+// SM for the plain cast): one unit took the plain cast of [8192, 7168] from
+// 29.44 to 29.15 us and the SwiGLU cast of [16384, 4096] from 27.07 to
+// 26.38 us, two units less (29.26, 26.57 us); on an input of a few MB, where
+// every warp has one or two units, prefetching them all took the plain cast of
+// [1024, 4096] from 3.67 to 2.7-2.8 us.
 inline int prologue_prefetch_units(int64_t input_bytes) {
     return input_bytes <= (int64_t{16} << 20) ? 4 : 1;
 }
